@@ -1,0 +1,13 @@
+"""fp64 CPU oracle for ring attention's chunked forward pass.
+
+TEST INFRASTRUCTURE ONLY: imported by tests/, __graft_entry__.smoke() and the
+CPU legs of bench.py, never by the library. See ``oracle.attention``.
+"""
+from .attention import (NEG_INF, attention_rows, chunk_stats, full_attention,
+                        merge_stats, normalize, ring_attention, ring_order,
+                        unmasked_pairs)
+from . import layouts
+
+__all__ = ["NEG_INF", "attention_rows", "chunk_stats", "full_attention",
+           "merge_stats", "normalize", "ring_attention", "ring_order",
+           "unmasked_pairs", "layouts"]

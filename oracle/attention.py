@@ -1,0 +1,239 @@
+"""Plain fp64 CPU oracle for the chunked (ring) forward pass of softmax attention.
+
+TEST INFRASTRUCTURE. Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU
+legs of ``bench.py`` (``cpu_baseline`` and ``--impl reference``) may import or
+run anything in this package. The library's product path (the CUDA kernels,
+the C ABI and the Python binding) never imports it, and it never imports the
+library: the two share no code. Inputs come in as plain arrays; every value is
+upcast exactly to float64 before any arithmetic.
+
+Sources (web pages; cited by title and section):
+
+* [EX]  Ring-attention exercise page "systems-distributed-ring-attention-online-
+        softmax": task statement (the three functions, their outputs, the
+        invariance "for any way of splitting ... even chunks of size 1") and
+        its two hints (max subtraction; the exp(own_max - new_max) rescale).
+* [BLOG] "Ring Attention: Distributed Reads with Online Softmax":
+        sections "Partition the sequence across devices", "Do not average
+        independently normalized shard outputs", "A simple forward schedule",
+        "Causal masks depend on global positions", "Try it".
+* [GLOS] Glossary entry "ring attention": algorithm steps (1)-(6) and the
+        "Online softmax" paragraph.
+
+Conventions (readings of what the pages leave open; each is listed in the
+design notes):
+
+* q: [B, Hq, Sq, D]; k, v: [B, Hkv, Sk, D]; Hq % Hkv == 0 and query head h
+  reads key/value head h // (Hq // Hkv) (grouped heads; the pages do not
+  discuss head sharing, this is the plainest grouping).
+* Scores are s_ij = scale * <q_i, k_j>; the returned row max m is in those
+  scaled, natural-log units, and l = sum_j exp(s_ij - m).
+* Causal: key j is visible to query i iff pos_k[j] <= pos_q[i], with GLOBAL
+  positions ([BLOG] "Causal masks depend on global positions").
+* A row that sees no key has u = 0, l = 0, m = -inf, and its output is 0.
+  In a merge a side with m = -inf contributes nothing (no exp(-inf + inf)).
+"""
+from __future__ import annotations
+
+import numpy as np
+
+NEG_INF = -np.inf
+
+
+def _f64(x):
+    return np.asarray(x, dtype=np.float64)
+
+
+def _visible(q_pos, k_pos, causal):
+    """Boolean [Sq, Sk] visibility matrix from global positions.
+
+    [BLOG] "Causal masks depend on global positions": a query may not read a
+    key that lies in its future, judged by global position, not by local
+    row/column index.
+    """
+    q_pos = np.asarray(q_pos, dtype=np.int64)
+    k_pos = np.asarray(k_pos, dtype=np.int64)
+    if not causal:
+        return np.ones((q_pos.shape[0], k_pos.shape[0]), dtype=bool)
+    return k_pos[None, :] <= q_pos[:, None]
+
+
+def _head_group(Hq, Hkv):
+    if Hkv <= 0 or Hq % Hkv != 0:
+        raise ValueError(f"Hq={Hq} must be a positive multiple of Hkv={Hkv}")
+    return Hq // Hkv
+
+
+def chunk_stats(q, k, v, q_pos, k_pos, causal, scale):
+    """Statistics of one key/value chunk, computed as if it were the only one.
+
+    [EX] task statement: returns (chunk_output, chunk_sum, chunk_max) = the
+    un-normalised weighted value sum u, the un-normalised softmax denominator
+    l, and the row-wise max score m. [EX] first hint: the same max-subtraction
+    as scaled dot-product attention, with numerator and denominator returned
+    separately instead of divided.
+
+    Returns u [B, Hq, Sq, D], l [B, Hq, Sq], m [B, Hq, Sq] (float64).
+    """
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, Hq, Sq, D = q.shape
+    Hkv, Sk = k.shape[1], k.shape[2]
+    g = _head_group(Hq, Hkv)
+    vis = _visible(q_pos, k_pos, causal)
+    u = np.zeros((B, Hq, Sq, v.shape[3]))
+    l = np.zeros((B, Hq, Sq))
+    m = np.full((B, Hq, Sq), NEG_INF)
+    if Sk == 0 or Sq == 0:
+        return u, l, m
+    for b in range(B):
+        for h in range(Hq):
+            kh, vh = k[b, h // g], v[b, h // g]
+            s = scale * (q[b, h] @ kh.T)                  # [Sq, Sk] scores
+            s = np.where(vis, s, NEG_INF)
+            mrow = s.max(axis=1)                          # -inf if nothing visible
+            shift = np.where(np.isfinite(mrow), mrow, 0.0)
+            w = np.exp(s - shift[:, None])                # exp(-inf) = 0
+            u[b, h] = w @ vh
+            l[b, h] = w.sum(axis=1)
+            m[b, h] = mrow
+    return u, l, m
+
+
+def merge_stats(acc, new):
+    """Online-softmax merge of two sets of statistics.
+
+    [EX] task statement and second hint: the shared max is
+    max(acc_max, chunk_max); BOTH sides are multiplied by
+    exp(own_max - new_max) before their numerators and denominators are added;
+    stats relative to different maxes are never added directly.
+    [BLOG] "Do not average ...": keep m, l and u per shard and merge them.
+
+    A side whose max is -inf (it saw no key) contributes zero.
+    """
+    u1, l1, m1 = (_f64(x) for x in acc)
+    u2, l2, m2 = (_f64(x) for x in new)
+    m = np.maximum(m1, m2)
+    with np.errstate(invalid="ignore"):
+        a1 = np.where(m1 == NEG_INF, 0.0, np.exp(m1 - m))
+        a2 = np.where(m2 == NEG_INF, 0.0, np.exp(m2 - m))
+    u = a1[..., None] * u1 + a2[..., None] * u2
+    l = a1 * l1 + a2 * l2
+    return u, l, m
+
+
+def normalize(u, l):
+    """Final output u / l ([BLOG] "A simple forward schedule", last step).
+
+    A row with l == 0 saw no key; its output is 0 (a reading: the pages do
+    not define it).
+    """
+    u, l = _f64(u), _f64(l)
+    with np.errstate(invalid="ignore", divide="ignore"):
+        o = np.where(l[..., None] > 0, u / np.where(l > 0, l, 1.0)[..., None], 0.0)
+    return o
+
+
+def full_attention(q, k, v, q_pos, k_pos, causal, scale):
+    """Ordinary softmax attention over the whole key/value sequence at once.
+
+    This is the plain definition the chunked method must equal exactly ([EX]
+    task statement: "the exact same result as computing ordinary attention over
+    the full, concatenated key/value sequence"). Per row: m = max of visible
+    scaled scores, l = sum exp(s - m), O = sum exp(s - m) v / l.
+
+    Returns O [B, Hq, Sq, D], m [B, Hq, Sq], l [B, Hq, Sq].
+    """
+    u, l, m = chunk_stats(q, k, v, q_pos, k_pos, causal, scale)
+    return normalize(u, l), m, l
+
+
+def ring_order(rank, world):
+    """Chunk visited by device ``rank`` at each ring step.
+
+    [BLOG] "Partition the sequence across devices": each device sends its
+    shard to the next device and receives one from its predecessor, so at step
+    s device r holds the shard that started on device (r - s) mod P.
+    [GLOS] algorithm steps (1)-(5): step 0 is the device's own chunk.
+    """
+    return [(rank - s) % world for s in range(world)]
+
+
+def ring_attention(q, k_chunks, v_chunks, q_pos, k_pos_chunks, causal, scale,
+                   order=None):
+    """The pages' chunked algorithm, written out: stats per chunk + merges.
+
+    [EX] task statement: visit key/value chunks one at a time, never forming
+    the full attention matrix. [BLOG] "A simple forward schedule": initialise
+    a running summary, for each shard compute its contribution and merge it,
+    finally normalise u / l. ``order`` lists the chunk indices to visit
+    (default: index order). Returns O, m, l like ``full_attention``.
+
+    This second path exists to check the pages' claims against the definition
+    (chunk invariance, merge correctness); parity tests of the CUDA path
+    compare against ``full_attention`` / ``attention_rows``.
+    """
+    q = _f64(q)
+    B, Hq, Sq, _ = q.shape
+    D = _f64(v_chunks[0]).shape[3] if len(v_chunks) else q.shape[3]
+    acc = (np.zeros((B, Hq, Sq, D)), np.zeros((B, Hq, Sq)),
+           np.full((B, Hq, Sq), NEG_INF))
+    if order is None:
+        order = range(len(k_chunks))
+    for c in order:
+        st = chunk_stats(q, k_chunks[c], v_chunks[c], q_pos, k_pos_chunks[c],
+                         causal, scale)
+        acc = merge_stats(acc, st)
+    u, l, m = acc
+    return normalize(u, l), m, l
+
+
+def attention_rows(q, k, v, q_pos, k_pos, causal, scale, rows):
+    """The definition of ``full_attention`` evaluated for selected rows only.
+
+    ``rows`` is a list of (b, h, i) triples. Each row is computed on its own,
+    exactly against all of its visible keys, so that sampled rows of very long
+    sequences can be checked without forming [Sq, Sk] matrices. Inputs may be
+    any array type convertible to float64 (per head slices are upcast lazily).
+
+    Returns arrays O [R, D], m [R], l [R] in the order of ``rows``.
+    """
+    rows = list(rows)
+    Hq = q.shape[1]
+    Hkv = k.shape[1]
+    g = _head_group(Hq, Hkv)
+    k_pos = np.asarray(k_pos, dtype=np.int64)
+    q_pos = np.asarray(q_pos, dtype=np.int64)
+    D = v.shape[3]
+    O = np.zeros((len(rows), D))
+    M = np.full(len(rows), NEG_INF)
+    L = np.zeros(len(rows))
+    by_head = {}
+    for idx, (b, h, i) in enumerate(rows):
+        by_head.setdefault((b, h // g), []).append((idx, h, i))
+    for (b, hk), items in by_head.items():
+        kh = _f64(k[b, hk])
+        vh = _f64(v[b, hk])
+        for idx, h, i in items:
+            qi = _f64(q[b, h, i])
+            s = scale * (kh @ qi)                          # [Sk]
+            if causal:
+                s = np.where(k_pos <= q_pos[i], s, NEG_INF)
+            if s.size == 0 or not np.isfinite(s.max()):
+                continue                                   # nothing visible
+            mi = s.max()
+            w = np.exp(s - mi)
+            L[idx] = w.sum()
+            M[idx] = mi
+            O[idx] = (w @ vh) / L[idx]
+    return O, M, L
+
+
+def unmasked_pairs(q_pos, k_pos, causal):
+    """Exact number of visible (query, key) pairs: the work a causal mask
+    leaves ([BLOG] "Separate local compute from network traffic": attention
+    arithmetic counts query-key pairs)."""
+    q_pos = np.sort(np.asarray(q_pos, dtype=np.int64))
+    k_pos = np.sort(np.asarray(k_pos, dtype=np.int64))
+    if not causal:
+        return int(q_pos.size) * int(k_pos.size)
+    return int(np.searchsorted(k_pos, q_pos, side="right").sum())
