@@ -1,0 +1,379 @@
+"""Benchmark of the ring-attention forward pass (one JSON line on stdout).
+
+A step is one ``ra_ring_attention`` call: the whole chunk walk (stats, merges,
+normalisation) over one batch of synthetic inputs resident in HBM. Default
+workload: bf16, 8 heads, 8192 queries = 8192 keys, head_dim 128, non-causal,
+8 contiguous chunks of 1024 walked in ring order by 8 query segments.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                  [--layout contiguous|zigzag|striped] [--impl reference]
+
+N > 1 (under torchrun): every rank runs its own replica of the workload on its
+own GPU (the path shards by query segment with no data exchange on one box);
+the time is the max over ranks and the value counts every rank's work.
+``--impl reference`` times the fp64 CPU oracle instead, on a bounded row
+sample of the same workload, on this machine's host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "ring_attention fwd TFLOP/s (bf16, causal-adjusted) and % of GB300 tensor peak"
+L2_FLUSH_BYTES = 512 << 20  # > 129 MB L2
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return float(pk["bf16_tflops"]), float(pk.get("bf16_tflops_sustained", pk["bf16_tflops"])), \
+            float(pk["hbm_gbs"]), "measured"
+    except Exception:
+        return 1900.0, 1700.0, 6800.0, "fallback"
+
+
+def _traffic(kernel_key):
+    """DRAM bytes per launch from a committed ncu summary, valid only while the
+    kernel source is unchanged (its hash is stored next to the counters)."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            tab = json.load(f)
+        ent = tab[kernel_key]
+        src = os.path.join(ROOT, "blockwise_attention_online_gb300", "csrc", ent["source"])
+        with open(src, "rb") as f:
+            h = hashlib.sha256(f.read()).hexdigest()[:16]
+        return int(ent["bytes_per_launch"]) if h == ent["source_sha"] else None
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the timed region runs."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                self.out = ""
+
+    def summary(self):
+        sms, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in (self.out or "").splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sms.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, val in zip(names, f[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(n)
+        if not sms:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sms), "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sms)}
+
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def build_workload(name, layout, device):
+    import torch
+    from blockwise_attention_online_gb300 import layouts, workloads
+    w = workloads.WORKLOADS[name]
+    if layout:
+        w = workloads.Workload(**{**w.__dict__, "layout": layout})
+    q, k, v = workloads.make_qkv(w, device=device)
+    P = w.n_chunks
+    rs = layouts.rank_spans(w.layout, w.S, P)
+    kc = layouts.shard(k, w.layout, P)
+    vc = layouts.shard(v, w.layout, P)
+    qs = torch.cat(layouts.shard(q, w.layout, P), dim=2).contiguous()
+    del q, k, v
+    segs = [(w.S // P, s) for s in rs]
+    return w, qs, kc, vc, rs, segs
+
+
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+    from blockwise_attention_online_gb300 import device_status, ring_attention
+
+    world, rank, local = _dist()
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+
+    w, qs, kc, vc, rs, segs = build_workload(args.workload, args.layout, dev)
+    flops = w.flops()
+    out = torch.empty_like(qs)
+    m = torch.empty(qs.shape[:3], device=dev, dtype=torch.float32)
+    l = torch.empty_like(m)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, device=dev, dtype=torch.float32)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        ring_attention(qs, kc, vc, chunk_spans=rs, q_segments=segs, causal=w.causal,
+                       out=out, m=m, l=l)
+
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        step()
+    torch.cuda.synchronize()
+    device_status()
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index) as clk:
+        for i in range(args.steps):
+            flush.fill_(float(i & 7))       # evict the previous step's data from L2
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    device_status()
+    times = [s.elapsed_time(e) for s, e in zip(starts, ends)]  # ms per launch
+    total_ms = sum(times)
+    t = torch.tensor([total_ms], device=dev, dtype=torch.float64)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    max_ms = float(t.item())
+    value = flops * args.steps * world / (max_ms * 1e-3) / 1e12
+
+    # end to end through the public call: pinned host inputs -> device -> host
+    e2e = None
+    if not args.no_e2e:
+        hq = qs.cpu().pin_memory()
+        hk = [x.cpu().pin_memory() for x in kc]
+        hv = [x.cpu().pin_memory() for x in vc]
+        ho = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        hm = torch.empty(m.shape, dtype=torch.float32).pin_memory()
+        hl = torch.empty(l.shape, dtype=torch.float32).pin_memory()
+        dq = torch.empty_like(qs)
+        dk = [torch.empty_like(x) for x in kc]
+        dv = [torch.empty_like(x) for x in vc]
+        h2d = hq.numel() * hq.element_size() + sum(x.numel() * x.element_size() for x in hk + hv)
+        d2h = ho.numel() * ho.element_size() + hm.numel() * 4 + hl.numel() * 4
+        n_e2e = max(3, min(args.steps, 50))
+
+        def e2e_step():
+            dq.copy_(hq, non_blocking=True)
+            for a, b in zip(dk, hk):
+                a.copy_(b, non_blocking=True)
+            for a, b in zip(dv, hv):
+                a.copy_(b, non_blocking=True)
+            ring_attention(dq, dk, dv, chunk_spans=rs, q_segments=segs, causal=w.causal,
+                           out=out, m=m, l=l)
+            ho.copy_(out, non_blocking=True)
+            hm.copy_(m, non_blocking=True)
+            hl.copy_(l, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        t0 = time.perf_counter()
+        for _ in range(n_e2e):
+            e2e_step()
+        torch.cuda.synchronize()
+        el = time.perf_counter() - t0
+        te = torch.tensor([el], device=dev, dtype=torch.float64)
+        if world > 1:
+            dist.all_reduce(te, op=dist.ReduceOp.MAX)
+        el = float(te.item())
+        e2e = {"value": round(flops * n_e2e * world / el / 1e12, 3), "unit": "TFLOP/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "steps": n_e2e}
+        device_status()
+
+    if world > 1:
+        dist.destroy_process_group()
+    if rank != 0:
+        return None
+
+    peak_b, peak_s, hbm, src = _peaks()
+    mean_ms = total_ms / args.steps
+    achieved = flops / (mean_ms * 1e-3) / 1e12
+    kernel_key = f"tc_ring_kernel:{w.name}:{w.layout}"
+    line = {
+        "metric": METRIC,
+        "value": round(value, 3),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(max_ms / args.steps, 6),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic: seeded N(0,1) Q/K/V (bf16), no dataset",
+        "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "S": w.S,
+                   "D": w.D, "causal": w.causal, "chunks": w.n_chunks, "layout": w.layout,
+                   "ring_order": "segment r visits chunks r, r-1, ...",
+                   "flops_per_step": flops,
+                   "l2": f"flushed before every step ({L2_FLUSH_BYTES >> 20} MiB write)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "pct_of_peak": round(100 * value / world / peak_b, 2),
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 3), "peak": peak_b,
+                     "unit": "TFLOP/s", "frac": round(achieved / peak_b, 4),
+                     "traffic": _traffic(kernel_key), "kernel": "tc_ring_kernel<128>",
+                     "peak_source": f"{src} bf16 burst (MEASURED_PEAKS.json)" if src == "measured"
+                     else "fallback 1.9 PFLOP/s"},
+        "clocks": clk.summary(),
+        "gpu_launches": args.steps,
+        "e2e": e2e,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
+    return line
+
+
+def _oracle_sample(w, rows_per_head, seed=1234):
+    import numpy as np
+    from blockwise_attention_online_gb300 import workloads
+    q, k, v = workloads.make_qkv(w, device="cpu")
+    rng = np.random.default_rng(seed)
+    heads = list(range(w.Hq))
+    return q.float(), k.float(), v.float(), heads, rng
+
+
+def _row_flops(w, i):
+    keys = (i + 1) if w.causal else w.S
+    return 4.0 * keys * w.D
+
+
+def cpu_baseline(w, seconds):
+    """The fp64 oracle, as it stands, on a bounded sample of the workload's
+    rows, timed on this machine's host cores."""
+    import numpy as np
+    import oracle
+    q, k, v, heads, rng = _oracle_sample(w, 0)
+    pos = np.arange(w.S)
+    done_flops, rows_done, el = 0.0, 0, 0.0
+    t0 = time.perf_counter()
+    while el < seconds:
+        rows = [(0, int(h), int(rng.integers(0, w.S))) for h in heads]
+        oracle.attention_rows(q, k, v, pos, pos, w.causal, w.scale, rows)
+        done_flops += sum(_row_flops(w, i) for _, _, i in rows)
+        rows_done += len(rows)
+        el = time.perf_counter() - t0
+    return {"value": round(done_flops / el / 1e12, 6), "unit": "TFLOP/s",
+            "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{rows_done} random query rows (one per head per round) of {w.name}, "
+                      f"each exact against all its visible keys, {el:.1f} s"}
+
+
+def run_reference(args):
+    """--impl reference: the fp64 oracle on the host cores, K timed steps, each
+    a bounded row sample (one random row per query head) of the workload."""
+    import numpy as np
+    import oracle
+    from blockwise_attention_online_gb300 import workloads
+    world, rank, _ = _dist()
+    if rank != 0:
+        return None
+    w = workloads.WORKLOADS[args.workload]
+    q, k, v, heads, rng = _oracle_sample(w, 0)
+    pos = np.arange(w.S)
+
+    def one():
+        rows = [(0, int(h), int(rng.integers(0, w.S))) for h in heads]
+        oracle.attention_rows(q, k, v, pos, pos, w.causal, w.scale, rows)
+        return sum(_row_flops(w, i) for _, _, i in rows)
+
+    for _ in range(args.warmup):
+        one()
+    t0 = time.perf_counter()
+    fl = 0.0
+    for _ in range(args.steps):
+        fl += one()
+    el = time.perf_counter() - t0
+    val = fl / el / 1e12
+    sample = f"{len(heads)} random query rows per step (one per head) of {w.name}"
+    return {"impl": "reference", "metric": METRIC, "value": round(val, 6), "unit": "TFLOP/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(el * 1e3 / args.steps, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic: seeded N(0,1) Q/K/V (bf16 values upcast to f64)",
+            "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "S": w.S,
+                       "D": w.D, "causal": w.causal, "chunks": w.n_chunks},
+            "cpu_baseline": {"value": round(val, 6), "unit": "TFLOP/s", "cores": os.cpu_count(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(val, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default="bf16_8k")
+    ap.add_argument("--layout", default=None)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        line = run_reference(args)
+    else:
+        line = run_gpu(args)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

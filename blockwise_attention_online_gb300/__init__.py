@@ -1,1 +1,11 @@
-"""GB300-native chunked (ring) attention forward: C-ABI CUDA library + binding."""
+"""GB300-native chunked (ring) attention forward: a C-ABI CUDA library
+(``_build/libra.so``, sources in ``csrc/``, header ``include/ra.h``) and a thin
+torch binding. The binding loads the library on first use and raises if it
+has not been built; there is no CPU fallback.
+"""
+from .api import (chunk_stats, default_scale, device_status, merge_stats,
+                  ring_attention, segment_work)
+from ._lib import RaError
+
+__all__ = ["chunk_stats", "default_scale", "device_status", "merge_stats",
+           "ring_attention", "segment_work", "RaError"]

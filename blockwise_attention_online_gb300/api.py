@@ -1,0 +1,197 @@
+"""Torch-facing binding of the C ABI: same operations, tensors in and out.
+
+Only argument marshalling happens here (pointers, strides, spans, the current
+CUDA stream). Every step of the computation runs in the library's kernels;
+PyTorch provides device memory and streams.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+
+import torch
+
+from . import _lib
+from ._lib import KvChunk, Problem, QSegment, Strides, check, load, positions
+
+Span = tuple  # (len, pos0, step)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return _lib.RA_BF16
+    if t.dtype == torch.float32:
+        return _lib.RA_F32
+    raise TypeError(f"unsupported dtype {t.dtype}: use bfloat16 or float32")
+
+
+def _strides(t: torch.Tensor) -> Strides:
+    if t.dim() != 4:
+        raise ValueError("tensors are [batch, head, row, head_dim]")
+    if t.shape[3] > 1 and t.stride(3) != 1:
+        raise ValueError("head_dim must be contiguous")
+    return Strides(t.stride(0), t.stride(1), t.stride(2))
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check_cuda(t: torch.Tensor, what: str):
+    if not t.is_cuda:
+        raise ValueError(f"{what} must be a CUDA tensor")
+
+
+def _segments(q: torch.Tensor, q_segments):
+    Sq = q.shape[2]
+    if q_segments is None:
+        q_segments = [(Sq, [(Sq, 0, 1)])]
+    arr = (QSegment * max(1, len(q_segments)))()
+    for i, (ln, spans) in enumerate(q_segments):
+        arr[i].len = int(ln)
+        arr[i].pos = positions(spans)
+    return arr, len(q_segments)
+
+
+def _chunks(k_chunks, v_chunks, chunk_spans):
+    if len(k_chunks) != len(v_chunks):
+        raise ValueError("need as many value chunks as key chunks")
+    if chunk_spans is None:
+        chunk_spans, p = [], 0
+        for k in k_chunks:
+            chunk_spans.append([(k.shape[2], p, 1)])
+            p += k.shape[2]
+    arr = (KvChunk * max(1, len(k_chunks)))()
+    for i, (k, v) in enumerate(zip(k_chunks, v_chunks)):
+        _check_cuda(k, "k"); _check_cuda(v, "v")
+        if k.shape != v.shape:
+            raise ValueError("k and v chunks must have the same shape")
+        arr[i].k = k.data_ptr()
+        arr[i].v = v.data_ptr()
+        arr[i].len = k.shape[2]
+        arr[i].k_strides = _strides(k)
+        arr[i].v_strides = _strides(v)
+        arr[i].pos = positions(chunk_spans[i])
+    return arr, len(k_chunks)
+
+
+def _problem(q, Hkv, causal, scale, out_strides):
+    B, Hq, Sq, D = q.shape
+    pb = Problem()
+    pb.B, pb.Hq, pb.Hkv, pb.D, pb.Sq = B, Hq, Hkv, D, Sq
+    pb.dtype = _dtype_code(q)
+    pb.causal = 1 if causal else 0
+    pb.scale = float(scale) if scale is not None else 0.0
+    pb.reserved = 0
+    pb.q_strides = _strides(q)
+    pb.o_strides = out_strides
+    return pb
+
+
+def ring_attention(q, k_chunks, v_chunks, *, chunk_spans=None, q_segments=None,
+                   causal=False, scale=None, out=None, m=None, l=None, stream=None):
+    """Chunked forward pass over key/value chunks (one persistent kernel).
+
+    q: [B, Hq, Sq, D] (bf16 or fp32, CUDA). k_chunks / v_chunks: lists of
+    [B, Hkv, len_c, D]. chunk_spans[c]: global positions of chunk c as spans
+    (default: the chunks concatenated in list order from position 0).
+    q_segments: list of (len, spans) splitting Q's rows (default: one segment
+    at positions 0..Sq-1); with as many segments as chunks, segment r walks
+    the chunks in ring order starting at chunk r.
+    Returns (O [B, Hq, Sq, D] like q, m [B, Hq, Sq] fp32, l [B, Hq, Sq] fp32).
+    """
+    lib = load()
+    _check_cuda(q, "q")
+    B, Hq, Sq, D = q.shape
+    Hkv = k_chunks[0].shape[1] if k_chunks else Hq
+    if out is None:
+        out = torch.empty_like(q)
+    if m is None:
+        m = torch.empty(B, Hq, Sq, device=q.device, dtype=torch.float32)
+    if l is None:
+        l = torch.empty(B, Hq, Sq, device=q.device, dtype=torch.float32)
+    pb = _problem(q, Hkv, causal, scale, _strides(out))
+    segs, nsegs = _segments(q, q_segments)
+    chs, nch = _chunks(k_chunks, v_chunks, chunk_spans)
+    check(lib.ra_ring_attention(ctypes.byref(pb), q.data_ptr(), segs, nsegs, chs, nch,
+                                out.data_ptr(), m.data_ptr(), l.data_ptr(), _stream(stream)))
+    return out, m, l
+
+
+def chunk_stats(q, k, v, *, spans=None, q_segments=None, causal=False, scale=None,
+                u=None, l=None, m=None, stream=None):
+    """(u, l, m) of one key/value chunk, as if it were the only one.
+
+    u: [B, Hq, Sq, D] fp32 un-normalised numerator; l, m: [B, Hq, Sq] fp32.
+    spans: global positions of the chunk's rows (default 0..len-1).
+    """
+    lib = load()
+    _check_cuda(q, "q")
+    B, Hq, Sq, D = q.shape
+    if u is None:
+        u = torch.empty(B, Hq, Sq, D, device=q.device, dtype=torch.float32)
+    if l is None:
+        l = torch.empty(B, Hq, Sq, device=q.device, dtype=torch.float32)
+    if m is None:
+        m = torch.empty(B, Hq, Sq, device=q.device, dtype=torch.float32)
+    pb = _problem(q, k.shape[1], causal, scale, _strides(u))
+    segs, nsegs = _segments(q, q_segments)
+    chs, _ = _chunks([k], [v], None if spans is None else [spans])
+    check(lib.ra_chunk_stats(ctypes.byref(pb), q.data_ptr(), segs, nsegs, chs,
+                             u.data_ptr(), l.data_ptr(), m.data_ptr(), _stream(stream)))
+    return u, l, m
+
+
+def merge_stats(u_acc, l_acc, m_acc, u_new, l_new, m_new, stream=None):
+    """In-place online-softmax merge of (u_new, l_new, m_new) into the accumulator."""
+    lib = load()
+    for t in (u_acc, l_acc, m_acc, u_new, l_new, m_new):
+        _check_cuda(t, "stats")
+        if t.dtype != torch.float32 or not t.is_contiguous():
+            raise ValueError("statistics must be contiguous fp32 tensors")
+    D = u_acc.shape[-1]
+    rows = u_acc.numel() // D
+    if u_new.numel() != u_acc.numel() or l_acc.numel() != rows or m_acc.numel() != rows \
+            or l_new.numel() != rows or m_new.numel() != rows:
+        raise ValueError("shape mismatch between the two sets of statistics")
+    check(lib.ra_merge_stats(rows, D, u_acc.data_ptr(), l_acc.data_ptr(), m_acc.data_ptr(),
+                             u_new.data_ptr(), l_new.data_ptr(), m_new.data_ptr(),
+                             _stream(stream)))
+    return u_acc, l_acc, m_acc
+
+
+def segment_work(B, Hq, Hkv, D, q_segments, chunk_lens, chunk_spans, causal, dtype=_lib.RA_BF16):
+    """Per query segment: visible (query, key) pairs per head and scheduled
+    128x128 tile products (host-side bookkeeping, no GPU needed)."""
+    lib = load()
+    Sq = sum(int(n) for n, _ in q_segments)
+    pb = Problem()
+    pb.B, pb.Hq, pb.Hkv, pb.D, pb.Sq = B, Hq, Hkv, D, Sq
+    pb.dtype, pb.causal, pb.scale, pb.reserved = dtype, 1 if causal else 0, 0.0, 0
+    pb.q_strides = Strides(Hq * Sq * D, Sq * D, D)
+    pb.o_strides = pb.q_strides
+    segs = (QSegment * len(q_segments))()
+    for i, (ln, spans) in enumerate(q_segments):
+        segs[i].len = int(ln)
+        segs[i].pos = positions(spans)
+    chs = (KvChunk * max(1, len(chunk_lens)))()
+    for i, (ln, spans) in enumerate(zip(chunk_lens, chunk_spans)):
+        chs[i].len = int(ln)
+        chs[i].pos = positions(spans)
+    pairs = (ctypes.c_int64 * len(q_segments))()
+    tiles = (ctypes.c_int64 * len(q_segments))()
+    check(lib.ra_segment_work(ctypes.byref(pb), segs, len(q_segments), chs, len(chunk_lens),
+                              ctypes.cast(pairs, ctypes.c_void_p),
+                              ctypes.cast(tiles, ctypes.c_void_p)))
+    return list(pairs), list(tiles)
+
+
+def device_status(stream=None):
+    """Synchronise ``stream`` and raise if a kernel gave up on a bounded wait."""
+    check(load().ra_device_status(_stream(stream)))
+
+
+def default_scale(D: int) -> float:
+    return 1.0 / math.sqrt(D)

@@ -1,0 +1,506 @@
+// Host side of the C ABI declared in include/ra.h: argument validation, plan
+// building (position spans, ring visit order, causal work per query tile
+// pair, longest-first order), TMA tensor-map creation and kernel launches.
+//
+// No device memory is allocated here: plans travel as kernel parameters.
+#include "ra.h"
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <numeric>
+#include <vector>
+
+#include "ra_plan.h"
+
+namespace {
+
+thread_local char g_msg[512] = "";
+
+ra_status fail(ra_status st, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+ra_status ok() {
+  g_msg[0] = '\0';
+  return RA_OK;
+}
+
+constexpr int64_t kPosLimit = (int64_t(1) << 31) - 1;
+constexpr int64_t kRowLimit = (int64_t(1) << 31) - 256;
+
+// A flattened monotone span of rows with global positions.
+struct Span {
+  int64_t row0, len, pos0, step;
+  int32_t owner;  // segment or chunk index
+};
+
+ra_status check_positions(const ra_positions& p, int64_t rows, const char* what,
+                          int64_t idx) {
+  if (p.nspan < 1 || p.nspan > RA_MAX_SPANS)
+    return fail(RA_ERR_INVALID, "%s %lld: nspan=%d not in [1,%d]", what,
+                (long long)idx, p.nspan, RA_MAX_SPANS);
+  if (p.reserved != 0)
+    return fail(RA_ERR_INVALID, "%s %lld: reserved field must be 0", what, (long long)idx);
+  int64_t total = 0;
+  for (int s = 0; s < p.nspan; ++s) {
+    const ra_span& sp = p.span[s];
+    if (sp.len < 0 || sp.pos0 < 0 || sp.step < 1)
+      return fail(RA_ERR_INVALID, "%s %lld span %d: need len>=0, pos0>=0, step>=1",
+                  what, (long long)idx, s);
+    if (sp.len > 0) {
+      // last position = pos0 + step*(len-1) must stay below 2^31-1
+      if (sp.len - 1 > (kPosLimit - 1 - sp.pos0) / sp.step)
+        return fail(RA_ERR_UNSUPPORTED, "%s %lld span %d: positions reach 2^31",
+                    what, (long long)idx, s);
+    }
+    total += sp.len;
+  }
+  if (total != rows)
+    return fail(RA_ERR_INVALID, "%s %lld: span lengths add to %lld, rows = %lld",
+                what, (long long)idx, (long long)total, (long long)rows);
+  return RA_OK;
+}
+
+struct Common {
+  int64_t B, Hq, Hkv, D, Sq;
+  int dtype, causal;
+  float scale;
+  std::vector<Span> qspans;   // query pieces, owner = segment
+  std::vector<Span> kvspans;  // key/value pieces, owner = chunk (row0 within chunk)
+  std::vector<int> chunk_begin;  // kvspans of chunk c: [begin[c], begin[c+1])
+  int nchunks;
+  bool ring;
+};
+
+ra_status check_strides(const ra_strides& s, const char* what) {
+  if (s.batch < 0 || s.head < 0 || s.row < 0)
+    return fail(RA_ERR_INVALID, "%s: negative stride", what);
+  return RA_OK;
+}
+
+ra_status validate(const ra_problem* pb, const void* q, const ra_q_segment* segs,
+                   int32_t nsegs, const ra_kv_chunk* chunks, int32_t nchunks,
+                   Common* c) {
+  if (!pb) return fail(RA_ERR_INVALID, "problem is NULL");
+  const ra_problem& p = *pb;
+  if (p.B < 1 || p.Hq < 1 || p.Hkv < 1 || p.D < 1 || p.Sq < 0)
+    return fail(RA_ERR_INVALID, "need B, Hq, Hkv, D >= 1 and Sq >= 0");
+  if (p.Hq % p.Hkv != 0)
+    return fail(RA_ERR_INVALID, "Hq=%lld is not a multiple of Hkv=%lld",
+                (long long)p.Hq, (long long)p.Hkv);
+  if (p.dtype != RA_F32 && p.dtype != RA_BF16)
+    return fail(RA_ERR_INVALID, "unknown dtype %d", p.dtype);
+  if (p.causal != 0 && p.causal != 1) return fail(RA_ERR_INVALID, "causal must be 0 or 1");
+  if (p.reserved != 0) return fail(RA_ERR_INVALID, "problem.reserved must be 0");
+  if (!std::isfinite(p.scale)) return fail(RA_ERR_INVALID, "scale is not finite");
+  if (p.dtype == RA_BF16 && p.D != 64 && p.D != 128)
+    return fail(RA_ERR_UNSUPPORTED, "bf16 path supports head_dim 64 or 128, got %lld",
+                (long long)p.D);
+  if (p.dtype == RA_F32 && p.D > 128)
+    return fail(RA_ERR_UNSUPPORTED, "fp32 path supports head_dim <= 128, got %lld",
+                (long long)p.D);
+  if (p.Sq > kRowLimit) return fail(RA_ERR_UNSUPPORTED, "Sq too large");
+  if (p.B * p.Hq > (int64_t(1) << 30)) return fail(RA_ERR_UNSUPPORTED, "B*Hq too large");
+  ra_status st;
+  if ((st = check_strides(p.q_strides, "q_strides")) != RA_OK) return st;
+  if ((st = check_strides(p.o_strides, "o_strides")) != RA_OK) return st;
+  if (p.Sq > 0 && !q) return fail(RA_ERR_INVALID, "q is NULL");
+  if (nsegs < 0 || (nsegs > 0 && !segs)) return fail(RA_ERR_INVALID, "bad segment list");
+  if (p.Sq > 0 && nsegs < 1) return fail(RA_ERR_INVALID, "need at least one query segment");
+  if (nchunks < 0 || (nchunks > 0 && !chunks)) return fail(RA_ERR_INVALID, "bad chunk list");
+
+  c->B = p.B; c->Hq = p.Hq; c->Hkv = p.Hkv; c->D = p.D; c->Sq = p.Sq;
+  c->dtype = p.dtype; c->causal = p.causal;
+  c->scale = p.scale > 0.f ? p.scale : float(1.0 / std::sqrt(double(p.D)));
+  c->qspans.clear(); c->kvspans.clear(); c->chunk_begin.assign(1, 0);
+  c->nchunks = nchunks;
+  c->ring = (nsegs == nchunks && nchunks > 1);
+
+  int64_t row = 0;
+  for (int32_t s = 0; s < nsegs; ++s) {
+    if (segs[s].len < 0) return fail(RA_ERR_INVALID, "segment %d: negative len", s);
+    if ((st = check_positions(segs[s].pos, segs[s].len, "segment", s)) != RA_OK) return st;
+    int64_t r = row;
+    for (int k = 0; k < segs[s].pos.nspan; ++k) {
+      const ra_span& sp = segs[s].pos.span[k];
+      if (sp.len > 0) c->qspans.push_back({r, sp.len, sp.pos0, sp.step, s});
+      r += sp.len;
+    }
+    row += segs[s].len;
+  }
+  if (row != p.Sq)
+    return fail(RA_ERR_INVALID, "segment lengths add to %lld, Sq = %lld",
+                (long long)row, (long long)p.Sq);
+
+  for (int32_t k = 0; k < nchunks; ++k) {
+    const ra_kv_chunk& ch = chunks[k];
+    if (ch.len < 0) return fail(RA_ERR_INVALID, "chunk %d: negative len", k);
+    if (ch.len > kRowLimit) return fail(RA_ERR_UNSUPPORTED, "chunk %d too long", k);
+    if ((st = check_positions(ch.pos, ch.len, "chunk", k)) != RA_OK) return st;
+    if (ch.len > 0) {
+      if (!ch.k || !ch.v) return fail(RA_ERR_INVALID, "chunk %d: NULL k or v", k);
+      if ((st = check_strides(ch.k_strides, "chunk k_strides")) != RA_OK) return st;
+      if ((st = check_strides(ch.v_strides, "chunk v_strides")) != RA_OK) return st;
+      int64_t r = 0;
+      for (int s = 0; s < ch.pos.nspan; ++s) {
+        const ra_span& sp = ch.pos.span[s];
+        if (sp.len > 0) c->kvspans.push_back({r, sp.len, sp.pos0, sp.step, k});
+        r += sp.len;
+      }
+    }
+    c->chunk_begin.push_back(int(c->kvspans.size()));
+  }
+  if ((int64_t)c->qspans.size() > ra::kMaxQPieces)
+    return fail(RA_ERR_UNSUPPORTED, "%zu query spans exceed the limit of %d",
+                c->qspans.size(), ra::kMaxQPieces);
+  return RA_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Highest position over query rows [r0, r1) (spans are sorted by row).
+int64_t qmax_of_rows(const std::vector<Span>& qs, int64_t r0, int64_t r1) {
+  int64_t best = -1;
+  for (const Span& s : qs) {
+    int64_t a = std::max(r0, s.row0), b = std::min(r1, s.row0 + s.len);
+    if (a < b) best = std::max(best, s.pos0 + s.step * (b - 1 - s.row0));
+  }
+  return best;
+}
+
+// Key tiles of a span (128 rows each) that are not entirely in the future of
+// a query whose highest position is qmax.
+int64_t live_tiles(const Span& kv, int64_t qmax, bool causal) {
+  int64_t nt = (kv.len + 127) / 128;
+  if (!causal) return nt;
+  if (qmax < kv.pos0) return 0;
+  int64_t last = (qmax - kv.pos0) / kv.step;  // last visible row index in span
+  return std::min(nt, last / 128 + 1);
+}
+
+// ----------------------------------------------------------- tensor maps
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+ra_status get_encoder() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  if (!g_encode) return fail(RA_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+  return RA_OK;
+}
+
+// 4-D bf16 map over [B, H, rows, D] with box 64 x 128 (one 128-byte swizzle
+// atom wide, one 128-row tile high); rows past `rows` read as zero.
+ra_status make_map(CUtensorMap* map, const void* base, int64_t D, int64_t rows,
+                   int64_t H, int64_t B, const ra_strides& st, const char* what) {
+  cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)rows, (cuuint64_t)H, (cuuint64_t)B};
+  cuuint64_t strides[3] = {(cuuint64_t)st.row * 2, (cuuint64_t)st.head * 2,
+                           (cuuint64_t)st.batch * 2};
+  // unused axes (extent 1) may carry any stride; TMA still wants a multiple of 16
+  if (rows == 1) strides[0] = std::max<cuuint64_t>(16, strides[0] & ~cuuint64_t(15));
+  if (H == 1) strides[1] = std::max<cuuint64_t>(16, strides[1] & ~cuuint64_t(15));
+  if (B == 1) strides[2] = std::max<cuuint64_t>(16, strides[2] & ~cuuint64_t(15));
+  cuuint32_t box[4] = {64, 128, 1, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base),
+                        dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(RA_ERR_INVALID, "tensor map for %s rejected (CUresult %d)", what, (int)r);
+  return RA_OK;
+}
+
+ra_status check_bf16_strides(const ra_strides& s, int64_t rows, int64_t H, int64_t B,
+                             const char* what) {
+  // TMA global strides must be multiples of 16 bytes (8 bf16 elements)
+  if ((rows > 1 && s.row % 8) || (H > 1 && s.head % 8) || (B > 1 && s.batch % 8))
+    return fail(RA_ERR_INVALID, "%s: bf16 strides must be multiples of 8 elements", what);
+  if (rows > 1 && s.row < 1) return fail(RA_ERR_INVALID, "%s: zero row stride", what);
+  return RA_OK;
+}
+
+int g_num_sms_cache[64];
+
+int num_sms() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (dev >= 0 && dev < 64 && g_num_sms_cache[dev] > 0) return g_num_sms_cache[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  if (dev >= 0 && dev < 64) g_num_sms_cache[dev] = n;
+  return n;
+}
+
+ra_status cuda_status(int err, const char* what) {
+  if (err == cudaSuccess) return ok();
+  return fail(RA_ERR_CUDA, "%s: %s", what, cudaGetErrorString((cudaError_t)err));
+}
+
+void fill_q_pieces(const Common& c, ra::QPiece* qp, int32_t* n) {
+  *n = (int32_t)c.qspans.size();
+  for (size_t i = 0; i < c.qspans.size(); ++i) {
+    const Span& s = c.qspans[i];
+    qp[i] = {int32_t(s.row0), int32_t(s.len), int32_t(s.pos0), int32_t(s.step), s.owner};
+  }
+}
+
+// ----------------------------------------------------------- bf16 plan
+ra_status run_tc(const Common& c, const ra_problem& p, const void* q,
+                 const ra_kv_chunk* chunks, void* out, float* m, float* l,
+                 bool stats_mode, void* stream) {
+  if (c.nchunks > ra::kTcMaxChunks)
+    return fail(RA_ERR_UNSUPPORTED, "bf16 path handles at most %d chunks, got %d",
+                ra::kTcMaxChunks, c.nchunks);
+  if ((int)c.kvspans.size() > ra::kTcMaxKvSegs)
+    return fail(RA_ERR_UNSUPPORTED, "bf16 path handles at most %d chunk spans, got %zu",
+                ra::kTcMaxKvSegs, c.kvspans.size());
+  ra_status st;
+  if (!aligned16(q)) return fail(RA_ERR_INVALID, "q must be 16-byte aligned");
+  if (!aligned16(out)) return fail(RA_ERR_INVALID, "output must be 16-byte aligned");
+  if ((st = check_bf16_strides(p.q_strides, c.Sq, c.Hq, c.B, "q_strides")) != RA_OK) return st;
+  const int64_t ovec = stats_mode ? 4 : 8;  // 16-byte row segments
+  if ((c.Sq > 1 && p.o_strides.row % ovec) || (c.Hq > 1 && p.o_strides.head % ovec) ||
+      (c.B > 1 && p.o_strides.batch % ovec))
+    return fail(RA_ERR_INVALID, "output strides must be multiples of %lld elements",
+                (long long)ovec);
+  for (int k = 0; k < c.nchunks; ++k) {
+    const ra_kv_chunk& ch = chunks[k];
+    if (ch.len == 0) continue;
+    if (!aligned16(ch.k) || !aligned16(ch.v))
+      return fail(RA_ERR_INVALID, "chunk %d: k and v must be 16-byte aligned", k);
+    if ((st = check_bf16_strides(ch.k_strides, ch.len, c.Hkv, c.B, "chunk k_strides")) != RA_OK) return st;
+    if ((st = check_bf16_strides(ch.v_strides, ch.len, c.Hkv, c.B, "chunk v_strides")) != RA_OK) return st;
+  }
+  if ((st = get_encoder()) != RA_OK) return st;
+
+  static thread_local ra::TcPlan plan;  // ~28 KB: keep it off the stack
+  std::memset(&plan, 0, sizeof(plan));
+  if ((st = make_map(&plan.qmap, q, c.D, std::max<int64_t>(c.Sq, 1), c.Hq, c.B,
+                     p.q_strides, "q")) != RA_OK)
+    return st;
+  for (int k = 0; k < c.nchunks; ++k) {
+    const ra_kv_chunk& ch = chunks[k];
+    if (ch.len == 0) continue;
+    if ((st = make_map(&plan.kmap[k], ch.k, c.D, ch.len, c.Hkv, c.B, ch.k_strides, "k")) != RA_OK) return st;
+    if ((st = make_map(&plan.vmap[k], ch.v, c.D, ch.len, c.Hkv, c.B, ch.v_strides, "v")) != RA_OK) return st;
+  }
+  plan.out = out; plan.m = m; plan.l = l;
+  plan.o_sb = p.o_strides.batch; plan.o_sh = p.o_strides.head; plan.o_sr = p.o_strides.row;
+  plan.timeout_ns = 2000000000ull;
+  plan.B = int32_t(c.B); plan.Hq = int32_t(c.Hq); plan.Hkv = int32_t(c.Hkv);
+  plan.Sq = int32_t(c.Sq);
+  plan.causal = c.causal; plan.stats_mode = stats_mode ? 1 : 0;
+  plan.ring = c.ring ? 1 : 0; plan.n_chunks = c.nchunks;
+  plan.scale = c.scale;
+  plan.scale_log2 = float(double(c.scale) * 1.4426950408889634);
+  fill_q_pieces(c, plan.qp, &plan.n_qpieces);
+  plan.n_kvsegs = int32_t(c.kvspans.size());
+  for (size_t i = 0; i < c.kvspans.size(); ++i) {
+    const Span& s = c.kvspans[i];
+    plan.ks[i] = {s.owner, int32_t(s.row0), int32_t(s.len), int32_t(s.pos0), int32_t(s.step),
+                  int32_t((s.len + 127) / 128)};
+  }
+  for (int k = 0; k <= c.nchunks; ++k) plan.chunk_seg_begin[k] = c.chunk_begin[k];
+
+  const int64_t npairs = (c.Sq + ra::kTcRowsPerUnit - 1) / ra::kTcRowsPerUnit;
+  plan.n_qpairs = int32_t(npairs);
+  const int64_t units = npairs * c.B * c.Hq;
+  if (units > (int64_t(1) << 31) - 1) return fail(RA_ERR_UNSUPPORTED, "too many work units");
+  plan.n_units = int32_t(units);
+  plan.has_order = 0;
+  if (npairs <= ra::kTcMaxOrder && c.causal) {
+    // longest-first: q-tile pairs with more live key tiles go first
+    std::vector<int64_t> work(npairs, 0);
+    for (int64_t qp = 0; qp < npairs; ++qp) {
+      int64_t r0 = qp * ra::kTcRowsPerUnit, r1 = std::min(c.Sq, r0 + ra::kTcRowsPerUnit);
+      int64_t qmax = qmax_of_rows(c.qspans, r0, r1);
+      for (const Span& kv : c.kvspans) work[qp] += live_tiles(kv, qmax, true);
+    }
+    std::vector<int32_t> idx(npairs);
+    std::iota(idx.begin(), idx.end(), 0);
+    std::stable_sort(idx.begin(), idx.end(),
+                     [&](int32_t a, int32_t b) { return work[a] > work[b]; });
+    for (int64_t i = 0; i < npairs; ++i) plan.order[i] = uint16_t(idx[i]);
+    plan.has_order = 1;
+  }
+  if (units == 0) return ok();
+  const int sms = num_sms();
+  if (sms <= 0) return cuda_status(cudaErrorNoDevice, "querying the SM count");
+  return cuda_status(ra::launch_tc_bf16(plan, int(c.D), sms, stream), "bf16 ring kernel launch");
+}
+
+// ----------------------------------------------------------- fp32 plan
+ra_status run_simt(const Common& c, const ra_problem& p, const void* q,
+                   const ra_kv_chunk* chunks, void* out, float* m, float* l,
+                   bool stats_mode, void* stream) {
+  if (c.nchunks > ra::kSimtMaxChunks)
+    return fail(RA_ERR_UNSUPPORTED, "fp32 path handles at most %d chunks, got %d",
+                ra::kSimtMaxChunks, c.nchunks);
+  if ((int)c.kvspans.size() > ra::kSimtMaxKvSegs)
+    return fail(RA_ERR_UNSUPPORTED, "fp32 path handles at most %d chunk spans, got %zu",
+                ra::kSimtMaxKvSegs, c.kvspans.size());
+  static thread_local ra::SimtPlan plan;
+  std::memset(&plan, 0, sizeof(plan));
+  plan.q = static_cast<const float*>(q);
+  plan.out = static_cast<float*>(out); plan.m = m; plan.l = l;
+  plan.q_sb = p.q_strides.batch; plan.q_sh = p.q_strides.head; plan.q_sr = p.q_strides.row;
+  plan.o_sb = p.o_strides.batch; plan.o_sh = p.o_strides.head; plan.o_sr = p.o_strides.row;
+  plan.B = int32_t(c.B); plan.Hq = int32_t(c.Hq); plan.Hkv = int32_t(c.Hkv);
+  plan.D = int32_t(c.D); plan.Sq = int32_t(c.Sq);
+  plan.causal = c.causal; plan.stats_mode = stats_mode ? 1 : 0;
+  plan.ring = c.ring ? 1 : 0; plan.n_chunks = c.nchunks;
+  plan.scale = c.scale;
+  fill_q_pieces(c, plan.qp, &plan.n_qpieces);
+  plan.n_kvsegs = int32_t(c.kvspans.size());
+  for (size_t i = 0; i < c.kvspans.size(); ++i) {
+    const Span& s = c.kvspans[i];
+    plan.ks[i] = {s.owner, int32_t(s.row0), int32_t(s.len), int32_t(s.pos0), int32_t(s.step),
+                  int32_t((s.len + 31) / 32)};
+  }
+  for (int k = 0; k <= c.nchunks; ++k) plan.chunk_seg_begin[k] = c.chunk_begin[k];
+  for (int k = 0; k < c.nchunks; ++k) {
+    const ra_kv_chunk& ch = chunks[k];
+    plan.ch[k] = {static_cast<const float*>(ch.k), static_cast<const float*>(ch.v),
+                  ch.k_strides.batch, ch.k_strides.head, ch.k_strides.row,
+                  ch.v_strides.batch, ch.v_strides.head, ch.v_strides.row};
+  }
+  if (c.Sq == 0) return ok();
+  return cuda_status(ra::launch_simt_f32(plan, stream), "fp32 ring kernel launch");
+}
+
+ra_status run(const ra_problem* pb, const void* q, const ra_q_segment* segs, int32_t nsegs,
+              const ra_kv_chunk* chunks, int32_t nchunks, void* out, float* m, float* l,
+              bool stats_mode, void* stream) {
+  Common c;
+  ra_status st = validate(pb, q, segs, nsegs, chunks, nchunks, &c);
+  if (st != RA_OK) return st;
+  if (c.Sq == 0) return ok();
+  if (!out || !m || !l) return fail(RA_ERR_INVALID, "output pointer is NULL");
+  if (c.dtype == RA_BF16) return run_tc(c, *pb, q, chunks, out, m, l, stats_mode, stream);
+  return run_simt(c, *pb, q, chunks, out, m, l, stats_mode, stream);
+}
+
+}  // namespace
+
+extern "C" {
+
+ra_status ra_chunk_stats(const ra_problem* problem, const void* q,
+                         const ra_q_segment* segs, int32_t nsegs,
+                         const ra_kv_chunk* chunk, float* u, float* l, float* m,
+                         void* stream) {
+  if (!chunk) return fail(RA_ERR_INVALID, "chunk is NULL");
+  return run(problem, q, segs, nsegs, chunk, 1, u, m, l, true, stream);
+}
+
+ra_status ra_ring_attention(const ra_problem* problem, const void* q,
+                            const ra_q_segment* segs, int32_t nsegs,
+                            const ra_kv_chunk* chunks, int32_t nchunks, void* o,
+                            float* m, float* l, void* stream) {
+  return run(problem, q, segs, nsegs, chunks, nchunks, o, m, l, false, stream);
+}
+
+ra_status ra_merge_stats(int64_t rows, int64_t D, float* u_acc, float* l_acc, float* m_acc,
+                         const float* u_new, const float* l_new, const float* m_new,
+                         void* stream) {
+  if (rows < 0 || D < 1) return fail(RA_ERR_INVALID, "need rows >= 0 and D >= 1");
+  if (rows == 0) return ok();
+  if (!u_acc || !l_acc || !m_acc || !u_new || !l_new || !m_new)
+    return fail(RA_ERR_INVALID, "NULL pointer");
+  if (rows > (int64_t(1) << 40) / D) return fail(RA_ERR_UNSUPPORTED, "too many elements");
+  const int sms = num_sms();
+  if (sms <= 0) return cuda_status(cudaErrorNoDevice, "querying the SM count");
+  return cuda_status(ra::launch_merge_f32(rows, D, u_acc, l_acc, m_acc, u_new, l_new, m_new,
+                                          sms, stream),
+                     "merge kernel launch");
+}
+
+ra_status ra_segment_work(const ra_problem* problem, const ra_q_segment* segs, int32_t nsegs,
+                          const ra_kv_chunk* chunks, int32_t nchunks, int64_t* pairs,
+                          int64_t* tiles) {
+  Common c;
+  // positions only: pointers are not needed for bookkeeping
+  ra_status st = validate(problem, reinterpret_cast<const void*>(16), segs, nsegs, nullptr,
+                          0, &c);
+  if (st != RA_OK) return st;
+  if (nchunks < 0 || (nchunks > 0 && !chunks)) return fail(RA_ERR_INVALID, "bad chunk list");
+  std::vector<Span> kv;
+  for (int32_t k = 0; k < nchunks; ++k) {
+    if (chunks[k].len < 0) return fail(RA_ERR_INVALID, "chunk %d: negative len", k);
+    if ((st = check_positions(chunks[k].pos, chunks[k].len, "chunk", k)) != RA_OK) return st;
+    int64_t r = 0;
+    for (int s = 0; s < chunks[k].pos.nspan; ++s) {
+      const ra_span& sp = chunks[k].pos.span[s];
+      if (sp.len > 0) kv.push_back({r, sp.len, sp.pos0, sp.step, k});
+      r += sp.len;
+    }
+  }
+  for (int32_t s = 0; s < nsegs; ++s) {
+    if (pairs) pairs[s] = 0;
+    if (tiles) tiles[s] = 0;
+  }
+  if (pairs) {
+    for (const Span& qs : c.qspans) {
+      int64_t acc = 0;
+      for (int64_t i = 0; i < qs.len; ++i) {
+        int64_t pq = qs.pos0 + qs.step * i;
+        for (const Span& ks : kv) {
+          if (!c.causal) { acc += ks.len; continue; }
+          if (pq < ks.pos0) continue;
+          acc += std::min(ks.len, (pq - ks.pos0) / ks.step + 1);
+        }
+      }
+      pairs[qs.owner] += acc;
+    }
+  }
+  if (tiles) {
+    const int64_t npairs = (c.Sq + ra::kTcRowsPerUnit - 1) / ra::kTcRowsPerUnit;
+    for (int64_t qp = 0; qp < npairs; ++qp) {
+      int64_t r0 = qp * ra::kTcRowsPerUnit, r1 = std::min(c.Sq, r0 + ra::kTcRowsPerUnit);
+      int64_t qmax = qmax_of_rows(c.qspans, r0, r1);
+      int owner = 0;
+      for (const Span& qs : c.qspans)
+        if (r0 >= qs.row0 && r0 < qs.row0 + qs.len) owner = qs.owner;
+      int64_t n = 0;
+      for (const Span& ks : kv) n += live_tiles(ks, qmax, c.causal != 0);
+      tiles[owner] += 2 * n;
+    }
+  }
+  return ok();
+}
+
+ra_status ra_device_status(void* stream) {
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(RA_ERR_CUDA, "stream: %s", cudaGetErrorString(e));
+  int code = 0;
+  int err = ra::read_and_clear_device_error(&code);
+  if (err != cudaSuccess) return cuda_status(err, "reading the device status word");
+  if (code != 0)
+    return fail(RA_ERR_TIMEOUT, "a kernel gave up waiting (code %d): its outputs are invalid",
+                code);
+  return ok();
+}
+
+const char* ra_last_error(void) { return g_msg; }
+
+int32_t ra_version(void) { return RA_VERSION; }
+
+}  // extern "C"

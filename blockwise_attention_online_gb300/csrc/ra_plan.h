@@ -1,0 +1,90 @@
+// Internal launch plans of the ring-attention kernels.
+//
+// A plan is built on the host from the caller's descriptors and passed to a
+// kernel BY VALUE as a __grid_constant__ parameter (at most 32 KB), so a call
+// needs no device allocation and no host-to-device copy besides the launch.
+// Rows and positions are 32-bit here; the host validates that they fit.
+#pragma once
+
+#include <cuda.h>
+#include <stdint.h>
+
+namespace ra {
+
+// Rows [row0, row0 + len) of Q have global positions pos0 + step * (i - row0).
+// `seg` is the query segment the rows belong to (its ring role).
+struct QPiece {
+  int32_t row0, len, pos0, step, seg;
+};
+
+// One monotone span of a key/value chunk, the unit the kernels iterate over:
+// rows [row0, row0 + len) of chunk `chunk`, positions pos0 + step * (i - row0).
+struct KvSeg {
+  int32_t chunk, row0, len, pos0, step, ntiles;  // ntiles: 128-row tiles
+};
+
+constexpr int kMaxQPieces = 64;
+
+// ---------------------------------------------------------------- bf16 path
+constexpr int kTcMaxChunks = 32;
+constexpr int kTcMaxKvSegs = 64;
+constexpr int kTcMaxOrder = 8192;  // q-tile pairs that can be LPT-ordered
+constexpr int kTcRowsPerUnit = 256;  // two 128-row query tiles per work unit
+
+struct alignas(128) TcPlan {
+  CUtensorMap qmap;                  // Q  [B, Hq, Sq, D] bf16, box 64 x 128
+  CUtensorMap kmap[kTcMaxChunks];    // K chunk c [B, Hkv, len, D]
+  CUtensorMap vmap[kTcMaxChunks];    // V chunk c
+  void* out;                         // O (bf16) or u (fp32, stats mode)
+  float* m;
+  float* l;
+  int64_t o_sb, o_sh, o_sr;          // element strides of out
+  unsigned long long timeout_ns;     // budget of any single wait
+  int32_t B, Hq, Hkv, Sq;
+  int32_t causal, stats_mode, ring, n_chunks;
+  float scale, scale_log2;
+  int32_t n_qpieces, n_kvsegs, n_qpairs, has_order;
+  int32_t n_units;
+  int32_t chunk_seg_begin[kTcMaxChunks + 1];
+  QPiece qp[kMaxQPieces];
+  KvSeg ks[kTcMaxKvSegs];
+  uint16_t order[kTcMaxOrder];       // q-pair visit order (longest first)
+};
+static_assert(sizeof(TcPlan) <= 32000, "bf16 plan must fit the parameter space");
+
+// ---------------------------------------------------------------- fp32 path
+constexpr int kSimtMaxChunks = 256;
+constexpr int kSimtMaxKvSegs = 320;
+
+struct SimtChunk {
+  const float* k;
+  const float* v;
+  int64_t k_sb, k_sh, k_sr, v_sb, v_sh, v_sr;
+};
+
+struct SimtPlan {
+  const float* q;
+  float* out;                        // O or u
+  float* m;
+  float* l;
+  int64_t q_sb, q_sh, q_sr, o_sb, o_sh, o_sr;
+  int32_t B, Hq, Hkv, D, Sq;
+  int32_t causal, stats_mode, ring, n_chunks;
+  int32_t n_qpieces, n_kvsegs;
+  float scale;
+  int32_t chunk_seg_begin[kSimtMaxChunks + 1];
+  QPiece qp[kMaxQPieces];
+  KvSeg ks[kSimtMaxKvSegs];
+  SimtChunk ch[kSimtMaxChunks];
+};
+static_assert(sizeof(SimtPlan) <= 32000, "fp32 plan must fit the parameter space");
+
+// Kernel launchers (defined in the .cu files; return a cudaError_t as int).
+int launch_tc_bf16(const TcPlan& plan, int D, int num_sms, void* stream);
+int launch_simt_f32(const SimtPlan& plan, void* stream);
+int launch_merge_f32(int64_t rows, int64_t D, float* u_acc, float* l_acc,
+                     float* m_acc, const float* u_new, const float* l_new,
+                     const float* m_new, int num_sms, void* stream);
+int read_and_clear_device_error(int* code);
+
+}  // namespace ra

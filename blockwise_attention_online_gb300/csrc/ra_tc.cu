@@ -1,0 +1,620 @@
+// bf16 ring-attention forward on the 5th-generation tensor cores (sm_103a).
+//
+// One persistent kernel runs the whole chunk walk of the ring forward pass
+// (exercise page "systems-distributed-ring-attention-online-softmax", task
+// statement; "Ring Attention: Distributed Reads with Online Softmax",
+// section "A simple forward schedule"; glossary "ring attention", algorithm
+// steps (1)-(6)). A work unit is (batch, query head, pair of 128-row query
+// tiles). For a unit the CTA visits the key/value chunks in the ring order of
+// the unit's query segment and, per 128-row key tile:
+//
+//   S_t = Q_t K^T                      tcgen05.mma, SMEM x SMEM -> TMEM (fp32)
+//   mask (causal / ragged), row max, exp2, row sum      softmax warpgroup t
+//   lazy rescale of O_t when the running max grows      (online-softmax merge)
+//   O_t += P_t V                       tcgen05.mma, TMEM(P, bf16) x SMEM -> TMEM
+//
+// m, l stay in registers and O in TMEM for the whole walk; only the final
+// O = u / l (or u itself for chunk statistics) goes back to HBM.
+//
+// Warp roles (384 threads):
+//   warp 0      TMA producer: Q tiles once per unit, then K_j, V_j into a ring
+//               of shared-memory stages. The pages' "receive the next shard
+//               while computing the current one" (blog, "A simple forward
+//               schedule"; glossary "Communication overlap") becomes this
+//               multi-stage prefetch with full/empty mbarriers.
+//   warp 1      MMA issuer (one thread) and TMEM owner.
+//   warps 4-7   softmax warpgroup for query tile 0 (TMEM lanes 0-127)
+//   warps 8-11  softmax warpgroup for query tile 1
+// The MMA order S0(j) S1(j) | PV0(j) S0(j+1) PV1(j) S1(j+1) | ... lets the
+// tensor core work on one tile while the other tile's softmax runs.
+//
+// TMEM columns: S0/P0 [0,128), S1/P1 [128,256), O0 [256,256+D), O1 [384,384+D).
+// P (bf16, two per column) overwrites the first 64 columns of its S after the
+// row has been read; tcgen05.mma operations of one thread execute in order, so
+// the next S MMA never overtakes the PV MMA that reads P.
+//
+// Every mbarrier wait is bounded by a time budget. On expiry the kernel records
+// a code in a device status word, tells its other warps to stop, waits for its
+// own copies and MMAs in flight, frees TMEM and returns.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "ra_plan.h"
+#include "ra_ptx.cuh"
+
+namespace ra {
+
+__device__ int g_ra_device_error = 0;
+
+namespace {
+
+using namespace ptx;
+
+constexpr int kThreads = 384;
+constexpr float kNegInf = -__builtin_huge_valf();
+// Rescale O and l only when the running max (log2 units) grows by more than
+// this: p = 2^(s - m_ref) then stays below 2^8, exact enough in bf16/fp32.
+constexpr float kRescaleLog2 = 8.0f;
+
+template <int D>
+struct Cfg {
+  static constexpr int kTileBytes = 128 * D * 2;  // one 128-row bf16 tile
+  static constexpr int kBoxBytes = 128 * 128;     // 128 rows x 64 bf16 (one swizzle atom wide)
+  static constexpr int kBoxes = D / 64;
+  static constexpr int kStages = (D == 128) ? 4 : 8;
+  static constexpr int kQOff = 0;
+  static constexpr int kKvOff = 2 * kTileBytes;
+  static constexpr int kBarOff = kKvOff + kStages * kTileBytes;
+  static constexpr int kBarBytes = 256;
+  static constexpr int kSmemBytes = kBarOff + kBarBytes + 1024;  // + alignment slack
+};
+
+// Wait sites, reported in the status word as 0x100 | site.
+enum : int {
+  kSiteProdQ = 1, kSiteProdKv = 2, kSiteMmaQ = 3, kSiteMmaKv = 4, kSiteMmaP = 5,
+  kSiteMmaO = 6, kSiteSoftS = 7, kSiteSoftO = 8, kSiteDrain = 9
+};
+
+struct Unit {
+  int b, hq, hkv, qrow0, qseg, qmax, n;
+};
+
+__device__ __forceinline__ int find_piece(const TcPlan& p, int row) {
+  int lo = 0, hi = p.n_qpieces - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (p.qp[mid].row0 <= row) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+__device__ __forceinline__ int row_position(const TcPlan& p, int row) {
+  const QPiece& q = p.qp[find_piece(p, row)];
+  return q.pos0 + q.step * (row - q.row0);
+}
+
+// Key tiles of span k that are not entirely in the future of position qmax.
+__device__ __forceinline__ int live_tiles(const TcPlan& p, int k, int qmax) {
+  const KvSeg& s = p.ks[k];
+  if (!p.causal) return s.ntiles;
+  if (qmax < s.pos0) return 0;
+  return min(s.ntiles, ((qmax - s.pos0) / s.step) / 128 + 1);
+}
+
+__device__ __forceinline__ void decode_unit(const TcPlan& p, int u, Unit& U) {
+  const int BH = p.B * p.Hq;
+  const int rank = u / BH, bh = u - rank * BH;
+  const int qpair = p.has_order ? int(p.order[rank]) : rank;
+  U.b = bh / p.Hq;
+  U.hq = bh - U.b * p.Hq;
+  U.hkv = U.hq / (p.Hq / p.Hkv);
+  U.qrow0 = qpair * kTcRowsPerUnit;
+  const int r1 = min(U.qrow0 + kTcRowsPerUnit, p.Sq);
+  int i = find_piece(p, U.qrow0);
+  U.qseg = p.qp[i].seg;
+  int qmax = -1;
+  for (; i < p.n_qpieces && p.qp[i].row0 < r1; ++i) {
+    const QPiece& q = p.qp[i];
+    const int e = min(r1, q.row0 + q.len);
+    qmax = max(qmax, q.pos0 + q.step * (e - 1 - q.row0));
+  }
+  U.qmax = qmax;
+  int n = 0;
+  for (int k = 0; k < p.n_kvsegs; ++k) n += live_tiles(p, k, qmax);
+  U.n = n;
+}
+
+// Walks the live key tiles of a unit: chunks in ring order, spans in order,
+// tiles in order. Every warp role runs the same walk.
+struct TileIter {
+  int s, ks, ks_end, t, nlive;
+  __device__ __forceinline__ TileIter() : s(-1), ks(0), ks_end(0), t(0), nlive(0) {}
+  __device__ __forceinline__ bool next(const TcPlan& p, const Unit& U, int& ks_out, int& t_out) {
+    while (true) {
+      if (t < nlive) {
+        ks_out = ks;
+        t_out = t++;
+        return true;
+      }
+      ++ks;
+      if (ks < ks_end) {
+        t = 0;
+        nlive = live_tiles(p, ks, U.qmax);
+        continue;
+      }
+      if (++s >= p.n_chunks) return false;
+      const int c = p.ring ? (U.qseg - s + p.n_chunks) % p.n_chunks : s;
+      ks = p.chunk_seg_begin[c] - 1;
+      ks_end = p.chunk_seg_begin[c + 1];
+      t = 0;
+      nlive = 0;
+    }
+  }
+};
+
+__device__ __forceinline__ void record_error(int code) { atomicCAS(&g_ra_device_error, 0, code); }
+
+// Bounded wait on an mbarrier phase. Returns false (and stops the CTA) when the
+// budget runs out or another warp already gave up.
+__device__ __noinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                      unsigned long long budget, int site) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer();
+  for (uint32_t n = 1;; ++n) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((n & 63u) == 0) {
+      if (*abort_flag) return false;
+      if (globaltimer() - t0 > budget) {
+        *abort_flag = 1;
+        record_error(0x100 | site);
+        return false;
+      }
+    }
+  }
+}
+
+// Warp-uniform version: every lane waits, the warp agrees on the outcome.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                          unsigned long long budget, int site) {
+  const bool ok = wait_bar(bar, parity, abort_flag, budget, site);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// Wait used while tearing down after an abort: ignores the abort flag.
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity,
+                                           unsigned long long budget) {
+  const unsigned long long t0 = globaltimer();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer() - t0 > budget) {
+      record_error(0x100 | kSiteDrain);
+      return;
+    }
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1) tc_ring_kernel(const __grid_constant__ TcPlan p) {
+  using C = Cfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_addr(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* const gbase = smem_raw + (base - raw);
+  const uint32_t sQ = base + C::kQOff;
+  const uint32_t sKV = base + C::kKvOff;
+  const uint32_t bars = base + C::kBarOff;
+  const uint32_t b_qfull = bars, b_qempty = bars + 8;
+  const uint32_t b_kvfull0 = bars + 16, b_kvempty0 = bars + 16 + 8 * C::kStages;
+  const uint32_t b_misc = bars + 16 + 16 * C::kStages;
+  const uint32_t b_sfull0 = b_misc, b_pfull0 = b_misc + 16, b_ofull0 = b_misc + 32,
+                 b_ofree0 = b_misc + 48, b_done = b_misc + 64;
+  uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::kBarOff + 16 + 16 * C::kStages + 72);
+  volatile int* const abort_flag =
+      reinterpret_cast<volatile int*>(gbase + C::kBarOff + 16 + 16 * C::kStages + 76);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const unsigned long long budget = p.timeout_ns;
+
+  if (threadIdx.x == 0) {
+    mbar_init(b_qfull, 1);
+    mbar_init(b_qempty, 1);
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(b_kvfull0 + 8 * s, 1);
+      mbar_init(b_kvempty0 + 8 * s, 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(b_sfull0 + 8 * t, 1);
+      mbar_init(b_pfull0 + 8 * t, 128);
+      mbar_init(b_ofull0 + 8 * t, 1);
+      mbar_init(b_ofree0 + 8 * t, 128);
+    }
+    mbar_init(b_done, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&p.qmap);
+    for (int c = 0; c < p.n_chunks; ++c) {
+      if (p.chunk_seg_begin[c] != p.chunk_seg_begin[c + 1]) {
+        prefetch_tmap(&p.kmap[c]);
+        prefetch_tmap(&p.vmap[c]);
+      }
+    }
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_addr(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    int it = 0, qn = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
+      Unit U;
+      decode_unit(p, u, U);
+      if (U.n == 0) continue;
+      ok = warp_wait(b_qempty, (qn & 1) ^ 1, abort_flag, budget, kSiteProdQ);
+      if (!ok) break;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(b_qfull, 2 * C::kTileBytes);
+#pragma unroll
+        for (int t = 0; t < 2; ++t)
+#pragma unroll
+          for (int bx = 0; bx < C::kBoxes; ++bx)
+            tma_load_4d(sQ + t * C::kTileBytes + bx * C::kBoxBytes, &p.qmap, b_qfull, bx * 64,
+                        U.qrow0 + 128 * t, U.hq, U.b);
+      }
+      __syncwarp();
+      ++qn;
+      TileIter iter;
+      int ks, t;
+      while (ok && iter.next(p, U, ks, t)) {
+        const KvSeg& sg = p.ks[ks];
+        const int row = sg.row0 + 128 * t;
+#pragma unroll
+        for (int kv = 0; kv < 2; ++kv) {
+          const int st = it % C::kStages;
+          ok = warp_wait(b_kvempty0 + 8 * st, ((it / C::kStages) & 1) ^ 1, abort_flag, budget,
+                         kSiteProdKv);
+          if (!ok) break;
+          if (lane == 0) {
+            const uint32_t full = b_kvfull0 + 8 * st;
+            mbar_arrive_expect_tx(full, C::kTileBytes);
+            const CUtensorMap* map = kv == 0 ? &p.kmap[sg.chunk] : &p.vmap[sg.chunk];
+#pragma unroll
+            for (int bx = 0; bx < C::kBoxes; ++bx)
+              tma_load_4d(sKV + st * C::kTileBytes + bx * C::kBoxBytes, map, full, bx * 64, row,
+                          U.hkv, U.b);
+          }
+          __syncwarp();
+          ++it;
+        }
+      }
+    }
+    if (!ok && lane == 0) {
+      // let the copies already in flight land before the CTA goes away
+      for (int s = 0; s < C::kStages; ++s) {
+        const int back = ((it - 1 - s) % C::kStages + C::kStages) % C::kStages;
+        const int last = it - 1 - back;
+        if (last >= 0) drain_wait(b_kvfull0 + 8 * s, (last / C::kStages) & 1, budget);
+      }
+      if (qn > 0) drain_wait(b_qfull, (qn - 1) & 1, budget);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    constexpr uint32_t kIdQK = idesc_bf16_f32(128, 128, 0, 0);
+    constexpr uint32_t kIdPV = idesc_bf16_f32(128, D, 0, 1);
+    const uint32_t tS0 = tmem, tO0 = tmem + 256;
+    auto issue_qk = [&](int t, int st) {
+      const uint32_t qa = sQ + t * C::kTileBytes, ka = sKV + st * C::kTileBytes;
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = (kk >> 2) * C::kBoxBytes + (kk & 3) * 32;
+        mma_ss(tS0 + 128 * t, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024),
+               kIdQK, kk > 0 ? 1u : 0u);
+      }
+    };
+    auto issue_pv = [&](int t, int st, bool acc) {
+      const uint32_t va = sKV + st * C::kTileBytes;
+#pragma unroll
+      for (int kk = 0; kk < 128 / 16; ++kk) {
+        mma_ts(tO0 + 128 * t, tS0 + 128 * t + kk * 8,
+               sdesc_sw128(va + kk * 16 * 128, C::kBoxBytes, 1024), kIdPV,
+               (acc || kk > 0) ? 1u : 0u);
+      }
+    };
+    int it = 0, qn = 0, un = 0;
+    uint32_t pc0 = 0, pc1 = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
+      Unit U;
+      decode_unit(p, u, U);
+      if (U.n == 0) continue;
+      ok = warp_wait(b_qfull, qn & 1, abort_flag, budget, kSiteMmaQ);
+      if (!ok) break;
+      ++qn;
+      int kst = it % C::kStages;
+      ok = warp_wait(b_kvfull0 + 8 * kst, (it / C::kStages) & 1, abort_flag, budget, kSiteMmaKv);
+      if (!ok) break;
+      ++it;
+      tc_fence_after();
+      if (lane == 0) {
+        issue_qk(0, kst);
+        mma_commit(b_sfull0);
+        issue_qk(1, kst);
+        mma_commit(b_sfull0 + 8);
+        mma_commit(b_kvempty0 + 8 * kst);
+        if (U.n == 1) mma_commit(b_qempty);
+      }
+      __syncwarp();
+      for (int j = 0; j < U.n; ++j) {
+        const bool more = j + 1 < U.n;
+        const int vst = it % C::kStages;
+        ok = warp_wait(b_kvfull0 + 8 * vst, (it / C::kStages) & 1, abort_flag, budget, kSiteMmaKv);
+        if (!ok) break;
+        ++it;
+        // query tile 0: PV, then the next S
+        ok = warp_wait(b_pfull0, pc0 & 1, abort_flag, budget, kSiteMmaP);
+        if (!ok) break;
+        ++pc0;
+        if (j == 0) {
+          ok = warp_wait(b_ofree0, (un & 1) ^ 1, abort_flag, budget, kSiteMmaO);
+          if (!ok) break;
+        }
+        tc_fence_after();
+        if (lane == 0) {
+          issue_pv(0, vst, j > 0);
+          if (!more) mma_commit(b_ofull0);
+        }
+        __syncwarp();
+        if (more) {
+          kst = it % C::kStages;
+          ok = warp_wait(b_kvfull0 + 8 * kst, (it / C::kStages) & 1, abort_flag, budget,
+                         kSiteMmaKv);
+          if (!ok) break;
+          ++it;
+          tc_fence_after();
+          if (lane == 0) {
+            issue_qk(0, kst);
+            mma_commit(b_sfull0);
+          }
+          __syncwarp();
+        }
+        // query tile 1
+        ok = warp_wait(b_pfull0 + 8, pc1 & 1, abort_flag, budget, kSiteMmaP);
+        if (!ok) break;
+        ++pc1;
+        if (j == 0) {
+          ok = warp_wait(b_ofree0 + 8, (un & 1) ^ 1, abort_flag, budget, kSiteMmaO);
+          if (!ok) break;
+        }
+        tc_fence_after();
+        if (lane == 0) {
+          issue_pv(1, vst, j > 0);
+          mma_commit(b_kvempty0 + 8 * vst);
+          if (!more) mma_commit(b_ofull0 + 8);
+          if (more) {
+            issue_qk(1, kst);
+            mma_commit(b_sfull0 + 8);
+            mma_commit(b_kvempty0 + 8 * kst);
+            if (j + 2 == U.n) mma_commit(b_qempty);
+          }
+        }
+        __syncwarp();
+      }
+      ++un;
+    }
+    // every MMA this thread issued must be complete before TMEM is freed
+    if (lane == 0) mma_commit(b_done);
+    __syncwarp();
+    if (lane == 0) drain_wait(b_done, 0, budget);
+    __syncwarp();
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ softmax
+    const int wg = (warp - 4) >> 2;
+    const int sub = warp & 3;
+    const int r = sub * 32 + lane;
+    const uint32_t lane_off = uint32_t(sub * 32) << 16;
+    const uint32_t tS = tmem + wg * 128 + lane_off;
+    const uint32_t tO = tmem + 256 + wg * 128 + lane_off;
+    const uint32_t b_sfull = b_sfull0 + 8 * wg, b_pfull = b_pfull0 + 8 * wg;
+    const uint32_t b_ofull = b_ofull0 + 8 * wg, b_ofree = b_ofree0 + 8 * wg;
+    const float c2 = p.scale_log2;
+    uint32_t sc = 0, oc = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
+      Unit U;
+      decode_unit(p, u, U);
+      const int grow = U.qrow0 + wg * 128 + r;
+      const bool rvalid = grow < p.Sq;
+      const int qpos = rvalid ? row_position(p, grow) : 0x7ffffffe;
+      float m_ref = kNegInf, mx = kNegInf, l = 0.f;
+      int j = 0;
+      if (U.n > 0) {
+        TileIter iter;
+        int ks, t;
+        while (iter.next(p, U, ks, t)) {
+          ok = warp_wait(b_sfull, sc & 1, abort_flag, budget, kSiteSoftS);
+          if (!ok) break;
+          ++sc;
+          tc_fence_after();
+          uint32_t s[4][32];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) tmem_ld32(tS + 32 * i, s[i]);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 4; ++i) reg_fence(s[i]);
+
+          // visible columns of this row: a prefix [0, L) of the tile
+          const KvSeg& sg = p.ks[ks];
+          int L = min(128, sg.len - 128 * t);
+          if (p.causal) {
+            const int first = sg.pos0 + sg.step * (128 * t);
+            L = qpos < first ? 0 : min(L, (qpos - first) / sg.step + 1);
+          }
+          float mx0 = kNegInf, mx1 = kNegInf, mx2 = kNegInf, mx3 = kNegInf;
+          if (L >= 128) {
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+              mx0 = fmaxf(mx0, __uint_as_float(s[0][c]));
+              mx1 = fmaxf(mx1, __uint_as_float(s[1][c]));
+              mx2 = fmaxf(mx2, __uint_as_float(s[2][c]));
+              mx3 = fmaxf(mx3, __uint_as_float(s[3][c]));
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+              for (int c = 0; c < 32; ++c)
+                if (32 * i + c >= L) s[i][c] = 0xff800000u;  // -inf
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+              mx0 = fmaxf(mx0, __uint_as_float(s[0][c]));
+              mx1 = fmaxf(mx1, __uint_as_float(s[1][c]));
+              mx2 = fmaxf(mx2, __uint_as_float(s[2][c]));
+              mx3 = fmaxf(mx3, __uint_as_float(s[3][c]));
+            }
+          }
+          const float rmax = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
+          mx = fmaxf(mx, rmax);
+          const float mnew = rmax * c2;
+          if (mnew > m_ref + kRescaleLog2) {
+            const float alpha = ex2(m_ref - mnew);
+            l *= alpha;
+            if (j > 0) {
+#pragma unroll
+              for (int cc = 0; cc < D / 32; ++cc) {
+                uint32_t o[32];
+                tmem_ld32(tO + 32 * cc, o);
+                tmem_ld_wait();
+                reg_fence(o);
+#pragma unroll
+                for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+                tmem_st32(tO + 32 * cc, o);
+              }
+            }
+            m_ref = mnew;
+          }
+          const float off = (m_ref == kNegInf) ? 0.f : m_ref;
+          float l0 = 0.f, l1 = 0.f;
+          uint32_t pk[2][32];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
+              const float a = ex2(fmaf(__uint_as_float(s[i][2 * c]), c2, -off));
+              const float b = ex2(fmaf(__uint_as_float(s[i][2 * c + 1]), c2, -off));
+              l0 += a;
+              l1 += b;
+              pk[i >> 1][(i & 1) * 16 + c] = pack_bf16x2(a, b);
+            }
+          }
+          l += l0 + l1;
+          tmem_st32(tS, pk[0]);
+          tmem_st32(tS + 32, pk[1]);
+          tmem_st_wait();
+          tc_fence_before();
+          mbar_arrive(b_pfull);
+          ++j;
+        }
+        if (!ok) break;
+        ok = warp_wait(b_ofull, oc & 1, abort_flag, budget, kSiteSoftO);
+        if (!ok) break;
+        ++oc;
+        tc_fence_after();
+      }
+      // epilogue: read O, release its TMEM, write this row's results
+      uint32_t o[D / 32][32];
+      if (U.n > 0) {
+#pragma unroll
+        for (int cc = 0; cc < D / 32; ++cc) tmem_ld32(tO + 32 * cc, o[cc]);
+        tmem_ld_wait();
+#pragma unroll
+        for (int cc = 0; cc < D / 32; ++cc) reg_fence(o[cc]);
+        tc_fence_before();
+        mbar_arrive(b_ofree);
+      } else {
+#pragma unroll
+        for (int cc = 0; cc < D / 32; ++cc)
+#pragma unroll
+          for (int c = 0; c < 32; ++c) o[cc][c] = 0u;
+      }
+      if (rvalid) {
+        const bool any = mx != kNegInf;
+        const float corr = any ? ex2(m_ref - mx * c2) : 0.f;
+        const size_t ml_idx = (size_t(U.b) * p.Hq + U.hq) * size_t(p.Sq) + grow;
+        p.m[ml_idx] = mx * p.scale;
+        p.l[ml_idx] = l * corr;
+        const int64_t orow = int64_t(U.b) * p.o_sb + int64_t(U.hq) * p.o_sh + int64_t(grow) * p.o_sr;
+        if (p.stats_mode) {
+          float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + orow);
+#pragma unroll
+          for (int cc = 0; cc < D / 32; ++cc)
+#pragma unroll
+            for (int c = 0; c < 32; c += 4)
+              dst[(cc * 32 + c) / 4] = make_float4(__uint_as_float(o[cc][c]) * corr,
+                                                   __uint_as_float(o[cc][c + 1]) * corr,
+                                                   __uint_as_float(o[cc][c + 2]) * corr,
+                                                   __uint_as_float(o[cc][c + 3]) * corr);
+        } else {
+          const float inv = l > 0.f ? 1.f / l : 0.f;
+          uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + orow);
+#pragma unroll
+          for (int cc = 0; cc < D / 32; ++cc)
+#pragma unroll
+            for (int c = 0; c < 32; c += 8) {
+              uint4 v;
+              v.x = pack_bf16x2(__uint_as_float(o[cc][c]) * inv, __uint_as_float(o[cc][c + 1]) * inv);
+              v.y = pack_bf16x2(__uint_as_float(o[cc][c + 2]) * inv, __uint_as_float(o[cc][c + 3]) * inv);
+              v.z = pack_bf16x2(__uint_as_float(o[cc][c + 4]) * inv, __uint_as_float(o[cc][c + 5]) * inv);
+              v.w = pack_bf16x2(__uint_as_float(o[cc][c + 6]) * inv, __uint_as_float(o[cc][c + 7]) * inv);
+              dst[(cc * 32 + c) / 8] = v;
+            }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+}  // namespace
+
+int launch_tc_bf16(const TcPlan& plan, int D, int num_sms, void* stream) {
+  const int grid = plan.n_units < num_sms ? plan.n_units : num_sms;
+  if (grid <= 0) return cudaSuccess;
+  cudaError_t e;
+  if (D == 128) {
+    e = cudaFuncSetAttribute(tc_ring_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Cfg<128>::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    tc_ring_kernel<128><<<grid, kThreads, Cfg<128>::kSmemBytes, static_cast<cudaStream_t>(stream)>>>(plan);
+  } else {
+    e = cudaFuncSetAttribute(tc_ring_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Cfg<64>::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    tc_ring_kernel<64><<<grid, kThreads, Cfg<64>::kSmemBytes, static_cast<cudaStream_t>(stream)>>>(plan);
+  }
+  return cudaGetLastError();
+}
+
+int read_and_clear_device_error(int* code) {
+  int v = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_ra_device_error, sizeof(int));
+  if (e != cudaSuccess) return e;
+  *code = v;
+  if (v != 0) {
+    const int zero = 0;
+    e = cudaMemcpyToSymbol(g_ra_device_error, &zero, sizeof(int));
+  }
+  return e;
+}
+
+}  // namespace ra

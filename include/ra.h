@@ -1,0 +1,211 @@
+/*
+ * ra.h - C ABI of a GB300 (sm_103a) library for the chunked forward pass of
+ * ring attention: exact softmax attention computed one key/value chunk at a
+ * time and combined with the online-softmax merge rule.
+ *
+ * Sources (web pages, cited by title and section):
+ *   [EX]   ring-attention exercise "systems-distributed-ring-attention-online-
+ *          softmax": task statement and hints.
+ *   [BLOG] "Ring Attention: Distributed Reads with Online Softmax".
+ *   [GLOS] glossary entry "ring attention".
+ *   [IRIS] pull request "Support ring attention" (IRIS, Triton, MI300X),
+ *          commit messages.
+ *
+ * Common conventions
+ * ------------------
+ * - Every pointer passed to a compute entry point is a DEVICE pointer owned
+ *   by the caller; the library never frees or retains it and allocates no
+ *   device memory of its own for these calls. Descriptor structs are read on
+ *   the host during the call only.
+ * - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
+ *   stream). A returned RA_OK means the work was validated and enqueued.
+ * - Every argument is validated before anything is enqueued. On any non-OK
+ *   status nothing was launched and no output was written;
+ *   ra_last_error() then returns a message for the calling thread.
+ * - Tensors are [batch, head, row, head_dim] with head_dim contiguous and the
+ *   other three axes given by element strides (ra_strides).
+ * - Query head h reads key/value head h / (Hq / Hkv) (grouped heads).
+ * - Scores are s = scale * <q, k>. The row max m is returned in those scaled,
+ *   natural-log units and l = sum exp(s - m) over the keys the row may see.
+ * - Causal masking uses GLOBAL positions ([BLOG] "Causal masks depend on
+ *   global positions"): key j is visible to query i iff pos(j) <= pos(i).
+ *   Positions are described per chunk / query segment by spans.
+ * - A row that sees no key gets O = 0 (or u = 0), l = 0, m = -inf.
+ * - dtype RA_BF16: Q, K, V and O are bfloat16; products are accumulated in
+ *   fp32 on the tensor cores; head_dim must be 64 or 128.
+ *   dtype RA_F32: everything is fp32 on CUDA cores (no TF32); head_dim
+ *   1..128.
+ */
+#ifndef RA_H_
+#define RA_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  RA_OK = 0,
+  RA_ERR_INVALID = 1,      /* bad argument: nothing was launched            */
+  RA_ERR_UNSUPPORTED = 2,  /* valid but outside what this build handles      */
+  RA_ERR_CUDA = 3,         /* a CUDA runtime/driver call failed              */
+  RA_ERR_TIMEOUT = 4       /* a kernel gave up waiting (see ra_device_status) */
+} ra_status;
+
+typedef enum { RA_F32 = 0, RA_BF16 = 1 } ra_dtype;
+
+#define RA_MAX_SPANS 4
+
+/* Rows [r, r + len) of a chunk / segment have global positions
+ * pos0, pos0 + step, ..., pos0 + (len - 1) * step.  step >= 1. */
+typedef struct {
+  int64_t len;
+  int64_t pos0;
+  int64_t step;
+} ra_span;
+
+/* Positions of consecutive rows: the spans are concatenated in order and their
+ * lengths add up to the owner's row count. One span describes a contiguous
+ * shard; two describe a zigzag (early block + late block) shard; a span with
+ * step P describes a striped shard. Positions must lie in [0, 2^31 - 1). */
+typedef struct {
+  int32_t nspan;            /* 1..RA_MAX_SPANS */
+  int32_t reserved;         /* must be 0 */
+  ra_span span[RA_MAX_SPANS];
+} ra_positions;
+
+typedef struct {
+  int64_t batch, head, row; /* element strides; head_dim is contiguous */
+} ra_strides;
+
+/* One key/value chunk ("shard" on the pages). K and V are [B, Hkv, len, D]. */
+typedef struct {
+  const void* k;
+  const void* v;
+  int64_t len;              /* rows in this chunk (0 = empty chunk, skipped) */
+  ra_strides k_strides;
+  ra_strides v_strides;
+  ra_positions pos;         /* global position of each row */
+} ra_kv_chunk;
+
+/* One query segment: the next `len` rows of Q (segments tile Q's rows in
+ * order). With as many segments as chunks, segment r plays device r of the
+ * ring and visits chunks r, r-1, ..., r+1 (mod P): at ring step s it holds the
+ * chunk that started on device r - s ([BLOG] "Partition the sequence across
+ * devices"; [GLOS] algorithm steps (1)-(5)). Otherwise every segment visits
+ * the chunks in index order. The result does not depend on the order beyond
+ * rounding. */
+typedef struct {
+  int64_t len;
+  ra_positions pos;
+} ra_q_segment;
+
+typedef struct {
+  int64_t B, Hq, Hkv, D;
+  int64_t Sq;               /* query rows (sum of the segment lengths) */
+  int32_t dtype;            /* ra_dtype of Q, K, V and O */
+  int32_t causal;           /* 0 or 1 */
+  float scale;              /* score scale; <= 0 selects 1/sqrt(D) */
+  int32_t reserved;         /* must be 0 */
+  ra_strides q_strides;     /* Q: [B, Hq, Sq, D] */
+  ra_strides o_strides;     /* O (ring) or u (chunk stats): [B, Hq, Sq, D] */
+} ra_problem;
+
+/*
+ * ra_chunk_stats - statistics of ONE key/value chunk for every query row,
+ * computed as if that chunk were the only one ([EX] task statement:
+ * attention_chunk_stats returns chunk_output, chunk_sum, chunk_max; [EX] hint
+ * 1: the max-subtraction of scaled dot-product attention, with numerator and
+ * denominator returned separately).
+ *
+ *   u [B, Hq, Sq, D] fp32 (problem->o_strides): sum_j exp(s_ij - m_i) v_j
+ *   l [B, Hq, Sq]    fp32 contiguous:           sum_j exp(s_ij - m_i)
+ *   m [B, Hq, Sq]    fp32 contiguous:           max_j s_ij  (-inf if none)
+ *
+ * q is [B, Hq, Sq, D] of problem->dtype; segs give the query positions
+ * (their ring roles do not matter here).
+ */
+ra_status ra_chunk_stats(const ra_problem* problem, const void* q,
+                         const ra_q_segment* segs, int32_t nsegs,
+                         const ra_kv_chunk* chunk,
+                         float* u, float* l, float* m, void* stream);
+
+/*
+ * ra_merge_stats - the online-softmax merge of two sets of statistics, in
+ * place into the accumulator ([EX] task statement and hint 2; [BLOG] "Do not
+ * average independently normalized shard outputs"):
+ *
+ *   m' = max(m_acc, m_new);  a = exp(m_acc - m'), b = exp(m_new - m')
+ *   u_acc = a u_acc + b u_new;  l_acc = a l_acc + b l_new;  m_acc = m'
+ *
+ * A side with m = -inf contributes nothing (a or b taken as 0). All arrays
+ * are fp32 and contiguous: u [rows, D], l and m [rows]. The _new arrays may
+ * not overlap the _acc arrays unless identical.
+ */
+ra_status ra_merge_stats(int64_t rows, int64_t D,
+                         float* u_acc, float* l_acc, float* m_acc,
+                         const float* u_new, const float* l_new,
+                         const float* m_new, void* stream);
+
+/*
+ * ra_ring_attention - the whole chunked forward pass in one persistent
+ * kernel: each query tile walks the key/value chunks in its segment's ring
+ * order, keeping m, l and the output accumulator on chip across all chunks,
+ * and finally writes O = u / l ([EX] task statement: ring_attention must equal
+ * ordinary attention over the concatenated key/value sequence for any
+ * chunking; [BLOG] "A simple forward schedule"; [GLOS] algorithm (1)-(6)).
+ *
+ *   O [B, Hq, Sq, D] of problem->dtype (problem->o_strides)
+ *   m [B, Hq, Sq] fp32 contiguous: the true row max of scaled scores
+ *   l [B, Hq, Sq] fp32 contiguous: sum exp(s - m) over visible keys
+ *
+ * Causal key/value tiles that lie entirely in a query tile's future are
+ * skipped; only tiles that straddle the diagonal are masked elementwise.
+ * Limits of this build (RA_ERR_UNSUPPORTED beyond them): bf16 at most 32
+ * non-empty chunks and 64 spans over all chunks; fp32 at most 256 chunks and
+ * 320 spans; at most 64 spans over all query segments.
+ */
+ra_status ra_ring_attention(const ra_problem* problem, const void* q,
+                            const ra_q_segment* segs, int32_t nsegs,
+                            const ra_kv_chunk* chunks, int32_t nchunks,
+                            void* o, float* m, float* l, void* stream);
+
+/*
+ * ra_segment_work - host-only bookkeeping for comparing sequence layouts
+ * ([BLOG] "Causal masks depend on global positions": contiguous causal
+ * sharding is imbalanced, paired early/late chunks even it out; [GLOS]
+ * "Variants (1) striped attention"). For each query segment r:
+ *   pairs[r] = number of (query row, key row) pairs of that segment that the
+ *              causal mask leaves visible, for one (batch, head);
+ *   tiles[r] = number of (128-row query tile, 128-row key tile) products the
+ *              bf16 kernel schedules for it after skipping dead tiles.
+ * Either output may be NULL. No device work.
+ */
+ra_status ra_segment_work(const ra_problem* problem,
+                          const ra_q_segment* segs, int32_t nsegs,
+                          const ra_kv_chunk* chunks, int32_t nchunks,
+                          int64_t* pairs, int64_t* tiles);
+
+/*
+ * ra_device_status - waits for `stream`, then reports whether any kernel of
+ * this library gave up on a bounded wait since the last call (RA_ERR_TIMEOUT;
+ * the flag is cleared) or whether the stream holds a CUDA error
+ * (RA_ERR_CUDA). Kernels never spin forever: every wait on the chip has a time
+ * budget after which the kernel records the timeout and exits cleanly.
+ */
+ra_status ra_device_status(void* stream);
+
+/* Message for the calling thread's last non-OK status ("" if none). */
+const char* ra_last_error(void);
+
+/* ABI version of this header: 10000 * major + 100 * minor + patch. */
+int32_t ra_version(void);
+
+#define RA_VERSION 100
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RA_H_ */

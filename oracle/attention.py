@@ -207,24 +207,32 @@ def attention_rows(q, k, v, q_pos, k_pos, causal, scale, rows):
     O = np.zeros((len(rows), D))
     M = np.full(len(rows), NEG_INF)
     L = np.zeros(len(rows))
+    if k.shape[2] == 0:
+        return O, M, L
     by_head = {}
     for idx, (b, h, i) in enumerate(rows):
         by_head.setdefault((b, h // g), []).append((idx, h, i))
     for (b, hk), items in by_head.items():
         kh = _f64(k[b, hk])
         vh = _f64(v[b, hk])
-        for idx, h, i in items:
-            qi = _f64(q[b, h, i])
-            s = scale * (kh @ qi)                          # [Sk]
+        # rows are independent: evaluate a group of them with one product
+        for g0 in range(0, len(items), 32):
+            grp = items[g0:g0 + 32]
+            idx = np.array([it[0] for it in grp])
+            qs = np.stack([_f64(q[b, h, i]) for _, h, i in grp])     # [R, D]
+            s = scale * (qs @ kh.T)                                  # [R, Sk]
             if causal:
-                s = np.where(k_pos <= q_pos[i], s, NEG_INF)
-            if s.size == 0 or not np.isfinite(s.max()):
-                continue                                   # nothing visible
-            mi = s.max()
-            w = np.exp(s - mi)
-            L[idx] = w.sum()
-            M[idx] = mi
-            O[idx] = (w @ vh) / L[idx]
+                qp = np.array([q_pos[i] for _, _, i in grp])
+                s = np.where(k_pos[None, :] <= qp[:, None], s, NEG_INF)
+            mrow = s.max(axis=1)
+            seen = np.isfinite(mrow)
+            shift = np.where(seen, mrow, 0.0)
+            w = np.exp(s - shift[:, None])
+            lrow = w.sum(axis=1)
+            num = w @ vh
+            O[idx] = np.where(seen[:, None], num / np.where(seen, lrow, 1.0)[:, None], 0.0)
+            M[idx] = mrow
+            L[idx] = np.where(seen, lrow, 0.0)
     return O, M, L
 
 

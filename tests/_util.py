@@ -1,0 +1,104 @@
+"""Shared helpers of the parity tests: tolerances, row samples, layout runs."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+from blockwise_attention_online_gb300 import layouts, ring_attention
+
+# fp32 path: max-abs 1e-5 on O and m; l (a sum of up to Sk terms of size <= 1)
+# to 1e-5 relative once it exceeds 1.
+F32_ATOL = 1e-5
+# bf16 path: O max-abs 1e-2; m and l relative 1e-3 (for m near 0 the bound is
+# 1e-3 absolute, a pure relative bound being ill-posed there).
+BF16_O_ATOL = 1e-2
+BF16_ML_RTOL = 1e-3
+
+
+def f64(t):
+    if isinstance(t, torch.Tensor):
+        return t.detach().to("cpu", torch.float64).numpy()
+    return np.asarray(t, dtype=np.float64)
+
+
+def _same_inf(a, b):
+    ia, ib = np.isinf(a), np.isinf(b)
+    assert np.array_equal(ia, ib), "-inf pattern differs"
+    assert np.array_equal(np.sign(a[ia]), np.sign(b[ib]))
+    return ~ia
+
+
+def assert_f32(O, m, l, Oref, mref, lref):
+    O, m, l = f64(O), f64(m), f64(l)
+    assert not np.isnan(O).any() and not np.isnan(l).any()
+    err = np.abs(O - Oref).max() if O.size else 0.0
+    assert err <= F32_ATOL, f"O max-abs {err:.3e}"
+    fin = _same_inf(m, mref)
+    if fin.any():
+        assert np.abs(m[fin] - mref[fin]).max() <= F32_ATOL
+    assert (np.abs(l - lref) <= F32_ATOL * np.maximum(1.0, lref)).all()
+
+
+def assert_bf16(O, m, l, Oref, mref, lref, what=""):
+    O, m, l = f64(O), f64(m), f64(l)
+    assert not np.isnan(O).any() and not np.isnan(l).any(), f"{what}: NaN"
+    err = np.abs(O - Oref).max() if O.size else 0.0
+    assert err <= BF16_O_ATOL, f"{what}: O max-abs {err:.3e}"
+    fin = _same_inf(m, mref)
+    if fin.any():
+        dm = np.abs(m[fin] - mref[fin]) / np.maximum(1.0, np.abs(mref[fin]))
+        assert dm.max() <= BF16_ML_RTOL, f"{what}: m rel {dm.max():.3e}"
+    pos = lref > 0
+    if pos.any():
+        dl = np.abs(l[pos] - lref[pos]) / lref[pos]
+        assert dl.max() <= BF16_ML_RTOL, f"{what}: l rel {dl.max():.3e}"
+    assert np.all(l[~pos] == 0)
+    return err
+
+
+def layout_run(q, k, v, P, kind, causal, scale=None):
+    """Shard global-order q, k, v per ``kind`` over P virtual ranks, run the
+    library's ring kernel, return O, m, l back in global order."""
+    S = k.shape[2]
+    rs = layouts.rank_spans(kind, S, P)
+    kc = layouts.shard(k, kind, P)
+    vc = layouts.shard(v, kind, P)
+    qs = torch.cat(layouts.shard(q, kind, P), dim=2).contiguous()
+    segs = [(S // P, s) for s in rs]       # as many segments as chunks: ring order
+    O, m, l = ring_attention(qs, kc, vc, chunk_spans=rs, q_segments=segs, causal=causal,
+                             scale=scale)
+    O = layouts.to_global(O, kind, P)
+    m = layouts.to_global(m.unsqueeze(-1), kind, P).squeeze(-1)
+    l = layouts.to_global(l.unsqueeze(-1), kind, P).squeeze(-1)
+    return O, m, l
+
+
+def sample_rows(S, boundaries, n_random, seed=1234, tile=128, max_tiles=64):
+    """Row sample: first/second/last rows, +-1 around every given boundary and
+    around (up to ``max_tiles`` evenly spread) tile boundaries, plus random
+    rows drawn with ``seed``."""
+    rows = {0, 1, S - 1}
+    for bd in boundaries:
+        for d in (-1, 0, 1):
+            if 0 <= bd + d < S:
+                rows.add(bd + d)
+    tb = list(range(tile, S, tile))
+    if len(tb) > max_tiles:
+        tb = tb[:: max(1, len(tb) // max_tiles)]
+    for bd in tb:
+        for d in (-1, 0):
+            rows.add(bd + d)
+    rng = np.random.default_rng(seed)
+    rows.update(int(x) for x in rng.integers(0, S, size=n_random))
+    return sorted(rows)
+
+
+def oracle_rows(q, k, v, causal, scale, heads, rows):
+    """fp64 oracle on sampled (head, row) pairs; q, k, v global-order CPU fp32."""
+    S = k.shape[2]
+    pos = np.arange(S)
+    trip = [(0, h, i) for h in heads for i in rows]
+    O, M, L = oracle.attention_rows(q, k, v, np.arange(q.shape[2]), pos, causal, scale, trip)
+    n = len(rows)
+    return (O.reshape(len(heads), n, -1), M.reshape(len(heads), n), L.reshape(len(heads), n))

@@ -1,0 +1,152 @@
+"""CPU-only checks of the C ABI: the library loads, exports every symbol the
+header declares, and rejects invalid arguments before anything is launched.
+Also the host-only bookkeeping (layout spans, per-segment work) against the
+oracle, bit for bit."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import layouts as olay
+from blockwise_attention_online_gb300 import _lib, layouts, segment_work
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _header_symbols():
+    with open(os.path.join(ROOT, "include", "ra.h")) as f:
+        text = f.read()
+    return sorted(set(re.findall(r"\b(ra_[a-z_]+)\s*\(", text)))
+
+
+def test_library_exports_every_header_symbol():
+    lib = _lib.load()
+    declared = _header_symbols()
+    assert set(declared) == set(_lib.EXPORTED)
+    for name in declared:
+        assert hasattr(lib, name), name
+    assert lib.ra_version() == 100
+
+
+def _problem(**kw):
+    p = _lib.Problem()
+    p.B, p.Hq, p.Hkv, p.D, p.Sq = kw.get("B", 1), kw.get("Hq", 2), kw.get("Hkv", 1), \
+        kw.get("D", 128), kw.get("Sq", 256)
+    p.dtype = kw.get("dtype", _lib.RA_BF16)
+    p.causal = kw.get("causal", 0)
+    p.scale = kw.get("scale", 0.0)
+    p.reserved = kw.get("reserved", 0)
+    D, Sq, Hq = p.D, p.Sq, p.Hq
+    p.q_strides = _lib.Strides(Hq * Sq * D, Sq * D, D)
+    p.o_strides = _lib.Strides(Hq * Sq * D, Sq * D, D)
+    return p
+
+
+def _segs(spec):
+    arr = (_lib.QSegment * len(spec))()
+    for i, (n, spans) in enumerate(spec):
+        arr[i].len = n
+        arr[i].pos = _lib.positions(spans)
+    return arr
+
+
+def _chunks(spec, ptr=4096, D=128, Hkv=1):
+    arr = (_lib.KvChunk * len(spec))()
+    for i, (n, spans) in enumerate(spec):
+        arr[i].k = ptr
+        arr[i].v = ptr
+        arr[i].len = n
+        st = _lib.Strides(Hkv * n * D, n * D, D)
+        arr[i].k_strides = st
+        arr[i].v_strides = st
+        arr[i].pos = _lib.positions(spans)
+    return arr
+
+
+def _call(p, segs, nsegs, chunks, nchunks, q=4096, o=4096, m=4096, l=4096):
+    lib = _lib.load()
+    return lib.ra_ring_attention(ctypes.byref(p), q, segs, nsegs, chunks, nchunks, o, m, l, None)
+
+
+GOOD_SEGS = [(256, [(256, 0, 1)])]
+GOOD_CHUNKS = [(128, [(128, 0, 1)]), (128, [(128, 128, 1)])]
+
+
+@pytest.mark.parametrize("bad", [
+    dict(Hq=3, Hkv=2),                 # Hq not a multiple of Hkv
+    dict(D=96),                        # bf16 head_dim outside {64, 128}
+    dict(dtype=7),
+    dict(causal=2),
+    dict(reserved=1),
+    dict(scale=float("nan")),
+    dict(B=0),
+])
+def test_invalid_problem_rejected(bad):
+    p = _problem(**bad)
+    st = _call(p, _segs(GOOD_SEGS), 1, _chunks(GOOD_CHUNKS), 2)
+    assert st in (_lib.RA_ERR_INVALID, _lib.RA_ERR_UNSUPPORTED)
+    assert _lib.load().ra_last_error().decode()
+
+
+def test_invalid_descriptors_rejected():
+    p = _problem()
+    lib = _lib.load()
+    # segment lengths must add up to Sq
+    assert _call(p, _segs([(200, [(200, 0, 1)])]), 1, _chunks(GOOD_CHUNKS), 2) == _lib.RA_ERR_INVALID
+    # span lengths must add up to the segment's length
+    assert _call(p, _segs([(256, [(255, 0, 1)])]), 1, _chunks(GOOD_CHUNKS), 2) == _lib.RA_ERR_INVALID
+    # step must be >= 1
+    assert _call(p, _segs([(256, [(256, 0, 0)])]), 1, _chunks(GOOD_CHUNKS), 2) == _lib.RA_ERR_INVALID
+    # chunk spans must cover the chunk
+    assert _call(p, _segs(GOOD_SEGS), 1, _chunks([(128, [(127, 0, 1)])]), 1) == _lib.RA_ERR_INVALID
+    # positions must stay below 2^31 - 1
+    assert _call(p, _segs([(256, [(256, 2**31 - 100, 1)])]), 1,
+                 _chunks(GOOD_CHUNKS), 2) == _lib.RA_ERR_UNSUPPORTED
+    # misaligned pointer for the TMA path
+    assert _call(p, _segs(GOOD_SEGS), 1, _chunks(GOOD_CHUNKS, ptr=4098), 2) == _lib.RA_ERR_INVALID
+    assert _call(p, _segs(GOOD_SEGS), 1, _chunks(GOOD_CHUNKS), 2, q=4100) == _lib.RA_ERR_INVALID
+    # too many chunks for the bf16 path
+    many = [(1, [(1, i, 1)]) for i in range(33)]
+    p2 = _problem(Sq=33)
+    assert _call(p2, _segs([(33, [(33, 0, 1)])]), 1, _chunks(many), 33) == _lib.RA_ERR_UNSUPPORTED
+    # NULL outputs
+    assert _call(p, _segs(GOOD_SEGS), 1, _chunks(GOOD_CHUNKS), 2, o=None) == _lib.RA_ERR_INVALID
+    assert lib.ra_merge_stats(4, 0, 1, 1, 1, 1, 1, 1, None) == _lib.RA_ERR_INVALID
+    assert lib.ra_merge_stats(-1, 8, 1, 1, 1, 1, 1, 1, None) == _lib.RA_ERR_INVALID
+    assert lib.ra_merge_stats(4, 8, None, 16, 16, 16, 16, 16, None) == _lib.RA_ERR_INVALID
+    # an empty problem is a valid no-op
+    assert _call(_problem(Sq=0), _segs([(0, [(0, 0, 1)])]), 1, _chunks(GOOD_CHUNKS), 2) == _lib.RA_OK
+    assert lib.ra_merge_stats(0, 8, None, None, None, None, None, None, None) == _lib.RA_OK
+
+
+@pytest.mark.parametrize("kind", ["contiguous", "zigzag", "striped"])
+@pytest.mark.parametrize("n,P", [(64, 4), (1024, 8), (96, 2)])
+def test_layout_spans_match_oracle_positions(kind, n, P):
+    got = [layouts.span_positions(s).numpy() for s in layouts.rank_spans(kind, n, P)]
+    want = olay.positions(kind, n, P)
+    for a, b in zip(got, want):
+        assert np.array_equal(a, b)
+    x = torch.arange(n).view(1, 1, n, 1).float()
+    sh = torch.cat(layouts.shard(x, kind, P), dim=2)
+    assert torch.equal(layouts.to_global(sh, kind, P), x)
+
+
+@pytest.mark.parametrize("kind", ["contiguous", "zigzag", "striped"])
+@pytest.mark.parametrize("causal", [False, True])
+def test_segment_work_is_exact(kind, causal):
+    """Visible (query, key) pairs per virtual rank: bit-exact against the
+    oracle's count; the scheduled tile products cover them."""
+    n, P = 4096, 8
+    rs = layouts.rank_spans(kind, n, P)
+    segs = [(n // P, s) for s in rs]
+    pairs, tiles = segment_work(1, 4, 4, 128, segs, [n // P] * P, rs, causal)
+    allk = np.arange(n)
+    want = [oracle.unmasked_pairs(p, allk, causal) for p in olay.positions(kind, n, P)]
+    assert pairs == want
+    assert all(t * 128 * 128 >= pr for t, pr in zip(tiles, pairs))
+    if causal and kind == "zigzag":
+        assert max(pairs) == min(pairs)
