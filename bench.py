@@ -118,6 +118,22 @@ def _dist():
     return world, rank, local
 
 
+def max_over_ranks(x: float, device=None) -> float:
+    """Largest value of ``x`` over all ranks (identity without a process group)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(flops_per_step: float, steps: int, world: int, max_ms: float) -> float:
+    """Work of every rank divided by the slowest rank's time."""
+    return flops_per_step * steps * world / (max_ms * 1e-3) / 1e12
+
+
 def build_workload(name, layout, device):
     import torch
     from blockwise_attention_online_gb300 import layouts, workloads
@@ -182,11 +198,8 @@ def run_gpu(args):
     device_status()
     times = [s.elapsed_time(e) for s, e in zip(starts, ends)]  # ms per launch
     total_ms = sum(times)
-    t = torch.tensor([total_ms], device=dev, dtype=torch.float64)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    max_ms = float(t.item())
-    value = flops * args.steps * world / (max_ms * 1e-3) / 1e12
+    max_ms = max_over_ranks(total_ms, dev)
+    value = whole_job_tflops(flops, args.steps, world, max_ms)
 
     # end to end through the public call: pinned host inputs -> device -> host
     e2e = None
@@ -225,12 +238,9 @@ def run_gpu(args):
         for _ in range(n_e2e):
             e2e_step()
         torch.cuda.synchronize()
-        el = time.perf_counter() - t0
-        te = torch.tensor([el], device=dev, dtype=torch.float64)
-        if world > 1:
-            dist.all_reduce(te, op=dist.ReduceOp.MAX)
-        el = float(te.item())
-        e2e = {"value": round(flops * n_e2e * world / el / 1e12, 3), "unit": "TFLOP/s",
+        el = max_over_ranks(time.perf_counter() - t0, dev)
+        e2e = {"value": round(whole_job_tflops(flops, n_e2e, world, el * 1e3), 3),
+               "unit": "TFLOP/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "steps": n_e2e}
         device_status()
@@ -273,7 +283,7 @@ def run_gpu(args):
         "gpu_launches": args.steps,
         "e2e": e2e,
     }
-    if not args.no_cpu_baseline:
+    if not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
     return line
 
@@ -356,7 +366,7 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--workload", default="bf16_8k")
     ap.add_argument("--layout", default=None)

@@ -156,7 +156,7 @@ __device__ __forceinline__ void record_error(int code) { atomicCAS(&g_ra_device_
 
 // Bounded wait on an mbarrier phase. Returns false (and stops the CTA) when the
 // budget runs out or another warp already gave up.
-__device__ __noinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                       unsigned long long budget, int site) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = globaltimer();
@@ -249,6 +249,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ring_kernel(const __grid_const
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
+  if (warp < 4) {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 80;\n" ::: "memory");
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     int it = 0, qn = 0;
@@ -309,21 +311,21 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ring_kernel(const __grid_const
     constexpr uint32_t kIdQK = idesc_bf16_f32(128, 128, 0, 0);
     constexpr uint32_t kIdPV = idesc_bf16_f32(128, D, 0, 1);
     const uint32_t tS0 = tmem, tO0 = tmem + 256;
+    // descriptor start addresses advance in 16-byte units inside the low word
     auto issue_qk = [&](int t, int st) {
-      const uint32_t qa = sQ + t * C::kTileBytes, ka = sKV + st * C::kTileBytes;
+      const uint64_t qd = sdesc_sw128(sQ + t * C::kTileBytes, 16, 1024);
+      const uint64_t kd = sdesc_sw128(sKV + st * C::kTileBytes, 16, 1024);
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t off = (kk >> 2) * C::kBoxBytes + (kk & 3) * 32;
-        mma_ss(tS0 + 128 * t, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024),
-               kIdQK, kk > 0 ? 1u : 0u);
+        const uint64_t off = uint64_t(((kk >> 2) * C::kBoxBytes + (kk & 3) * 32) >> 4);
+        mma_ss(tS0 + 128 * t, qd + off, kd + off, kIdQK, kk > 0 ? 1u : 0u);
       }
     };
     auto issue_pv = [&](int t, int st, bool acc) {
-      const uint32_t va = sKV + st * C::kTileBytes;
+      const uint64_t vd = sdesc_sw128(sKV + st * C::kTileBytes, C::kBoxBytes, 1024);
 #pragma unroll
       for (int kk = 0; kk < 128 / 16; ++kk) {
-        mma_ts(tO0 + 128 * t, tS0 + 128 * t + kk * 8,
-               sdesc_sw128(va + kk * 16 * 128, C::kBoxBytes, 1024), kIdPV,
+        mma_ts(tO0 + 128 * t, tS0 + 128 * t + kk * 8, vd + uint64_t((kk * 16 * 128) >> 4), kIdPV,
                (acc || kk > 0) ? 1u : 0u);
       }
     };
@@ -413,7 +415,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ring_kernel(const __grid_const
     __syncwarp();
     if (lane == 0) drain_wait(b_done, 0, budget);
     __syncwarp();
-  } else if (warp >= 4) {
+  }
+  } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 208;\n" ::: "memory");
     // ------------------------------------------------------------ softmax
     const int wg = (warp - 4) >> 2;
     const int sub = warp & 3;
@@ -482,40 +486,45 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ring_kernel(const __grid_const
           const float rmax = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
           mx = fmaxf(mx, rmax);
           const float mnew = rmax * c2;
-          if (mnew > m_ref + kRescaleLog2) {
-            const float alpha = ex2(m_ref - mnew);
+          // The O rescale touches TMEM with warp-collective loads and stores, so
+          // the whole warp takes the branch when any of its rows needs it; rows
+          // that do not need it keep their reference max (alpha = 1).
+          const bool grow_ref = mnew > m_ref + kRescaleLog2;
+          if (__any_sync(0xffffffffu, grow_ref)) {
+            const float m_to = grow_ref ? mnew : m_ref;
+            const float alpha = grow_ref ? ex2(m_ref - mnew) : 1.f;
             l *= alpha;
             if (j > 0) {
-#pragma unroll
-              for (int cc = 0; cc < D / 32; ++cc) {
-                uint32_t o[32];
-                tmem_ld32(tO + 32 * cc, o);
+#pragma unroll 1
+              for (int cc = 0; cc < D / 16; ++cc) {
+                uint32_t o[16];
+                tmem_ld16(tO + 16 * cc, o);
                 tmem_ld_wait();
                 reg_fence(o);
 #pragma unroll
-                for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
-                tmem_st32(tO + 32 * cc, o);
+                for (int c = 0; c < 16; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+                tmem_st16(tO + 16 * cc, o);
               }
             }
-            m_ref = mnew;
+            m_ref = m_to;
           }
           const float off = (m_ref == kNegInf) ? 0.f : m_ref;
           float l0 = 0.f, l1 = 0.f;
-          uint32_t pk[2][32];
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
+            // 32 scores -> 16 packed bf16 pairs -> P columns [16 i, 16 i + 16)
+            uint32_t pk[16];
 #pragma unroll
             for (int c = 0; c < 16; ++c) {
               const float a = ex2(fmaf(__uint_as_float(s[i][2 * c]), c2, -off));
               const float b = ex2(fmaf(__uint_as_float(s[i][2 * c + 1]), c2, -off));
               l0 += a;
               l1 += b;
-              pk[i >> 1][(i & 1) * 16 + c] = pack_bf16x2(a, b);
+              pk[c] = pack_bf16x2(a, b);
             }
+            tmem_st16(tS + 16 * i, pk);
           }
           l += l0 + l1;
-          tmem_st32(tS, pk[0]);
-          tmem_st32(tS + 32, pk[1]);
           tmem_st_wait();
           tc_fence_before();
           mbar_arrive(b_pfull);
@@ -527,54 +536,63 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ring_kernel(const __grid_const
         ++oc;
         tc_fence_after();
       }
-      // epilogue: read O, release its TMEM, write this row's results
-      uint32_t o[D / 32][32];
-      if (U.n > 0) {
+      // epilogue: read O in halves (bounded register use), release its TMEM
+      // after the last read, write this row's results
+      const bool any = mx != kNegInf;
+      const float corr = any ? ex2(m_ref - mx * c2) : 0.f;
+      const float fo = p.stats_mode ? corr : (l > 0.f ? 1.f / l : 0.f);
+      const int64_t orow = int64_t(U.b) * p.o_sb + int64_t(U.hq) * p.o_sh + int64_t(grow) * p.o_sr;
+      constexpr int kHalf = D / 64;  // 32-column chunks per half
 #pragma unroll
-        for (int cc = 0; cc < D / 32; ++cc) tmem_ld32(tO + 32 * cc, o[cc]);
-        tmem_ld_wait();
+      for (int h = 0; h < 2; ++h) {
+        uint32_t o[kHalf][32];
+        if (U.n > 0) {
 #pragma unroll
-        for (int cc = 0; cc < D / 32; ++cc) reg_fence(o[cc]);
-        tc_fence_before();
-        mbar_arrive(b_ofree);
-      } else {
+          for (int cc = 0; cc < kHalf; ++cc) tmem_ld32(tO + 32 * (h * kHalf + cc), o[cc]);
+          tmem_ld_wait();
 #pragma unroll
-        for (int cc = 0; cc < D / 32; ++cc)
+          for (int cc = 0; cc < kHalf; ++cc) reg_fence(o[cc]);
+          if (h == 1) {
+            tc_fence_before();
+            mbar_arrive(b_ofree);
+          }
+        } else {
 #pragma unroll
-          for (int c = 0; c < 32; ++c) o[cc][c] = 0u;
+          for (int cc = 0; cc < kHalf; ++cc)
+#pragma unroll
+            for (int c = 0; c < 32; ++c) o[cc][c] = 0u;
+        }
+        if (rvalid) {
+          if (p.stats_mode) {
+            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + orow) + h * (D / 8);
+#pragma unroll
+            for (int cc = 0; cc < kHalf; ++cc)
+#pragma unroll
+              for (int c = 0; c < 32; c += 4)
+                dst[(cc * 32 + c) / 4] = make_float4(__uint_as_float(o[cc][c]) * fo,
+                                                     __uint_as_float(o[cc][c + 1]) * fo,
+                                                     __uint_as_float(o[cc][c + 2]) * fo,
+                                                     __uint_as_float(o[cc][c + 3]) * fo);
+          } else {
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + orow) + h * (D / 16);
+#pragma unroll
+            for (int cc = 0; cc < kHalf; ++cc)
+#pragma unroll
+              for (int c = 0; c < 32; c += 8) {
+                uint4 v;
+                v.x = pack_bf16x2(__uint_as_float(o[cc][c]) * fo, __uint_as_float(o[cc][c + 1]) * fo);
+                v.y = pack_bf16x2(__uint_as_float(o[cc][c + 2]) * fo, __uint_as_float(o[cc][c + 3]) * fo);
+                v.z = pack_bf16x2(__uint_as_float(o[cc][c + 4]) * fo, __uint_as_float(o[cc][c + 5]) * fo);
+                v.w = pack_bf16x2(__uint_as_float(o[cc][c + 6]) * fo, __uint_as_float(o[cc][c + 7]) * fo);
+                dst[(cc * 32 + c) / 8] = v;
+              }
+          }
+        }
       }
       if (rvalid) {
-        const bool any = mx != kNegInf;
-        const float corr = any ? ex2(m_ref - mx * c2) : 0.f;
         const size_t ml_idx = (size_t(U.b) * p.Hq + U.hq) * size_t(p.Sq) + grow;
         p.m[ml_idx] = mx * p.scale;
         p.l[ml_idx] = l * corr;
-        const int64_t orow = int64_t(U.b) * p.o_sb + int64_t(U.hq) * p.o_sh + int64_t(grow) * p.o_sr;
-        if (p.stats_mode) {
-          float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + orow);
-#pragma unroll
-          for (int cc = 0; cc < D / 32; ++cc)
-#pragma unroll
-            for (int c = 0; c < 32; c += 4)
-              dst[(cc * 32 + c) / 4] = make_float4(__uint_as_float(o[cc][c]) * corr,
-                                                   __uint_as_float(o[cc][c + 1]) * corr,
-                                                   __uint_as_float(o[cc][c + 2]) * corr,
-                                                   __uint_as_float(o[cc][c + 3]) * corr);
-        } else {
-          const float inv = l > 0.f ? 1.f / l : 0.f;
-          uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + orow);
-#pragma unroll
-          for (int cc = 0; cc < D / 32; ++cc)
-#pragma unroll
-            for (int c = 0; c < 32; c += 8) {
-              uint4 v;
-              v.x = pack_bf16x2(__uint_as_float(o[cc][c]) * inv, __uint_as_float(o[cc][c + 1]) * inv);
-              v.y = pack_bf16x2(__uint_as_float(o[cc][c + 2]) * inv, __uint_as_float(o[cc][c + 3]) * inv);
-              v.z = pack_bf16x2(__uint_as_float(o[cc][c + 4]) * inv, __uint_as_float(o[cc][c + 5]) * inv);
-              v.w = pack_bf16x2(__uint_as_float(o[cc][c + 6]) * inv, __uint_as_float(o[cc][c + 7]) * inv);
-              dst[(cc * 32 + c) / 8] = v;
-            }
-        }
       }
     }
   }

@@ -94,8 +94,22 @@ def sample_rows(S, boundaries, n_random, seed=1234, tile=128, max_tiles=64):
     return sorted(rows)
 
 
+class LazyHeads:
+    """Read-only view handing the oracle one (batch, head) slice at a time as a
+    float32 host array, so that device tensors of long sequences never have to
+    be copied to the host whole."""
+
+    def __init__(self, t):
+        self.t = t
+        self.shape = tuple(t.shape)
+
+    def __getitem__(self, idx):
+        return self.t[idx].float().cpu().numpy()
+
+
 def oracle_rows(q, k, v, causal, scale, heads, rows):
-    """fp64 oracle on sampled (head, row) pairs; q, k, v global-order CPU fp32."""
+    """fp64 oracle on sampled (head, row) pairs of global-order q, k, v."""
+    q, k, v = LazyHeads(q), LazyHeads(k), LazyHeads(v)
     S = k.shape[2]
     pos = np.arange(S)
     trip = [(0, h, i) for h in heads for i in rows]
