@@ -436,7 +436,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ring_kernel(const __grid_const
       const int grow = U.qrow0 + wg * 128 + r;
       const bool rvalid = grow < p.Sq;
       const int qpos = rvalid ? row_position(p, grow) : 0x7ffffffe;
-      float m_ref = kNegInf, mx = kNegInf, l = 0.f;
+      float m_ref = kNegInf, mx = kNegInf, l = 0.f, lr = 0.f;
       int j = 0;
       if (U.n > 0) {
         TileIter iter;
@@ -460,30 +460,22 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ring_kernel(const __grid_const
             const int first = sg.pos0 + sg.step * (128 * t);
             L = qpos < first ? 0 : min(L, (qpos - first) / sg.step + 1);
           }
-          float mx0 = kNegInf, mx1 = kNegInf, mx2 = kNegInf, mx3 = kNegInf;
-          if (L >= 128) {
-#pragma unroll
-            for (int c = 0; c < 32; ++c) {
-              mx0 = fmaxf(mx0, __uint_as_float(s[0][c]));
-              mx1 = fmaxf(mx1, __uint_as_float(s[1][c]));
-              mx2 = fmaxf(mx2, __uint_as_float(s[2][c]));
-              mx3 = fmaxf(mx3, __uint_as_float(s[3][c]));
-            }
-          } else {
+          if (L < 128) {
 #pragma unroll
             for (int i = 0; i < 4; ++i)
 #pragma unroll
               for (int c = 0; c < 32; ++c)
                 if (32 * i + c >= L) s[i][c] = 0xff800000u;  // -inf
-#pragma unroll
-            for (int c = 0; c < 32; ++c) {
-              mx0 = fmaxf(mx0, __uint_as_float(s[0][c]));
-              mx1 = fmaxf(mx1, __uint_as_float(s[1][c]));
-              mx2 = fmaxf(mx2, __uint_as_float(s[2][c]));
-              mx3 = fmaxf(mx3, __uint_as_float(s[3][c]));
-            }
           }
-          const float rmax = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
+          float mx0 = kNegInf, mx1 = kNegInf, mx2 = kNegInf, mx3 = kNegInf;
+#pragma unroll
+          for (int c = 0; c < 32; c += 2) {
+            mx0 = max3(mx0, __uint_as_float(s[0][c]), __uint_as_float(s[0][c + 1]));
+            mx1 = max3(mx1, __uint_as_float(s[1][c]), __uint_as_float(s[1][c + 1]));
+            mx2 = max3(mx2, __uint_as_float(s[2][c]), __uint_as_float(s[2][c + 1]));
+            mx3 = max3(mx3, __uint_as_float(s[3][c]), __uint_as_float(s[3][c + 1]));
+          }
+          const float rmax = fmaxf(max3(mx0, mx1, mx2), mx3);
           mx = fmaxf(mx, rmax);
           const float mnew = rmax * c2;
           // The O rescale touches TMEM with warp-collective loads and stores, so
@@ -494,6 +486,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ring_kernel(const __grid_const
             const float m_to = grow_ref ? mnew : m_ref;
             const float alpha = grow_ref ? ex2(m_ref - mnew) : 1.f;
             l *= alpha;
+            lr *= alpha;
             if (j > 0) {
 #pragma unroll 1
               for (int cc = 0; cc < D / 16; ++cc) {
@@ -509,22 +502,33 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ring_kernel(const __grid_const
             m_ref = m_to;
           }
           const float off = (m_ref == kNegInf) ? 0.f : m_ref;
-          float l0 = 0.f, l1 = 0.f;
+          // p = 2^(s*c2 - off) two at a time; l sums the fp32 p (returned), lr
+          // sums the bf16-rounded p that P.V actually uses (normalises O)
+          const uint64_t c2x2 = f2(c2, c2), noff = f2(-off, -off);
+          uint64_t lacc = 0, racc = 0;
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
-            // 32 scores -> 16 packed bf16 pairs -> P columns [16 i, 16 i + 16)
             uint32_t pk[16];
 #pragma unroll
             for (int c = 0; c < 16; ++c) {
-              const float a = ex2(fmaf(__uint_as_float(s[i][2 * c]), c2, -off));
-              const float b = ex2(fmaf(__uint_as_float(s[i][2 * c + 1]), c2, -off));
-              l0 += a;
-              l1 += b;
-              pk[c] = pack_bf16x2(a, b);
+              float x0, x1;
+              f2_split(fma2(f2(__uint_as_float(s[i][2 * c]), __uint_as_float(s[i][2 * c + 1])),
+                            c2x2, noff), x0, x1);
+              const float a = ex2(x0), b = ex2(x1);
+              lacc = add2(lacc, f2(a, b));
+              const uint32_t w = pack_bf16x2(a, b);
+              racc = add2(racc, f2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u)));
+              pk[c] = w;
             }
             tmem_st16(tS + 16 * i, pk);
           }
-          l += l0 + l1;
+          {
+            float a0, a1, r0, r1;
+            f2_split(lacc, a0, a1);
+            f2_split(racc, r0, r1);
+            l += a0 + a1;
+            lr += r0 + r1;
+          }
           tmem_st_wait();
           tc_fence_before();
           mbar_arrive(b_pfull);
@@ -540,7 +544,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ring_kernel(const __grid_const
       // after the last read, write this row's results
       const bool any = mx != kNegInf;
       const float corr = any ? ex2(m_ref - mx * c2) : 0.f;
-      const float fo = p.stats_mode ? corr : (l > 0.f ? 1.f / l : 0.f);
+      const float fo = p.stats_mode ? corr * (lr > 0.f ? l / lr : 0.f) : (lr > 0.f ? 1.f / lr : 0.f);
       const int64_t orow = int64_t(U.b) * p.o_sb + int64_t(U.hq) * p.o_sh + int64_t(grow) * p.o_sr;
       constexpr int kHalf = D / 64;  // 32-column chunks per half
 #pragma unroll
