@@ -48,7 +48,7 @@ class QSegment(ctypes.Structure):
 class Problem(ctypes.Structure):
     _fields_ = [("B", c_int64), ("Hq", c_int64), ("Hkv", c_int64), ("D", c_int64),
                 ("Sq", c_int64), ("dtype", c_int32), ("causal", c_int32),
-                ("scale", c_float), ("reserved", c_int32),
+                ("scale", c_float), ("o_fp32", c_int32),
                 ("q_strides", Strides), ("o_strides", Strides)]
 
 

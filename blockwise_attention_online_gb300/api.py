@@ -84,14 +84,15 @@ def _problem(q, Hkv, causal, scale, out_strides):
     pb.dtype = _dtype_code(q)
     pb.causal = 1 if causal else 0
     pb.scale = float(scale) if scale is not None else 0.0
-    pb.reserved = 0
+    pb.o_fp32 = 0
     pb.q_strides = _strides(q)
     pb.o_strides = out_strides
     return pb
 
 
 def ring_attention(q, k_chunks, v_chunks, *, chunk_spans=None, q_segments=None,
-                   causal=False, scale=None, out=None, m=None, l=None, stream=None):
+                   causal=False, scale=None, out=None, m=None, l=None, out_dtype=None,
+                   stream=None):
     """Chunked forward pass over key/value chunks (one persistent kernel).
 
     q: [B, Hq, Sq, D] (bf16 or fp32, CUDA). k_chunks / v_chunks: lists of
@@ -100,19 +101,24 @@ def ring_attention(q, k_chunks, v_chunks, *, chunk_spans=None, q_segments=None,
     q_segments: list of (len, spans) splitting Q's rows (default: one segment
     at positions 0..Sq-1); with as many segments as chunks, segment r walks
     the chunks in ring order starting at chunk r.
-    Returns (O [B, Hq, Sq, D] like q, m [B, Hq, Sq] fp32, l [B, Hq, Sq] fp32).
+    out_dtype: torch.float32 to receive O in fp32 from bf16 inputs (default:
+    the dtype of q, or of ``out`` when given).
+    Returns (O [B, Hq, Sq, D], m [B, Hq, Sq] fp32, l [B, Hq, Sq] fp32).
     """
     lib = load()
     _check_cuda(q, "q")
     B, Hq, Sq, D = q.shape
     Hkv = k_chunks[0].shape[1] if k_chunks else Hq
     if out is None:
-        out = torch.empty_like(q)
+        out = torch.empty(q.shape, device=q.device, dtype=out_dtype or q.dtype)
+    if out.dtype not in (q.dtype, torch.float32):
+        raise TypeError("O must have the dtype of q or float32")
     if m is None:
         m = torch.empty(B, Hq, Sq, device=q.device, dtype=torch.float32)
     if l is None:
         l = torch.empty(B, Hq, Sq, device=q.device, dtype=torch.float32)
     pb = _problem(q, Hkv, causal, scale, _strides(out))
+    pb.o_fp32 = 1 if (out.dtype == torch.float32 and q.dtype != torch.float32) else 0
     segs, nsegs = _segments(q, q_segments)
     chs, nch = _chunks(k_chunks, v_chunks, chunk_spans)
     check(lib.ra_ring_attention(ctypes.byref(pb), q.data_ptr(), segs, nsegs, chs, nch,
@@ -169,7 +175,7 @@ def segment_work(B, Hq, Hkv, D, q_segments, chunk_lens, chunk_spans, causal, dty
     Sq = sum(int(n) for n, _ in q_segments)
     pb = Problem()
     pb.B, pb.Hq, pb.Hkv, pb.D, pb.Sq = B, Hq, Hkv, D, Sq
-    pb.dtype, pb.causal, pb.scale, pb.reserved = dtype, 1 if causal else 0, 0.0, 0
+    pb.dtype, pb.causal, pb.scale, pb.o_fp32 = dtype, 1 if causal else 0, 0.0, 0
     pb.q_strides = Strides(Hq * Sq * D, Sq * D, D)
     pb.o_strides = pb.q_strides
     segs = (QSegment * len(q_segments))()

@@ -103,7 +103,7 @@ ra_status validate(const ra_problem* pb, const void* q, const ra_q_segment* segs
   if (p.dtype != RA_F32 && p.dtype != RA_BF16)
     return fail(RA_ERR_INVALID, "unknown dtype %d", p.dtype);
   if (p.causal != 0 && p.causal != 1) return fail(RA_ERR_INVALID, "causal must be 0 or 1");
-  if (p.reserved != 0) return fail(RA_ERR_INVALID, "problem.reserved must be 0");
+  if (p.o_fp32 != 0 && p.o_fp32 != 1) return fail(RA_ERR_INVALID, "o_fp32 must be 0 or 1");
   if (!std::isfinite(p.scale)) return fail(RA_ERR_INVALID, "scale is not finite");
   if (p.dtype == RA_BF16 && p.D != 64 && p.D != 128)
     return fail(RA_ERR_UNSUPPORTED, "bf16 path supports head_dim 64 or 128, got %lld",
@@ -277,7 +277,8 @@ ra_status run_tc(const Common& c, const ra_problem& p, const void* q,
   if (!aligned16(q)) return fail(RA_ERR_INVALID, "q must be 16-byte aligned");
   if (!aligned16(out)) return fail(RA_ERR_INVALID, "output must be 16-byte aligned");
   if ((st = check_bf16_strides(p.q_strides, c.Sq, c.Hq, c.B, "q_strides")) != RA_OK) return st;
-  const int64_t ovec = stats_mode ? 4 : 8;  // 16-byte row segments
+  const bool out_f32 = stats_mode || p.o_fp32 == 1;
+  const int64_t ovec = out_f32 ? 4 : 8;  // 16-byte row segments
   if ((c.Sq > 1 && p.o_strides.row % ovec) || (c.Hq > 1 && p.o_strides.head % ovec) ||
       (c.B > 1 && p.o_strides.batch % ovec))
     return fail(RA_ERR_INVALID, "output strides must be multiples of %lld elements",
@@ -312,6 +313,7 @@ ra_status run_tc(const Common& c, const ra_problem& p, const void* q,
   plan.ring = c.ring ? 1 : 0; plan.n_chunks = c.nchunks;
   plan.scale = c.scale;
   plan.scale_log2 = float(double(c.scale) * 1.4426950408889634);
+  plan.o_fp32 = out_f32 ? 1 : 0;
   fill_q_pieces(c, plan.qp, &plan.n_qpieces);
   plan.n_kvsegs = int32_t(c.kvspans.size());
   for (size_t i = 0; i < c.kvspans.size(); ++i) {

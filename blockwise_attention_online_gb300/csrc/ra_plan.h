@@ -43,6 +43,7 @@ struct alignas(128) TcPlan {
   int32_t B, Hq, Hkv, Sq;
   int32_t causal, stats_mode, ring, n_chunks;
   float scale, scale_log2;
+  int32_t o_fp32;                    // ring mode: O written as fp32 instead of bf16
   int32_t n_qpieces, n_kvsegs, n_qpairs, has_order;
   int32_t n_units;
   int32_t chunk_seg_begin[kTcMaxChunks + 1];

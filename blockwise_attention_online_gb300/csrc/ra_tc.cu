@@ -155,16 +155,21 @@ struct TileIter {
 __device__ __forceinline__ void record_error(int code) { atomicCAS(&g_ra_device_error, 0, code); }
 
 // Bounded wait on an mbarrier phase. Returns false (and stops the CTA) when the
-// budget runs out or another warp already gave up.
+// budget runs out or another warp already gave up. The fast path is a plain
+// try_wait loop (try_wait itself sleeps until the phase completes or a short
+// hardware limit passes); the clock is only read every 1024 failed tries, so
+// a hand-off between warps costs no timer latency.
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                      unsigned long long budget, int site) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const unsigned long long t0 = globaltimer();
+                                         unsigned long long budget, int site) {
+  unsigned long long t0 = 0;
   for (uint32_t n = 1;; ++n) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((n & 63u) == 0) {
+    if ((n & 1023u) == 0) {
       if (*abort_flag) return false;
-      if (globaltimer() - t0 > budget) {
+      const unsigned long long now = globaltimer();
+      if (t0 == 0) {
+        t0 = now;
+      } else if (now - t0 > budget) {
         *abort_flag = 1;
         record_error(0x100 | site);
         return false;
@@ -442,6 +447,17 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ring_kernel(const __grid_const
         TileIter iter;
         int ks, t;
         while (iter.next(p, U, ks, t)) {
+          // visible columns of this row: a prefix [0, L) of the tile (known
+          // before S arrives)
+          int L;
+          {
+            const KvSeg& sg = p.ks[ks];
+            L = min(128, sg.len - 128 * t);
+            if (p.causal) {
+              const int first = sg.pos0 + sg.step * (128 * t);
+              L = qpos < first ? 0 : min(L, (qpos - first) / sg.step + 1);
+            }
+          }
           ok = warp_wait(b_sfull, sc & 1, abort_flag, budget, kSiteSoftS);
           if (!ok) break;
           ++sc;
@@ -452,14 +468,6 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ring_kernel(const __grid_const
           tmem_ld_wait();
 #pragma unroll
           for (int i = 0; i < 4; ++i) reg_fence(s[i]);
-
-          // visible columns of this row: a prefix [0, L) of the tile
-          const KvSeg& sg = p.ks[ks];
-          int L = min(128, sg.len - 128 * t);
-          if (p.causal) {
-            const int first = sg.pos0 + sg.step * (128 * t);
-            L = qpos < first ? 0 : min(L, (qpos - first) / sg.step + 1);
-          }
           if (L < 128) {
 #pragma unroll
             for (int i = 0; i < 4; ++i)
@@ -505,7 +513,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ring_kernel(const __grid_const
           // p = 2^(s*c2 - off) two at a time; l sums the fp32 p (returned), lr
           // sums the bf16-rounded p that P.V actually uses (normalises O)
           const uint64_t c2x2 = f2(c2, c2), noff = f2(-off, -off);
-          uint64_t lacc = 0, racc = 0;
+          uint64_t lacc[2] = {0, 0}, racc[2] = {0, 0};
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             uint32_t pk[16];
@@ -515,19 +523,21 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ring_kernel(const __grid_const
               f2_split(fma2(f2(__uint_as_float(s[i][2 * c]), __uint_as_float(s[i][2 * c + 1])),
                             c2x2, noff), x0, x1);
               const float a = ex2(x0), b = ex2(x1);
-              lacc = add2(lacc, f2(a, b));
+              lacc[c & 1] = add2(lacc[c & 1], f2(a, b));
               const uint32_t w = pack_bf16x2(a, b);
-              racc = add2(racc, f2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u)));
+              racc[c & 1] = add2(racc[c & 1], f2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u)));
               pk[c] = w;
             }
             tmem_st16(tS + 16 * i, pk);
           }
           {
-            float a0, a1, r0, r1;
-            f2_split(lacc, a0, a1);
-            f2_split(racc, r0, r1);
-            l += a0 + a1;
-            lr += r0 + r1;
+            float a0, a1, a2, a3, r0, r1, r2, r3;
+            f2_split(lacc[0], a0, a1);
+            f2_split(lacc[1], a2, a3);
+            f2_split(racc[0], r0, r1);
+            f2_split(racc[1], r2, r3);
+            l += (a0 + a1) + (a2 + a3);
+            lr += (r0 + r1) + (r2 + r3);
           }
           tmem_st_wait();
           tc_fence_before();
@@ -567,7 +577,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ring_kernel(const __grid_const
             for (int c = 0; c < 32; ++c) o[cc][c] = 0u;
         }
         if (rvalid) {
-          if (p.stats_mode) {
+          if (p.o_fp32) {
             float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + orow) + h * (D / 8);
 #pragma unroll
             for (int cc = 0; cc < kHalf; ++cc)

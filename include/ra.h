@@ -107,7 +107,9 @@ typedef struct {
   int32_t dtype;            /* ra_dtype of Q, K, V and O */
   int32_t causal;           /* 0 or 1 */
   float scale;              /* score scale; <= 0 selects 1/sqrt(D) */
-  int32_t reserved;         /* must be 0 */
+  int32_t o_fp32;           /* 1: write O in fp32 even for bf16 inputs; 0: O has
+                               the input dtype. (A bf16 O carries its own
+                               rounding of up to 2^-9 relative.) */
   ra_strides q_strides;     /* Q: [B, Hq, Sq, D] */
   ra_strides o_strides;     /* O (ring) or u (chunk stats): [B, Hq, Sq, D] */
 } ra_problem;
@@ -156,7 +158,8 @@ ra_status ra_merge_stats(int64_t rows, int64_t D,
  * ordinary attention over the concatenated key/value sequence for any
  * chunking; [BLOG] "A simple forward schedule"; [GLOS] algorithm (1)-(6)).
  *
- *   O [B, Hq, Sq, D] of problem->dtype (problem->o_strides)
+ *   O [B, Hq, Sq, D] of problem->dtype, or fp32 if problem->o_fp32
+ *     (problem->o_strides)
  *   m [B, Hq, Sq] fp32 contiguous: the true row max of scaled scores
  *   l [B, Hq, Sq] fp32 contiguous: sum exp(s - m) over visible keys
  *

@@ -39,7 +39,7 @@ def _problem(**kw):
     p.dtype = kw.get("dtype", _lib.RA_BF16)
     p.causal = kw.get("causal", 0)
     p.scale = kw.get("scale", 0.0)
-    p.reserved = kw.get("reserved", 0)
+    p.o_fp32 = kw.get("o_fp32", 0)
     D, Sq, Hq = p.D, p.Sq, p.Hq
     p.q_strides = _lib.Strides(Hq * Sq * D, Sq * D, D)
     p.o_strides = _lib.Strides(Hq * Sq * D, Sq * D, D)
@@ -81,7 +81,7 @@ GOOD_CHUNKS = [(128, [(128, 0, 1)]), (128, [(128, 128, 1)])]
     dict(D=96),                        # bf16 head_dim outside {64, 128}
     dict(dtype=7),
     dict(causal=2),
-    dict(reserved=1),
+    dict(o_fp32=2),
     dict(scale=float("nan")),
     dict(B=0),
 ])

@@ -208,6 +208,22 @@ def test_bf16_fully_masked_rows():
     assert torch.all(O == 0) and torch.all(l == 0) and torch.all(torch.isneginf(m))
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_bf16_fp32_output_matches_bf16_output(causal):
+    """The fp32-O option changes only the final store: the bf16 O is the fp32
+    O rounded to nearest even, and m, l are identical."""
+    q, k, v = _bf16_inputs(1, 2, 2, 700, 128, seed=23)
+    kc = _split(k.to(DEV), [300, 400]); vc = _split(v.to(DEV), [300, 400])
+    O32, m32, l32 = ring_attention(q.to(DEV), kc, vc, causal=causal, out_dtype=torch.float32)
+    O16, m16, l16 = ring_attention(q.to(DEV), kc, vc, causal=causal)
+    device_status()
+    assert O32.dtype == torch.float32 and O16.dtype == torch.bfloat16
+    assert torch.equal(O32.to(torch.bfloat16), O16)
+    assert torch.equal(m32, m16) and torch.equal(l32, l16)
+    ref = _full_ref(q, k, v, causal, 1 / math.sqrt(128))
+    assert_bf16(O32, m32, l32, *ref, what="fp32 O")
+
+
 def test_bf16_cfg2_full_oracle():
     """bf16, 8 heads, 8192 x 8192, head_dim 128, 8 contiguous chunks of 1024 in
     ring order over 8 query segments; every row checked."""
