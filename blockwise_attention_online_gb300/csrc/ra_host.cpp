@@ -10,6 +10,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -325,29 +326,83 @@ ra_status run_tc(const Common& c, const ra_problem& p, const void* q,
 
   const int64_t npairs = (c.Sq + ra::kTcRowsPerUnit - 1) / ra::kTcRowsPerUnit;
   plan.n_qpairs = int32_t(npairs);
-  const int64_t units = npairs * c.B * c.Hq;
+  const int64_t BH = c.B * c.Hq;
+  const int64_t units = npairs * BH;
   if (units > (int64_t(1) << 31) - 1) return fail(RA_ERR_UNSUPPORTED, "too many work units");
   plan.n_units = int32_t(units);
+  if (units == 0) return ok();
+
+  // live key tiles of every query-tile pair (the same for every head)
+  std::vector<int64_t> work(npairs, 0);
+  for (int64_t qp = 0; qp < npairs; ++qp) {
+    int64_t r0 = qp * ra::kTcRowsPerUnit, r1 = std::min(c.Sq, r0 + ra::kTcRowsPerUnit);
+    int64_t qmax = qmax_of_rows(c.qspans, r0, r1);
+    for (const Span& kv : c.kvspans) work[qp] += live_tiles(kv, qmax, c.causal != 0);
+  }
+  // visit order of the pairs: longest first when the work differs (causal)
+  std::vector<int32_t> order(npairs);
+  std::iota(order.begin(), order.end(), 0);
   plan.has_order = 0;
   if (npairs <= ra::kTcMaxOrder && c.causal) {
-    // longest-first: q-tile pairs with more live key tiles go first
-    std::vector<int64_t> work(npairs, 0);
-    for (int64_t qp = 0; qp < npairs; ++qp) {
-      int64_t r0 = qp * ra::kTcRowsPerUnit, r1 = std::min(c.Sq, r0 + ra::kTcRowsPerUnit);
-      int64_t qmax = qmax_of_rows(c.qspans, r0, r1);
-      for (const Span& kv : c.kvspans) work[qp] += live_tiles(kv, qmax, true);
-    }
-    std::vector<int32_t> idx(npairs);
-    std::iota(idx.begin(), idx.end(), 0);
-    std::stable_sort(idx.begin(), idx.end(),
+    std::stable_sort(order.begin(), order.end(),
                      [&](int32_t a, int32_t b) { return work[a] > work[b]; });
-    for (int64_t i = 0; i < npairs; ++i) plan.order[i] = uint16_t(idx[i]);
+    for (int64_t i = 0; i < npairs; ++i) plan.order[i] = uint16_t(order[i]);
     plan.has_order = 1;
   }
-  if (units == 0) return ok();
+  auto unit_tiles = [&](int64_t u) { return work[order[u / BH]]; };
+
   const int sms = num_sms();
   if (sms <= 0) return cuda_status(cudaErrorNoDevice, "querying the SM count");
-  return cuda_status(ra::launch_tc_bf16(plan, int(c.D), sms, stream), "bf16 ring kernel launch");
+  int64_t total_tiles = 0;
+  for (int64_t qp = 0; qp < npairs; ++qp) total_tiles += work[qp] * BH;
+  // one CTA per SM; small problems use fewer CTAs (at least ~8 tiles each)
+  int64_t G = std::min<int64_t>(std::min(sms, ra::kTcMaxGrid), std::max<int64_t>(1, total_tiles / 8));
+  if (units >= G) G = std::min(sms, ra::kTcMaxGrid);
+  // whole rounds stay data-parallel; the last one to two rounds are split by tiles
+  int64_t R = units >= 2 * G ? units / G - 1 : 0;
+  int64_t sk_units = units - R * G;
+  if (sk_units > ra::kTcMaxSkUnits) {  // cannot happen with G <= kTcMaxGrid
+    R = units / G;
+    sk_units = units - R * G;
+  }
+  plan.grid = int32_t(G);
+  plan.dp_rounds = int32_t(R);
+  plan.sk_units = int32_t(sk_units);
+  int64_t T = 0;
+  plan.sk_prefix[0] = 0;
+  for (int64_t i = 0; i < sk_units; ++i) {
+    T += unit_tiles(R * G + i);
+    plan.sk_prefix[i + 1] = int32_t(T);
+  }
+  if (T > (int64_t(1) << 30)) return fail(RA_ERR_UNSUPPORTED, "stream-K range too large");
+  plan.sk_total = int32_t(T);
+  // does any CTA boundary fall strictly inside a unit?
+  bool split = false;
+  for (int64_t cta = 1; cta < G && !split; ++cta) {
+    const int64_t a = cta * T / G;
+    for (int64_t i = 0; i < sk_units; ++i)
+      if (plan.sk_prefix[i] < a && a < plan.sk_prefix[i + 1]) { split = true; break; }
+  }
+  static std::atomic<unsigned> epoch_counter{0};
+  unsigned ep = ++epoch_counter;
+  if (ep == 0) ep = ++epoch_counter;
+  plan.epoch = ep;
+  void* scratch = nullptr;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  if (split) {
+    const size_t bytes = ra::tc_scratch_bytes(int(G), int(c.D));
+    cudaError_t e = cudaMallocAsync(&scratch, bytes, cs);
+    if (e != cudaSuccess) return cuda_status(e, "allocating stream-K scratch");
+    ra::tc_scratch_carve(scratch, int(G), int(c.D), &plan.scratch);
+    e = cudaMemsetAsync(plan.scratch.flags, 0, size_t(G) * 2 * sizeof(unsigned), cs);
+    if (e != cudaSuccess) {
+      cudaFreeAsync(scratch, cs);
+      return cuda_status(e, "clearing stream-K flags");
+    }
+  }
+  const int err = ra::launch_tc_bf16(plan, int(c.D), stream);
+  if (scratch) cudaFreeAsync(scratch, cs);
+  return cuda_status(err, "bf16 ring kernel launch");
 }
 
 // ----------------------------------------------------------- fp32 plan

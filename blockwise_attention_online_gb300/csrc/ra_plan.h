@@ -30,6 +30,17 @@ constexpr int kTcMaxChunks = 32;
 constexpr int kTcMaxKvSegs = 64;
 constexpr int kTcMaxOrder = 8192;  // q-tile pairs that can be LPT-ordered
 constexpr int kTcRowsPerUnit = 256;  // two 128-row query tiles per work unit
+constexpr int kTcMaxSkUnits = 320;   // units in the stream-K tail (< 2 x grid)
+constexpr int kTcMaxGrid = 160;      // CTAs of one launch (one per SM)
+
+// Scratch of the stream-K tail: one slot per CTA holds the partial results of
+// the unit that CTA started mid-way (raw O, then per row m_ref, max, l, l_r),
+// published by an epoch flag per query tile.
+struct TcScratch {
+  float* o;         // [grid][2][128][D]
+  float4* stats;    // [grid][2][128]
+  unsigned* flags;  // [grid][2]
+};
 
 struct alignas(128) TcPlan {
   CUtensorMap qmap;                  // Q  [B, Hq, Sq, D] bf16, box 64 x 128
@@ -46,6 +57,12 @@ struct alignas(128) TcPlan {
   int32_t o_fp32;                    // ring mode: O written as fp32 instead of bf16
   int32_t n_qpieces, n_kvsegs, n_qpairs, has_order;
   int32_t n_units;
+  // work split: every CTA first takes dp_rounds whole units round-robin, then
+  // its share [c*T/G, (c+1)*T/G) of the T key tiles of units dp_rounds*G ..
+  int32_t grid, dp_rounds, sk_units, sk_total;
+  unsigned epoch;                    // value a published partial carries
+  TcScratch scratch;                 // null pointers when no unit is split
+  int32_t sk_prefix[kTcMaxSkUnits + 1];
   int32_t chunk_seg_begin[kTcMaxChunks + 1];
   QPiece qp[kMaxQPieces];
   KvSeg ks[kTcMaxKvSegs];
@@ -81,7 +98,9 @@ struct SimtPlan {
 static_assert(sizeof(SimtPlan) <= 32000, "fp32 plan must fit the parameter space");
 
 // Kernel launchers (defined in the .cu files; return a cudaError_t as int).
-int launch_tc_bf16(const TcPlan& plan, int D, int num_sms, void* stream);
+int launch_tc_bf16(const TcPlan& plan, int D, void* stream);
+size_t tc_scratch_bytes(int grid, int D);
+void tc_scratch_carve(void* base, int grid, int D, TcScratch* s);
 int launch_simt_f32(const SimtPlan& plan, void* stream);
 int launch_merge_f32(int64_t rows, int64_t D, float* u_acc, float* l_acc,
                      float* m_acc, const float* u_new, const float* l_new,

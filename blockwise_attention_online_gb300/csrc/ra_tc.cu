@@ -129,6 +129,30 @@ __device__ __forceinline__ void decode_unit(const TcPlan& p, int u, Unit& U) {
 struct TileIter {
   int s, ks, ks_end, t, nlive;
   __device__ __forceinline__ TileIter() : s(-1), ks(0), ks_end(0), t(0), nlive(0) {}
+  // Position the walk on tile number `skip` of the unit (whole spans are
+  // stepped over at once).
+  __device__ __forceinline__ void seek(const TcPlan& p, const Unit& U, int skip) {
+    while (skip > 0) {
+      if (t < nlive) {
+        const int take = min(skip, nlive - t);
+        t += take;
+        skip -= take;
+        continue;
+      }
+      ++ks;
+      if (ks < ks_end) {
+        t = 0;
+        nlive = live_tiles(p, ks, U.qmax);
+        continue;
+      }
+      if (++s >= p.n_chunks) return;
+      const int c = p.ring ? (U.qseg - s + p.n_chunks) % p.n_chunks : s;
+      ks = p.chunk_seg_begin[c] - 1;
+      ks_end = p.chunk_seg_begin[c + 1];
+      t = 0;
+      nlive = 0;
+    }
+  }
   __device__ __forceinline__ bool next(const TcPlan& p, const Unit& U, int& ks_out, int& t_out) {
     while (true) {
       if (t < nlive) {
@@ -149,6 +173,57 @@ struct TileIter {
       t = 0;
       nlive = 0;
     }
+  }
+};
+
+// A CTA's work, in order: whole units c, c+G, ... for dp_rounds rounds, then
+// its share [c*T/G, (c+1)*T/G) of the key tiles of the remaining units (a
+// stream-K split). A share may begin inside a unit (a TAIL part: it publishes
+// partial results to its scratch slot) and may end inside one (a HEAD part: it
+// merges the partials of the CTAs that hold the rest before the epilogue).
+enum : int { kFull = 0, kHead = 1, kTail = 2 };
+
+struct Item {
+  int u, t0, t1, kind;
+};
+
+struct Walker {
+  int k, i;
+  long long a, b;
+  __device__ __forceinline__ void init(const TcPlan& p) {
+    k = 0;
+    const long long T = p.sk_total, G = p.grid, c = blockIdx.x;
+    a = c * T / G;
+    b = (c + 1) * T / G;
+    // last unit starting at or before a; step back over empty units at a
+    int lo = 0, hi = p.sk_units - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (p.sk_prefix[mid] <= a) lo = mid; else hi = mid - 1;
+    }
+    while (lo > 0 && p.sk_prefix[lo] == a && p.sk_prefix[lo - 1] == a) --lo;
+    i = lo;
+  }
+  __device__ __forceinline__ bool next(const TcPlan& p, Item& it) {
+    if (k < p.dp_rounds) {
+      it.u = blockIdx.x + k * p.grid;
+      it.t0 = 0;
+      it.t1 = -1;  // the whole unit
+      it.kind = kFull;
+      ++k;
+      return true;
+    }
+    if (i >= p.sk_units) return false;
+    const long long lo = p.sk_prefix[i], hi = p.sk_prefix[i + 1];
+    const bool last_cta = int(blockIdx.x) == p.grid - 1;
+    if (!(lo < b || (last_cta && lo == b))) return false;
+    if (hi <= a && !(hi == lo && lo == a)) return false;  // nothing of it here
+    it.u = p.dp_rounds * p.grid + i;
+    it.t0 = int((lo > a ? lo : a) - lo);
+    it.t1 = int((hi < b ? hi : b) - lo);
+    it.kind = (it.t0 > 0) ? kTail : (it.t1 < hi - lo ? kHead : kFull);
+    ++i;
+    return true;
   }
 };
 
@@ -195,6 +270,20 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity,
       return;
     }
   }
+}
+
+// Publishing and reading the partial results of split units (global memory,
+// release/acquire at GPU scope).
+__device__ __forceinline__ void st_release(unsigned* addr, unsigned v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ unsigned ld_acquire(const unsigned* addr) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ void wg_bar(int id) {
+  asm volatile("bar.sync %0, 128;" ::"r"(id) : "memory");
 }
 
 template <int D>
@@ -260,10 +349,14 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ring_kernel(const __grid_const
     // ------------------------------------------------------------ producer
     int it = 0, qn = 0;
     bool ok = true;
-    for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
+    Walker wk;
+    wk.init(p);
+    Item I;
+    while (ok && wk.next(p, I)) {
       Unit U;
-      decode_unit(p, u, U);
-      if (U.n == 0) continue;
+      decode_unit(p, I.u, U);
+      const int n = (I.t1 < 0 ? U.n : I.t1) - I.t0;
+      if (n == 0) continue;
       ok = warp_wait(b_qempty, (qn & 1) ^ 1, abort_flag, budget, kSiteProdQ);
       if (!ok) break;
       if (lane == 0) {
@@ -278,8 +371,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ring_kernel(const __grid_const
       __syncwarp();
       ++qn;
       TileIter iter;
+      iter.seek(p, U, I.t0);
       int ks, t;
-      while (ok && iter.next(p, U, ks, t)) {
+      for (int j = 0; ok && j < n && iter.next(p, U, ks, t); ++j) {
         const KvSeg& sg = p.ks[ks];
         const int row = sg.row0 + 128 * t;
 #pragma unroll
@@ -337,10 +431,14 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ring_kernel(const __grid_const
     int it = 0, qn = 0, un = 0;
     uint32_t pc0 = 0, pc1 = 0;
     bool ok = true;
-    for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
+    Walker wk;
+    wk.init(p);
+    Item I;
+    while (ok && wk.next(p, I)) {
       Unit U;
-      decode_unit(p, u, U);
-      if (U.n == 0) continue;
+      decode_unit(p, I.u, U);
+      const int n = (I.t1 < 0 ? U.n : I.t1) - I.t0;
+      if (n == 0) continue;
       ok = warp_wait(b_qfull, qn & 1, abort_flag, budget, kSiteMmaQ);
       if (!ok) break;
       ++qn;
@@ -355,11 +453,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ring_kernel(const __grid_const
         issue_qk(1, kst);
         mma_commit(b_sfull0 + 8);
         mma_commit(b_kvempty0 + 8 * kst);
-        if (U.n == 1) mma_commit(b_qempty);
+        if (n == 1) mma_commit(b_qempty);
       }
       __syncwarp();
-      for (int j = 0; j < U.n; ++j) {
-        const bool more = j + 1 < U.n;
+      for (int j = 0; j < n; ++j) {
+        const bool more = j + 1 < n;
         const int vst = it % C::kStages;
         ok = warp_wait(b_kvfull0 + 8 * vst, (it / C::kStages) & 1, abort_flag, budget, kSiteMmaKv);
         if (!ok) break;
@@ -408,7 +506,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ring_kernel(const __grid_const
             issue_qk(1, kst);
             mma_commit(b_sfull0 + 8);
             mma_commit(b_kvempty0 + 8 * kst);
-            if (j + 2 == U.n) mma_commit(b_qempty);
+            if (j + 2 == n) mma_commit(b_qempty);
           }
         }
         __syncwarp();
@@ -435,18 +533,22 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ring_kernel(const __grid_const
     const float c2 = p.scale_log2;
     uint32_t sc = 0, oc = 0;
     bool ok = true;
-    for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
+    Walker wk;
+    wk.init(p);
+    Item I;
+    while (ok && wk.next(p, I)) {
       Unit U;
-      decode_unit(p, u, U);
+      decode_unit(p, I.u, U);
+      const int n = (I.t1 < 0 ? U.n : I.t1) - I.t0;
       const int grow = U.qrow0 + wg * 128 + r;
       const bool rvalid = grow < p.Sq;
       const int qpos = rvalid ? row_position(p, grow) : 0x7ffffffe;
       float m_ref = kNegInf, mx = kNegInf, l = 0.f, lr = 0.f;
-      int j = 0;
-      if (U.n > 0) {
+      if (n > 0) {
         TileIter iter;
+        iter.seek(p, U, I.t0);
         int ks, t;
-        while (iter.next(p, U, ks, t)) {
+        for (int j = 0; j < n && iter.next(p, U, ks, t); ++j) {
           // visible columns of this row: a prefix [0, L) of the tile (known
           // before S arrives)
           int L;
@@ -513,7 +615,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ring_kernel(const __grid_const
           // p = 2^(s*c2 - off) two at a time; l sums the fp32 p (returned), lr
           // sums the bf16-rounded p that P.V actually uses (normalises O)
           const uint64_t c2x2 = f2(c2, c2), noff = f2(-off, -off);
-          uint64_t lacc[2] = {0, 0}, racc[2] = {0, 0};
+          uint64_t lacc[2] = {0, 0};
+          float racc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             uint32_t pk[16];
@@ -525,24 +628,21 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ring_kernel(const __grid_const
               const float a = ex2(x0), b = ex2(x1);
               lacc[c & 1] = add2(lacc[c & 1], f2(a, b));
               const uint32_t w = pack_bf16x2(a, b);
-              racc[c & 1] = add2(racc[c & 1], f2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u)));
+              add_bf16x2_halves(racc[2 * (c & 1)], racc[2 * (c & 1) + 1], w);
               pk[c] = w;
             }
             tmem_st16(tS + 16 * i, pk);
           }
           {
-            float a0, a1, a2, a3, r0, r1, r2, r3;
+            float a0, a1, a2, a3;
             f2_split(lacc[0], a0, a1);
             f2_split(lacc[1], a2, a3);
-            f2_split(racc[0], r0, r1);
-            f2_split(racc[1], r2, r3);
             l += (a0 + a1) + (a2 + a3);
-            lr += (r0 + r1) + (r2 + r3);
+            lr += (racc[0] + racc[1]) + (racc[2] + racc[3]);
           }
           tmem_st_wait();
           tc_fence_before();
           mbar_arrive(b_pfull);
-          ++j;
         }
         if (!ok) break;
         ok = warp_wait(b_ofull, oc & 1, abort_flag, budget, kSiteSoftO);
@@ -550,17 +650,110 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ring_kernel(const __grid_const
         ++oc;
         tc_fence_after();
       }
-      // epilogue: read O in halves (bounded register use), release its TMEM
-      // after the last read, write this row's results
+      constexpr int kHalf = D / 64;  // 32-column chunks per half of O
+      const size_t slot_row = (size_t(blockIdx.x) * 2 + wg) * 128 + r;
+      if (I.kind == kTail) {
+        // ---- publish this part's raw partial results for the unit's head
+        float* dst = p.scratch.o + slot_row * D;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t o[kHalf][32];
+#pragma unroll
+          for (int cc = 0; cc < kHalf; ++cc) tmem_ld32(tO + 32 * (h * kHalf + cc), o[cc]);
+          tmem_ld_wait();
+#pragma unroll
+          for (int cc = 0; cc < kHalf; ++cc) reg_fence(o[cc]);
+          if (h == 1) {
+            tc_fence_before();
+            mbar_arrive(b_ofree);
+          }
+          float4* d4 = reinterpret_cast<float4*>(dst) + h * (D / 8);
+#pragma unroll
+          for (int cc = 0; cc < kHalf; ++cc)
+#pragma unroll
+            for (int c = 0; c < 32; c += 4)
+              d4[(cc * 32 + c) / 4] = make_float4(__uint_as_float(o[cc][c]), __uint_as_float(o[cc][c + 1]),
+                                                  __uint_as_float(o[cc][c + 2]), __uint_as_float(o[cc][c + 3]));
+        }
+        p.scratch.stats[slot_row] = make_float4(m_ref, mx, l, lr);
+        wg_bar(1 + wg);
+        if (r == 0) {
+          __threadfence();
+          st_release(p.scratch.flags + blockIdx.x * 2 + wg, p.epoch);
+        }
+        continue;
+      }
+      // ---- a head part: merge the partials of the CTAs holding the unit's rest
+      float a_self = 1.f;
+      int c_first = 0, c_end = 0;  // CTAs [c_first, c_end) hold later parts
+      if (I.kind == kHead) {
+        const long long T = p.sk_total, G = p.grid;
+        const long long hi = p.sk_prefix[I.u - p.dp_rounds * p.grid + 1];
+        c_first = blockIdx.x + 1;
+        c_end = c_first;
+        while (c_end < p.grid && (long long)c_end * T / G < hi) ++c_end;
+        // wait for every later part's flag (one thread polls, the warpgroup follows)
+        if (r == 0) {
+          for (int c = c_first; c < c_end; ++c) {
+            const long long ca = (long long)c * T / G, cb = (long long)(c + 1) * T / G;
+            if (ca >= cb) continue;  // that CTA holds no tiles at all
+            const unsigned* f = p.scratch.flags + c * 2 + wg;
+            unsigned long long t0 = 0;
+            for (uint32_t k = 1; ld_acquire(f) != p.epoch; ++k) {
+              if ((k & 255u) == 0) {
+                if (*abort_flag) break;
+                const unsigned long long now = globaltimer();
+                if (t0 == 0) t0 = now;
+                else if (now - t0 > budget) {
+                  *abort_flag = 1;
+                  record_error(0x100 | kSiteDrain);
+                  break;
+                }
+              }
+            }
+          }
+        }
+        wg_bar(1 + wg);
+        if (__any_sync(0xffffffffu, *abort_flag != 0)) {  // warp-uniform: TMEM loads follow
+          ok = false;
+          // TMEM O must still be released for the MMA warp's bookkeeping
+          if (n > 0) {
+            tc_fence_before();
+            mbar_arrive(b_ofree);
+          }
+          break;
+        }
+        float M = m_ref;
+        for (int c = c_first; c < c_end; ++c) {
+          const long long ca = (long long)c * T / G, cb = (long long)(c + 1) * T / G;
+          if (ca >= cb) continue;
+          const float4 st = __ldcg(p.scratch.stats + (size_t(c) * 2 + wg) * 128 + r);
+          M = fmaxf(M, st.x);
+        }
+        a_self = (m_ref == kNegInf) ? 0.f : ex2(m_ref - M);
+        l *= a_self;
+        lr *= a_self;
+        for (int c = c_first; c < c_end; ++c) {
+          const long long ca = (long long)c * T / G, cb = (long long)(c + 1) * T / G;
+          if (ca >= cb) continue;
+          const float4 st = __ldcg(p.scratch.stats + (size_t(c) * 2 + wg) * 128 + r);
+          const float bp = (st.x == kNegInf) ? 0.f : ex2(st.x - M);
+          mx = fmaxf(mx, st.y);
+          l += bp * st.z;
+          lr += bp * st.w;
+        }
+        m_ref = M;
+      }
+      // epilogue: read O in halves (bounded register use), fold in any
+      // partials, release TMEM after the last read, write this row's results
       const bool any = mx != kNegInf;
       const float corr = any ? ex2(m_ref - mx * c2) : 0.f;
       const float fo = p.stats_mode ? corr * (lr > 0.f ? l / lr : 0.f) : (lr > 0.f ? 1.f / lr : 0.f);
       const int64_t orow = int64_t(U.b) * p.o_sb + int64_t(U.hq) * p.o_sh + int64_t(grow) * p.o_sr;
-      constexpr int kHalf = D / 64;  // 32-column chunks per half
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         uint32_t o[kHalf][32];
-        if (U.n > 0) {
+        if (n > 0) {
 #pragma unroll
           for (int cc = 0; cc < kHalf; ++cc) tmem_ld32(tO + 32 * (h * kHalf + cc), o[cc]);
           tmem_ld_wait();
@@ -575,6 +768,31 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ring_kernel(const __grid_const
           for (int cc = 0; cc < kHalf; ++cc)
 #pragma unroll
             for (int c = 0; c < 32; ++c) o[cc][c] = 0u;
+        }
+        if (I.kind == kHead) {
+#pragma unroll
+          for (int cc = 0; cc < kHalf; ++cc)
+#pragma unroll
+            for (int c = 0; c < 32; ++c) o[cc][c] = __float_as_uint(__uint_as_float(o[cc][c]) * a_self);
+          for (int c = c_first; c < c_end; ++c) {
+            const long long ca = (long long)c * p.sk_total / p.grid;
+            const long long cb = (long long)(c + 1) * p.sk_total / p.grid;
+            if (ca >= cb) continue;
+            const size_t prow = (size_t(c) * 2 + wg) * 128 + r;
+            const float4 st = __ldcg(p.scratch.stats + prow);
+            const float bp = (st.x == kNegInf) ? 0.f : ex2(st.x - m_ref);
+            const float4* src = reinterpret_cast<const float4*>(p.scratch.o + prow * D) + h * (D / 8);
+#pragma unroll
+            for (int cc = 0; cc < kHalf; ++cc)
+#pragma unroll
+              for (int c4 = 0; c4 < 32; c4 += 4) {
+                const float4 v = __ldcg(src + (cc * 32 + c4) / 4);
+                o[cc][c4] = __float_as_uint(fmaf(bp, v.x, __uint_as_float(o[cc][c4])));
+                o[cc][c4 + 1] = __float_as_uint(fmaf(bp, v.y, __uint_as_float(o[cc][c4 + 1])));
+                o[cc][c4 + 2] = __float_as_uint(fmaf(bp, v.z, __uint_as_float(o[cc][c4 + 2])));
+                o[cc][c4 + 3] = __float_as_uint(fmaf(bp, v.w, __uint_as_float(o[cc][c4 + 3])));
+              }
+          }
         }
         if (rvalid) {
           if (p.o_fp32) {
@@ -619,22 +837,43 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ring_kernel(const __grid_const
 
 }  // namespace
 
-int launch_tc_bf16(const TcPlan& plan, int D, int num_sms, void* stream) {
-  const int grid = plan.n_units < num_sms ? plan.n_units : num_sms;
-  if (grid <= 0) return cudaSuccess;
-  cudaError_t e;
-  if (D == 128) {
-    e = cudaFuncSetAttribute(tc_ring_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Cfg<128>::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    tc_ring_kernel<128><<<grid, kThreads, Cfg<128>::kSmemBytes, static_cast<cudaStream_t>(stream)>>>(plan);
-  } else {
-    e = cudaFuncSetAttribute(tc_ring_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Cfg<64>::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    tc_ring_kernel<64><<<grid, kThreads, Cfg<64>::kSmemBytes, static_cast<cudaStream_t>(stream)>>>(plan);
-  }
+size_t tc_scratch_bytes(int grid, int D) {
+  return size_t(grid) * 2 * 128 * (size_t(D) * 4 + 16) + size_t(grid) * 2 * 4 + 256;
+}
+
+void tc_scratch_carve(void* base, int grid, int D, TcScratch* s) {
+  char* b = static_cast<char*>(base);
+  s->o = reinterpret_cast<float*>(b);
+  b += size_t(grid) * 2 * 128 * D * 4;
+  s->stats = reinterpret_cast<float4*>(b);
+  b += size_t(grid) * 2 * 128 * 16;
+  s->flags = reinterpret_cast<unsigned*>(b);
+}
+
+template <int D>
+static int launch_d(const TcPlan& plan, void* stream) {
+  cudaError_t e = cudaFuncSetAttribute(tc_ring_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       Cfg<D>::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(plan.grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = Cfg<D>::kSmemBytes;
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute attr[1];
+  // a head part waits for partials of later CTAs: all CTAs must be resident
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = plan.scratch.flags != nullptr ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, tc_ring_kernel<D>, plan);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
+}
+
+int launch_tc_bf16(const TcPlan& plan, int D, void* stream) {
+  if (plan.grid <= 0) return cudaSuccess;
+  return D == 128 ? launch_d<128>(plan, stream) : launch_d<64>(plan, stream);
 }
 
 int read_and_clear_device_error(int* code) {
