@@ -344,7 +344,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ring_kernel(const __grid_const
   const uint32_t tmem = *tmem_slot;
 
   if (warp < 4) {
-  asm volatile("setmaxnreg.dec.sync.aligned.u32 80;\n" ::: "memory");
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 88;\n" ::: "memory");
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     int it = 0, qn = 0;

@@ -32,7 +32,8 @@ def _check_sampled(w, q, k, v, O, m, l, boundaries, heads, n_random=48):
 
 def _invariance(O, m, l, O1, m1, l1):
     assert torch.isfinite(O.float()).all() and torch.isfinite(l).all()
-    assert (O.float() - O1.float()).abs().max().item() <= 1e-2
+    # two results, each within 1e-2 of the exact one
+    assert (O.float() - O1.float()).abs().max().item() <= 2e-2
     rel = ((m - m1).abs() / m1.abs().clamp_min(1)).max().item()
     assert rel <= 1e-3
     assert ((l - l1).abs() / l1).max().item() <= 1e-3
