@@ -265,9 +265,14 @@ void fill_q_pieces(const Common& c, ra::QPiece* qp, int32_t* n) {
 }
 
 // ----------------------------------------------------------- bf16 plan
+// Where the scratch of a split launch comes from: a stream-ordered allocation
+// for this call, or the library's fixed per-device array (no allocation).
+enum class ScratchSource { kAllocate, kStatic };
+
 ra_status run_tc(const Common& c, const ra_problem& p, const void* q,
                  const ra_kv_chunk* chunks, void* out, float* m, float* l,
-                 bool stats_mode, void* stream) {
+                 bool stats_mode, void* stream,
+                 ScratchSource source = ScratchSource::kAllocate) {
   if (c.nchunks > ra::kTcMaxChunks)
     return fail(RA_ERR_UNSUPPORTED, "bf16 path handles at most %d chunks, got %d",
                 ra::kTcMaxChunks, c.nchunks);
@@ -389,6 +394,21 @@ ra_status run_tc(const Common& c, const ra_problem& p, const void* q,
   plan.epoch = ep;
   void* scratch = nullptr;
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  if (split && source == ScratchSource::kStatic) {
+    const size_t bytes = ra::tc_scratch_bytes(int(G), int(c.D));
+    void* base = nullptr;
+    size_t cap = 0;
+    cudaError_t e = static_cast<cudaError_t>(ra::tc_static_scratch(&base, &cap));
+    if (e != cudaSuccess) return cuda_status(e, "looking up the fixed scratch array");
+    if (bytes > cap)
+      return fail(RA_ERR_UNSUPPORTED, "split needs %zu bytes of scratch, the fixed array holds %zu",
+                  bytes, cap);
+    ra::tc_scratch_carve(base, int(G), int(c.D), &plan.scratch);
+    // the array keeps the previous call's contents: clear the flags
+    e = cudaMemsetAsync(plan.scratch.flags, 0, size_t(G) * 2 * sizeof(unsigned), cs);
+    if (e != cudaSuccess) return cuda_status(e, "clearing stream-K flags");
+    return cuda_status(ra::launch_tc_bf16(plan, int(c.D), stream), "bf16 ring kernel launch");
+  }
   if (split) {
     const size_t bytes = ra::tc_scratch_bytes(int(G), int(c.D));
     cudaError_t e = cudaMallocAsync(&scratch, bytes, cs);
@@ -446,13 +466,14 @@ ra_status run_simt(const Common& c, const ra_problem& p, const void* q,
 
 ra_status run(const ra_problem* pb, const void* q, const ra_q_segment* segs, int32_t nsegs,
               const ra_kv_chunk* chunks, int32_t nchunks, void* out, float* m, float* l,
-              bool stats_mode, void* stream) {
+              bool stats_mode, void* stream,
+              ScratchSource source = ScratchSource::kAllocate) {
   Common c;
   ra_status st = validate(pb, q, segs, nsegs, chunks, nchunks, &c);
   if (st != RA_OK) return st;
   if (c.Sq == 0) return ok();
   if (!out || !m || !l) return fail(RA_ERR_INVALID, "output pointer is NULL");
-  if (c.dtype == RA_BF16) return run_tc(c, *pb, q, chunks, out, m, l, stats_mode, stream);
+  if (c.dtype == RA_BF16) return run_tc(c, *pb, q, chunks, out, m, l, stats_mode, stream, source);
   return run_simt(c, *pb, q, chunks, out, m, l, stats_mode, stream);
 }
 
@@ -473,6 +494,14 @@ ra_status ra_ring_attention(const ra_problem* problem, const void* q,
                             const ra_kv_chunk* chunks, int32_t nchunks, void* o,
                             float* m, float* l, void* stream) {
   return run(problem, q, segs, nsegs, chunks, nchunks, o, m, l, false, stream);
+}
+
+ra_status ra_ring_attention_noalloc(const ra_problem* problem, const void* q,
+                                    const ra_q_segment* segs, int32_t nsegs,
+                                    const ra_kv_chunk* chunks, int32_t nchunks, void* o,
+                                    float* m, float* l, void* stream) {
+  return run(problem, q, segs, nsegs, chunks, nchunks, o, m, l, false, stream,
+             ScratchSource::kStatic);
 }
 
 ra_status ra_merge_stats(int64_t rows, int64_t D, float* u_acc, float* l_acc, float* m_acc,

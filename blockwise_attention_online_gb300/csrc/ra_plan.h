@@ -101,6 +101,9 @@ static_assert(sizeof(SimtPlan) <= 32000, "fp32 plan must fit the parameter space
 int launch_tc_bf16(const TcPlan& plan, int D, void* stream);
 size_t tc_scratch_bytes(int grid, int D);
 void tc_scratch_carve(void* base, int grid, int D, TcScratch* s);
+// Device address of the fixed scratch array used by ra_ring_attention_noalloc
+// on the current device (looked up once per device); returns a cudaError_t.
+int tc_static_scratch(void** ptr, size_t* bytes);
 int launch_simt_f32(const SimtPlan& plan, void* stream);
 int launch_merge_f32(int64_t rows, int64_t D, float* u_acc, float* l_acc,
                      float* m_acc, const float* u_new, const float* l_new,

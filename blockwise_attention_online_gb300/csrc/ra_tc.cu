@@ -39,12 +39,21 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+
+#include "ra.h"
 #include "ra_plan.h"
 #include "ra_ptx.cuh"
 
 namespace ra {
 
 __device__ int g_ra_device_error = 0;
+
+// Scratch of ra_ring_attention_noalloc: one fixed array per device, part of
+// the library's device image (zero at load, kept until the process exits).
+// Host code must not use its name as a pointer: the device address comes from
+// cudaGetSymbolAddress below.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[RA_NOALLOC_SCRATCH_BYTES];
 
 namespace {
 
@@ -874,6 +883,26 @@ static int launch_d(const TcPlan& plan, void* stream) {
 int launch_tc_bf16(const TcPlan& plan, int D, void* stream) {
   if (plan.grid <= 0) return cudaSuccess;
   return D == 128 ? launch_d<128>(plan, stream) : launch_d<64>(plan, stream);
+}
+
+int tc_static_scratch(void** ptr, size_t* bytes) {
+  constexpr int kMaxDevices = 64;
+  static std::mutex mu;
+  static void* addr[kMaxDevices] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (addr[dev] == nullptr) {  // once per device, with that device current
+    void* a = nullptr;
+    e = cudaGetSymbolAddress(&a, g_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    addr[dev] = a;
+  }
+  *ptr = addr[dev];
+  *bytes = sizeof(g_noalloc_scratch);
+  return cudaSuccess;
 }
 
 int read_and_clear_device_error(int* code) {

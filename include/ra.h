@@ -14,9 +14,10 @@
  * Common conventions
  * ------------------
  * - Every pointer passed to a compute entry point is a DEVICE pointer owned
- *   by the caller; the library never frees or retains it and allocates no
- *   device memory of its own for these calls. Descriptor structs are read on
- *   the host during the call only.
+ *   by the caller; the library never frees or retains it. The only memory
+ *   the library itself allocates is ra_ring_attention's per-call scratch
+ *   (see there). Descriptor structs are read on the host during the call
+ *   only.
  * - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
  *   stream). A returned RA_OK means the work was validated and enqueued.
  * - Every argument is validated before anything is enqueued. On any non-OK
@@ -165,6 +166,9 @@ ra_status ra_merge_stats(int64_t rows, int64_t D,
  *
  * Causal key/value tiles that lie entirely in a query tile's future are
  * skipped; only tiles that straddle the diagonal are masked elementwise.
+ * When the last rounds of work are split across CTAs (bf16 path), the call
+ * allocates a scratch buffer of up to about 21 MB with cudaMallocAsync on
+ * `stream` and frees it with cudaFreeAsync on the same stream.
  * Limits of this build (RA_ERR_UNSUPPORTED beyond them): bf16 at most 32
  * non-empty chunks and 64 spans over all chunks; fp32 at most 256 chunks and
  * 320 spans; at most 64 spans over all query segments.
@@ -173,6 +177,40 @@ ra_status ra_ring_attention(const ra_problem* problem, const void* q,
                             const ra_q_segment* segs, int32_t nsegs,
                             const ra_kv_chunk* chunks, int32_t nchunks,
                             void* o, float* m, float* l, void* stream);
+
+/*
+ * ra_ring_attention_noalloc - ra_ring_attention for callers that must not
+ * allocate device memory. (The pages have no counterpart: this is a
+ * deployment variant of the same kernel.)
+ *
+ * ra_ring_attention may allocate a per-call scratch buffer (stream-ordered,
+ * freed again at the end of the call) when it splits a work unit across CTAs.
+ * Some callers cannot allow that: a process whose device memory is entirely
+ * reserved by another allocator (for example a framework's caching pool
+ * sized to the whole GPU), where a foreign allocation fails or fragments
+ * memory; or a deployment that must keep its footprint fixed after start-up
+ * and may not allocate on the request path. This entry point computes the
+ * same results with the same kernel, but takes its scratch from one fixed
+ * array of RA_NOALLOC_SCRATCH_BYTES in the library's device image; every GPU
+ * that loads the library holds that array until the process exits. It calls
+ * no cudaMalloc, cudaFree or other allocating routine.
+ *
+ * - The first call on a device looks up the array's device address (once per
+ *   device, with that device current). Make that first call before any
+ *   stream capture.
+ * - All calls share the array and it keeps the last call's contents; the
+ *   parts that must start cleared are cleared by each call on its stream.
+ *   Calls whose kernels overlap on the GPU (other streams, other threads)
+ *   race on the array: serialise them.
+ * - A problem whose split needs more scratch than the array holds is rejected
+ *   with RA_ERR_UNSUPPORTED before anything is launched.
+ * Arguments, layouts and results are those of ra_ring_attention.
+ */
+#define RA_NOALLOC_SCRATCH_BYTES (24u << 20)
+ra_status ra_ring_attention_noalloc(const ra_problem* problem, const void* q,
+                                    const ra_q_segment* segs, int32_t nsegs,
+                                    const ra_kv_chunk* chunks, int32_t nchunks,
+                                    void* o, float* m, float* l, void* stream);
 
 /*
  * ra_segment_work - host-only bookkeeping for comparing sequence layouts
