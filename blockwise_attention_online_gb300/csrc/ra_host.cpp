@@ -14,6 +14,7 @@
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <numeric>
@@ -312,7 +313,15 @@ ra_status run_tc(const Common& c, const ra_problem& p, const void* q,
   }
   plan.out = out; plan.m = m; plan.l = l;
   plan.o_sb = p.o_strides.batch; plan.o_sh = p.o_strides.head; plan.o_sr = p.o_strides.row;
+  // Diagnostics: RA_WAIT_BUDGET_NS sets the budget of every on-chip wait
+  // (default 2 s); RA_TEST_STALL=1 makes every CTA wait on a barrier that is
+  // never completed, so that the bounded-wait path can be tested end to end.
   plan.timeout_ns = 2000000000ull;
+  if (const char* e = std::getenv("RA_WAIT_BUDGET_NS")) {
+    const long long v = std::atoll(e);
+    if (v >= 1000) plan.timeout_ns = (unsigned long long)v;
+  }
+  if (const char* e = std::getenv("RA_TEST_STALL")) plan.test_stall = std::atoi(e) == 1;
   plan.B = int32_t(c.B); plan.Hq = int32_t(c.Hq); plan.Hkv = int32_t(c.Hkv);
   plan.Sq = int32_t(c.Sq);
   plan.causal = c.causal; plan.stats_mode = stats_mode ? 1 : 0;

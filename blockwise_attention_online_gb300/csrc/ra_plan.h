@@ -51,6 +51,7 @@ struct alignas(128) TcPlan {
   float* l;
   int64_t o_sb, o_sh, o_sr;          // element strides of out
   unsigned long long timeout_ns;     // budget of any single wait
+  int32_t test_stall;                // test hook: MMA warp first waits on a barrier nobody arrives on
   int32_t B, Hq, Hkv, Sq;
   int32_t causal, stats_mode, ring, n_chunks;
   float scale, scale_log2;

@@ -81,7 +81,8 @@ struct Cfg {
 // Wait sites, reported in the status word as 0x100 | site.
 enum : int {
   kSiteProdQ = 1, kSiteProdKv = 2, kSiteMmaQ = 3, kSiteMmaKv = 4, kSiteMmaP = 5,
-  kSiteMmaO = 6, kSiteSoftS = 7, kSiteSoftO = 8, kSiteDrain = 9
+  kSiteMmaO = 6, kSiteSoftS = 7, kSiteSoftO = 8, kSiteDrain = 9, kSiteTest = 10,
+  kSitePartial = 11
 };
 
 struct Unit {
@@ -239,25 +240,21 @@ struct Walker {
 __device__ __forceinline__ void record_error(int code) { atomicCAS(&g_ra_device_error, 0, code); }
 
 // Bounded wait on an mbarrier phase. Returns false (and stops the CTA) when the
-// budget runs out or another warp already gave up. The fast path is a plain
-// try_wait loop (try_wait itself sleeps until the phase completes or a short
-// hardware limit passes); the clock is only read every 1024 failed tries, so
-// a hand-off between warps costs no timer latency.
+// budget runs out or another warp already gave up. Each try may sleep up to
+// 1 ms until the phase completes, so a waiting warp does not take issue slots
+// from the warps that share its scheduler; the clock is read only after an
+// unsuccessful try.
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                          unsigned long long budget, int site) {
-  unsigned long long t0 = 0;
-  for (uint32_t n = 1;; ++n) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((n & 1023u) == 0) {
-      if (*abort_flag) return false;
-      const unsigned long long now = globaltimer();
-      if (t0 == 0) {
-        t0 = now;
-      } else if (now - t0 > budget) {
-        *abort_flag = 1;
-        record_error(0x100 | site);
-        return false;
-      }
+  if (mbar_try_wait_sleep(bar, parity, 1000000u)) return true;
+  const unsigned long long t0 = globaltimer();
+  while (true) {
+    if (mbar_try_wait_sleep(bar, parity, 1000000u)) return true;
+    if (*abort_flag) return false;
+    if (globaltimer() - t0 > budget) {
+      *abort_flag = 1;
+      record_error(0x100 | site);
+      return false;
     }
   }
 }
@@ -269,12 +266,15 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
   return __all_sync(0xffffffffu, ok);
 }
 
-// Wait used while tearing down after an abort: ignores the abort flag.
-__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity,
-                                           unsigned long long budget) {
+// Wait used while tearing down after an abort: ignores the abort flag and
+// has its own generous budget (copies and MMAs already issued always finish;
+// the CTA must not exit before they do, whatever the normal wait budget is).
+constexpr unsigned long long kDrainBudgetNs = 2000000000ull;
+
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, unsigned long long) {
   const unsigned long long t0 = globaltimer();
   while (!mbar_try_wait(bar, parity)) {
-    if (globaltimer() - t0 > budget) {
+    if (globaltimer() - t0 > kDrainBudgetNs) {
       record_error(0x100 | kSiteDrain);
       return;
     }
@@ -310,9 +310,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ring_kernel(const __grid_const
   const uint32_t b_misc = bars + 16 + 16 * C::kStages;
   const uint32_t b_sfull0 = b_misc, b_pfull0 = b_misc + 16, b_ofull0 = b_misc + 32,
                  b_ofree0 = b_misc + 48, b_done = b_misc + 64;
-  uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::kBarOff + 16 + 16 * C::kStages + 72);
+  const uint32_t b_never = b_misc + 72;  // test hook: nobody arrives on it
+  uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::kBarOff + 16 + 16 * C::kStages + 80);
   volatile int* const abort_flag =
-      reinterpret_cast<volatile int*>(gbase + C::kBarOff + 16 + 16 * C::kStages + 76);
+      reinterpret_cast<volatile int*>(gbase + C::kBarOff + 16 + 16 * C::kStages + 84);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const unsigned long long budget = p.timeout_ns;
@@ -331,6 +332,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ring_kernel(const __grid_const
       mbar_init(b_ofree0 + 8 * t, 128);
     }
     mbar_init(b_done, 1);
+    mbar_init(b_never, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -353,67 +355,68 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ring_kernel(const __grid_const
   const uint32_t tmem = *tmem_slot;
 
   if (warp < 4) {
-  asm volatile("setmaxnreg.dec.sync.aligned.u32 88;\n" ::: "memory");
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 104;\n" ::: "memory");
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    int it = 0, qn = 0;
-    bool ok = true;
-    Walker wk;
-    wk.init(p);
-    Item I;
-    while (ok && wk.next(p, I)) {
-      Unit U;
-      decode_unit(p, I.u, U);
-      const int n = (I.t1 < 0 ? U.n : I.t1) - I.t0;
-      if (n == 0) continue;
-      ok = warp_wait(b_qempty, (qn & 1) ^ 1, abort_flag, budget, kSiteProdQ);
-      if (!ok) break;
-      if (lane == 0) {
-        mbar_arrive_expect_tx(b_qfull, 2 * C::kTileBytes);
+    if (lane == 0) {  // one thread waits and issues the copies
+      int it = 0, qn = 0;
+      bool ok = true;
+      Walker wk;
+      wk.init(p);
+      Item I;
+      while (ok && wk.next(p, I)) {
+        Unit U;
+        decode_unit(p, I.u, U);
+        const int n = (I.t1 < 0 ? U.n : I.t1) - I.t0;
+        if (n == 0) continue;
+        ok = wait_bar(b_qempty, (qn & 1) ^ 1, abort_flag, budget, kSiteProdQ);
+        if (!ok) break;
+        {
+          mbar_arrive_expect_tx(b_qfull, 2 * C::kTileBytes);
 #pragma unroll
-        for (int t = 0; t < 2; ++t)
-#pragma unroll
-          for (int bx = 0; bx < C::kBoxes; ++bx)
-            tma_load_4d(sQ + t * C::kTileBytes + bx * C::kBoxBytes, &p.qmap, b_qfull, bx * 64,
-                        U.qrow0 + 128 * t, U.hq, U.b);
-      }
-      __syncwarp();
-      ++qn;
-      TileIter iter;
-      iter.seek(p, U, I.t0);
-      int ks, t;
-      for (int j = 0; ok && j < n && iter.next(p, U, ks, t); ++j) {
-        const KvSeg& sg = p.ks[ks];
-        const int row = sg.row0 + 128 * t;
-#pragma unroll
-        for (int kv = 0; kv < 2; ++kv) {
-          const int st = it % C::kStages;
-          ok = warp_wait(b_kvempty0 + 8 * st, ((it / C::kStages) & 1) ^ 1, abort_flag, budget,
-                         kSiteProdKv);
-          if (!ok) break;
-          if (lane == 0) {
-            const uint32_t full = b_kvfull0 + 8 * st;
-            mbar_arrive_expect_tx(full, C::kTileBytes);
-            const CUtensorMap* map = kv == 0 ? &p.kmap[sg.chunk] : &p.vmap[sg.chunk];
+          for (int t = 0; t < 2; ++t)
 #pragma unroll
             for (int bx = 0; bx < C::kBoxes; ++bx)
-              tma_load_4d(sKV + st * C::kTileBytes + bx * C::kBoxBytes, map, full, bx * 64, row,
-                          U.hkv, U.b);
+              tma_load_4d(sQ + t * C::kTileBytes + bx * C::kBoxBytes, &p.qmap, b_qfull, bx * 64,
+                          U.qrow0 + 128 * t, U.hq, U.b);
+        }
+        ++qn;
+        TileIter iter;
+        iter.seek(p, U, I.t0);
+        int ks, t;
+        for (int j = 0; ok && j < n && iter.next(p, U, ks, t); ++j) {
+          const KvSeg& sg = p.ks[ks];
+          const int row = sg.row0 + 128 * t;
+#pragma unroll
+          for (int kv = 0; kv < 2; ++kv) {
+            const int st = it % C::kStages;
+            ok = wait_bar(b_kvempty0 + 8 * st, ((it / C::kStages) & 1) ^ 1, abort_flag, budget,
+                        kSiteProdKv);
+            if (!ok) break;
+            {
+              const uint32_t full = b_kvfull0 + 8 * st;
+              mbar_arrive_expect_tx(full, C::kTileBytes);
+              const CUtensorMap* map = kv == 0 ? &p.kmap[sg.chunk] : &p.vmap[sg.chunk];
+#pragma unroll
+              for (int bx = 0; bx < C::kBoxes; ++bx)
+                tma_load_4d(sKV + st * C::kTileBytes + bx * C::kBoxBytes, map, full, bx * 64, row,
+                            U.hkv, U.b);
+            }
+            ++it;
           }
-          __syncwarp();
-          ++it;
         }
       }
-    }
-    if (!ok && lane == 0) {
-      // let the copies already in flight land before the CTA goes away
-      for (int s = 0; s < C::kStages; ++s) {
-        const int back = ((it - 1 - s) % C::kStages + C::kStages) % C::kStages;
-        const int last = it - 1 - back;
-        if (last >= 0) drain_wait(b_kvfull0 + 8 * s, (last / C::kStages) & 1, budget);
+      if (!ok) {
+        // let the copies already in flight land before the CTA goes away
+        for (int s = 0; s < C::kStages; ++s) {
+          const int back = ((it - 1 - s) % C::kStages + C::kStages) % C::kStages;
+          const int last = it - 1 - back;
+          if (last >= 0) drain_wait(b_kvfull0 + 8 * s, (last / C::kStages) & 1, budget);
+        }
+        if (qn > 0) drain_wait(b_qfull, (qn - 1) & 1, budget);
       }
-      if (qn > 0) drain_wait(b_qfull, (qn - 1) & 1, budget);
     }
+    __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     constexpr uint32_t kIdQK = idesc_bf16_f32(128, 128, 0, 0);
@@ -437,77 +440,74 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ring_kernel(const __grid_const
                (acc || kk > 0) ? 1u : 0u);
       }
     };
-    int it = 0, qn = 0, un = 0;
-    uint32_t pc0 = 0, pc1 = 0;
-    bool ok = true;
-    Walker wk;
-    wk.init(p);
-    Item I;
-    while (ok && wk.next(p, I)) {
-      Unit U;
-      decode_unit(p, I.u, U);
-      const int n = (I.t1 < 0 ? U.n : I.t1) - I.t0;
-      if (n == 0) continue;
-      ok = warp_wait(b_qfull, qn & 1, abort_flag, budget, kSiteMmaQ);
-      if (!ok) break;
-      ++qn;
-      int kst = it % C::kStages;
-      ok = warp_wait(b_kvfull0 + 8 * kst, (it / C::kStages) & 1, abort_flag, budget, kSiteMmaKv);
-      if (!ok) break;
-      ++it;
-      tc_fence_after();
-      if (lane == 0) {
+    // One thread waits and issues: no warp-level hand-off on the critical
+    // path. Per ring step the K/V waits come first (their copies landed long
+    // ago), so that each P_t wait is followed by one fence and the PV_t and
+    // S_t MMAs back to back.
+    if (lane == 0) {
+      int it = 0, qn = 0, un = 0;
+      uint32_t pc0 = 0, pc1 = 0;
+      bool ok = true;
+      if (p.test_stall) ok = wait_bar(b_never, 0, abort_flag, budget, kSiteTest);
+      Walker wk;
+      wk.init(p);
+      Item I;
+      while (ok && wk.next(p, I)) {
+        Unit U;
+        decode_unit(p, I.u, U);
+        const int n = (I.t1 < 0 ? U.n : I.t1) - I.t0;
+        if (n == 0) continue;
+        ok = wait_bar(b_qfull, qn & 1, abort_flag, budget, kSiteMmaQ);
+        if (!ok) break;
+        ++qn;
+        int kst = it % C::kStages;
+        ok = wait_bar(b_kvfull0 + 8 * kst, (it / C::kStages) & 1, abort_flag, budget, kSiteMmaKv);
+        if (!ok) break;
+        ++it;
+        tc_fence_after();
         issue_qk(0, kst);
         mma_commit(b_sfull0);
         issue_qk(1, kst);
         mma_commit(b_sfull0 + 8);
         mma_commit(b_kvempty0 + 8 * kst);
         if (n == 1) mma_commit(b_qempty);
-      }
-      __syncwarp();
-      for (int j = 0; j < n; ++j) {
-        const bool more = j + 1 < n;
-        const int vst = it % C::kStages;
-        ok = warp_wait(b_kvfull0 + 8 * vst, (it / C::kStages) & 1, abort_flag, budget, kSiteMmaKv);
-        if (!ok) break;
-        ++it;
-        // query tile 0: PV, then the next S
-        ok = warp_wait(b_pfull0, pc0 & 1, abort_flag, budget, kSiteMmaP);
-        if (!ok) break;
-        ++pc0;
-        if (j == 0) {
-          ok = warp_wait(b_ofree0, (un & 1) ^ 1, abort_flag, budget, kSiteMmaO);
-          if (!ok) break;
-        }
-        tc_fence_after();
-        if (lane == 0) {
-          issue_pv(0, vst, j > 0);
-          if (!more) mma_commit(b_ofull0);
-        }
-        __syncwarp();
-        if (more) {
-          kst = it % C::kStages;
-          ok = warp_wait(b_kvfull0 + 8 * kst, (it / C::kStages) & 1, abort_flag, budget,
-                         kSiteMmaKv);
+        for (int j = 0; j < n; ++j) {
+          const bool more = j + 1 < n;
+          const int vst = it % C::kStages;
+          ok = wait_bar(b_kvfull0 + 8 * vst, (it / C::kStages) & 1, abort_flag, budget, kSiteMmaKv);
           if (!ok) break;
           ++it;
+          if (more) {
+            kst = it % C::kStages;
+            ok = wait_bar(b_kvfull0 + 8 * kst, (it / C::kStages) & 1, abort_flag, budget,
+                          kSiteMmaKv);
+            if (!ok) break;
+            ++it;
+          }
+          // query tile 0: PV, then the next S
+          ok = wait_bar(b_pfull0, pc0 & 1, abort_flag, budget, kSiteMmaP);
+          if (!ok) break;
+          ++pc0;
+          if (j == 0) {
+            ok = wait_bar(b_ofree0, (un & 1) ^ 1, abort_flag, budget, kSiteMmaO);
+            if (!ok) break;
+          }
           tc_fence_after();
-          if (lane == 0) {
+          issue_pv(0, vst, j > 0);
+          if (!more) mma_commit(b_ofull0);
+          if (more) {
             issue_qk(0, kst);
             mma_commit(b_sfull0);
           }
-          __syncwarp();
-        }
-        // query tile 1
-        ok = warp_wait(b_pfull0 + 8, pc1 & 1, abort_flag, budget, kSiteMmaP);
-        if (!ok) break;
-        ++pc1;
-        if (j == 0) {
-          ok = warp_wait(b_ofree0 + 8, (un & 1) ^ 1, abort_flag, budget, kSiteMmaO);
+          // query tile 1
+          ok = wait_bar(b_pfull0 + 8, pc1 & 1, abort_flag, budget, kSiteMmaP);
           if (!ok) break;
-        }
-        tc_fence_after();
-        if (lane == 0) {
+          ++pc1;
+          if (j == 0) {
+            ok = wait_bar(b_ofree0 + 8, (un & 1) ^ 1, abort_flag, budget, kSiteMmaO);
+            if (!ok) break;
+          }
+          tc_fence_after();
           issue_pv(1, vst, j > 0);
           mma_commit(b_kvempty0 + 8 * vst);
           if (!more) mma_commit(b_ofull0 + 8);
@@ -518,18 +518,16 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ring_kernel(const __grid_const
             if (j + 2 == n) mma_commit(b_qempty);
           }
         }
-        __syncwarp();
+        ++un;
       }
-      ++un;
+      // every MMA this thread issued must be complete before TMEM is freed
+      mma_commit(b_done);
+      drain_wait(b_done, 0, budget);
     }
-    // every MMA this thread issued must be complete before TMEM is freed
-    if (lane == 0) mma_commit(b_done);
-    __syncwarp();
-    if (lane == 0) drain_wait(b_done, 0, budget);
     __syncwarp();
   }
   } else {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 208;\n" ::: "memory");
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 200;\n" ::: "memory");
     // ------------------------------------------------------------ softmax
     const int wg = (warp - 4) >> 2;
     const int sub = warp & 3;
@@ -715,7 +713,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ring_kernel(const __grid_const
                 if (t0 == 0) t0 = now;
                 else if (now - t0 > budget) {
                   *abort_flag = 1;
-                  record_error(0x100 | kSiteDrain);
+                  record_error(0x100 | kSitePartial);
                   break;
                 }
               }
