@@ -22,7 +22,8 @@
 //               while computing the current one" (blog, "A simple forward
 //               schedule"; glossary "Communication overlap") becomes this
 //               multi-stage prefetch with full/empty mbarriers.
-//   warp 1      MMA issuer (one thread) and TMEM owner.
+//   warp 1      MMA issuer (the warp waits, one elected lane issues) and TMEM
+//               owner.
 //   warps 4-7   softmax warpgroup for query tile 0 (TMEM lanes 0-127)
 //   warps 8-11  softmax warpgroup for query tile 1
 // The MMA order S0(j) S1(j) | PV0(j) S0(j+1) PV1(j) S1(j+1) | ... lets the
@@ -440,15 +441,18 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ring_kernel(const __grid_const
                (acc || kk > 0) ? 1u : 0u);
       }
     };
-    // One thread waits and issues: no warp-level hand-off on the critical
-    // path. Per ring step the K/V waits come first (their copies landed long
-    // ago), so that each P_t wait is followed by one fence and the PV_t and
-    // S_t MMAs back to back.
-    if (lane == 0) {
+    // The whole warp runs the walk and the waits, so every descriptor and
+    // address stays warp-uniform; one elected lane issues each group of MMAs.
+    // (Issuing from a single-lane branch measured 80-110 cycles per MMA, above
+    // the 64 cycles an M=128, N=128, K=16 MMA takes.) Per ring step the K/V
+    // waits come first (their copies landed long ago), so that each P_t wait
+    // is followed by one fence and the PV_t and S_t MMAs back to back.
+    {
+      const bool leader = elect_one();
       int it = 0, qn = 0, un = 0;
       uint32_t pc0 = 0, pc1 = 0;
       bool ok = true;
-      if (p.test_stall) ok = wait_bar(b_never, 0, abort_flag, budget, kSiteTest);
+      if (p.test_stall) ok = warp_wait(b_never, 0, abort_flag, budget, kSiteTest);
       Walker wk;
       wk.init(p);
       Item I;
@@ -457,71 +461,81 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ring_kernel(const __grid_const
         decode_unit(p, I.u, U);
         const int n = (I.t1 < 0 ? U.n : I.t1) - I.t0;
         if (n == 0) continue;
-        ok = wait_bar(b_qfull, qn & 1, abort_flag, budget, kSiteMmaQ);
+        ok = warp_wait(b_qfull, qn & 1, abort_flag, budget, kSiteMmaQ);
         if (!ok) break;
         ++qn;
         int kst = it % C::kStages;
-        ok = wait_bar(b_kvfull0 + 8 * kst, (it / C::kStages) & 1, abort_flag, budget, kSiteMmaKv);
+        ok = warp_wait(b_kvfull0 + 8 * kst, (it / C::kStages) & 1, abort_flag, budget, kSiteMmaKv);
         if (!ok) break;
         ++it;
         tc_fence_after();
-        issue_qk(0, kst);
-        mma_commit(b_sfull0);
-        issue_qk(1, kst);
-        mma_commit(b_sfull0 + 8);
-        mma_commit(b_kvempty0 + 8 * kst);
-        if (n == 1) mma_commit(b_qempty);
+        if (leader) {
+          issue_qk(0, kst);
+          mma_commit(b_sfull0);
+          issue_qk(1, kst);
+          mma_commit(b_sfull0 + 8);
+          mma_commit(b_kvempty0 + 8 * kst);
+          if (n == 1) mma_commit(b_qempty);
+        }
+        __syncwarp();
         for (int j = 0; j < n; ++j) {
           const bool more = j + 1 < n;
           const int vst = it % C::kStages;
-          ok = wait_bar(b_kvfull0 + 8 * vst, (it / C::kStages) & 1, abort_flag, budget, kSiteMmaKv);
+          ok = warp_wait(b_kvfull0 + 8 * vst, (it / C::kStages) & 1, abort_flag, budget, kSiteMmaKv);
           if (!ok) break;
           ++it;
           if (more) {
             kst = it % C::kStages;
-            ok = wait_bar(b_kvfull0 + 8 * kst, (it / C::kStages) & 1, abort_flag, budget,
+            ok = warp_wait(b_kvfull0 + 8 * kst, (it / C::kStages) & 1, abort_flag, budget,
                           kSiteMmaKv);
             if (!ok) break;
             ++it;
           }
           // query tile 0: PV, then the next S
-          ok = wait_bar(b_pfull0, pc0 & 1, abort_flag, budget, kSiteMmaP);
+          ok = warp_wait(b_pfull0, pc0 & 1, abort_flag, budget, kSiteMmaP);
           if (!ok) break;
           ++pc0;
           if (j == 0) {
-            ok = wait_bar(b_ofree0, (un & 1) ^ 1, abort_flag, budget, kSiteMmaO);
+            ok = warp_wait(b_ofree0, (un & 1) ^ 1, abort_flag, budget, kSiteMmaO);
             if (!ok) break;
           }
           tc_fence_after();
-          issue_pv(0, vst, j > 0);
-          if (!more) mma_commit(b_ofull0);
-          if (more) {
-            issue_qk(0, kst);
-            mma_commit(b_sfull0);
+          if (leader) {
+            issue_pv(0, vst, j > 0);
+            if (!more) mma_commit(b_ofull0);
+            if (more) {
+              issue_qk(0, kst);
+              mma_commit(b_sfull0);
+            }
           }
+          __syncwarp();
           // query tile 1
-          ok = wait_bar(b_pfull0 + 8, pc1 & 1, abort_flag, budget, kSiteMmaP);
+          ok = warp_wait(b_pfull0 + 8, pc1 & 1, abort_flag, budget, kSiteMmaP);
           if (!ok) break;
           ++pc1;
           if (j == 0) {
-            ok = wait_bar(b_ofree0 + 8, (un & 1) ^ 1, abort_flag, budget, kSiteMmaO);
+            ok = warp_wait(b_ofree0 + 8, (un & 1) ^ 1, abort_flag, budget, kSiteMmaO);
             if (!ok) break;
           }
           tc_fence_after();
-          issue_pv(1, vst, j > 0);
-          mma_commit(b_kvempty0 + 8 * vst);
-          if (!more) mma_commit(b_ofull0 + 8);
-          if (more) {
-            issue_qk(1, kst);
-            mma_commit(b_sfull0 + 8);
-            mma_commit(b_kvempty0 + 8 * kst);
-            if (j + 2 == n) mma_commit(b_qempty);
+          if (leader) {
+            issue_pv(1, vst, j > 0);
+            mma_commit(b_kvempty0 + 8 * vst);
+            if (!more) mma_commit(b_ofull0 + 8);
+            if (more) {
+              issue_qk(1, kst);
+              mma_commit(b_sfull0 + 8);
+              mma_commit(b_kvempty0 + 8 * kst);
+              if (j + 2 == n) mma_commit(b_qempty);
+            }
           }
+          __syncwarp();
         }
         ++un;
       }
-      // every MMA this thread issued must be complete before TMEM is freed
-      mma_commit(b_done);
+      // every MMA this warp issued must be complete before TMEM is freed
+      if (leader) mma_commit(b_done);
+      __syncwarp();
       drain_wait(b_done, 0, budget);
     }
     __syncwarp();
