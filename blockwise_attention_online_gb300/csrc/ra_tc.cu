@@ -76,7 +76,11 @@ struct Cfg {
   static constexpr int kKvOff = 2 * kTileBytes;
   static constexpr int kBarOff = kKvOff + kStages * kTileBytes;
   static constexpr int kBarBytes = 256;
-  static constexpr int kSmemBytes = kBarOff + kBarBytes + 1024;  // + alignment slack
+  // output staging: 4 KB per softmax warp (32 rows x 128 bytes)
+  static constexpr int kStageOff = kBarOff + kBarBytes;
+  static constexpr int kStageBytes = 8 * 4096;
+  static constexpr int kSmemBytes = kStageOff + kStageBytes + 1024;  // + alignment slack
+  static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 };
 
 // Wait sites, reported in the status word as 0x100 | site.
@@ -280,6 +284,32 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, unsign
       return;
     }
   }
+}
+
+// One warp writes NC 16-byte chunks of each of its 32 output rows (a row piece
+// of NC * 16 bytes) through its shared-memory staging area. Each lane deposits
+// its own row (chunk slots XOR-swizzled by row, so neither side has bank
+// conflicts); then each store instruction covers 32 / NC whole row pieces
+// instead of 32 rows 16 bytes apart. Rows at and past `rows_valid` are not
+// written. Every lane of the warp must call it.
+template <int NC>
+__device__ __forceinline__ void warp_store_staged(uint8_t* stage, const uint4 (&ch)[NC], int lane,
+                                                  char* row0, int64_t row_bytes, int rows_valid) {
+  static_assert(NC == 4 || NC == 8, "row piece of 64 or 128 bytes");
+#pragma unroll
+  for (int k = 0; k < NC; ++k)
+    *reinterpret_cast<uint4*>(stage + lane * (NC * 16) + ((k ^ (lane & (NC - 1))) * 16)) = ch[k];
+  __syncwarp();
+  constexpr int kRowsPer = 32 / NC;
+  const int kq = lane & (NC - 1), rsub = lane / NC;
+#pragma unroll
+  for (int it = 0; it < NC; ++it) {
+    const int row = it * kRowsPer + rsub;
+    const uint4 v =
+        *reinterpret_cast<const uint4*>(stage + row * (NC * 16) + ((kq ^ (row & (NC - 1))) * 16));
+    if (row < rows_valid) *reinterpret_cast<uint4*>(row0 + row * row_bytes + kq * 16) = v;
+  }
+  __syncwarp();
 }
 
 // Publishing and reading the partial results of split units (global memory,
@@ -690,9 +720,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ring_kernel(const __grid_const
       }
       constexpr int kHalf = D / 64;  // 32-column chunks per half of O
       const size_t slot_row = (size_t(blockIdx.x) * 2 + wg) * 128 + r;
+      // A scratch slot (one per CTA and warpgroup) holds raw O as [D/4][128]
+      // float4: lane r touches element (k, r), so every warp access covers
+      // 512 contiguous bytes.
+      constexpr size_t kSlotF4 = size_t(128) * (D / 4);
       if (I.kind == kTail) {
         // ---- publish this part's raw partial results for the unit's head
-        float* dst = p.scratch.o + slot_row * D;
+        float4* const dst = reinterpret_cast<float4*>(p.scratch.o) + (size_t(blockIdx.x) * 2 + wg) * kSlotF4 + r;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           uint32_t o[kHalf][32];
@@ -705,13 +739,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ring_kernel(const __grid_const
             tc_fence_before();
             mbar_arrive(b_ofree);
           }
-          float4* d4 = reinterpret_cast<float4*>(dst) + h * (D / 8);
 #pragma unroll
           for (int cc = 0; cc < kHalf; ++cc)
 #pragma unroll
             for (int c = 0; c < 32; c += 4)
-              d4[(cc * 32 + c) / 4] = make_float4(__uint_as_float(o[cc][c]), __uint_as_float(o[cc][c + 1]),
-                                                  __uint_as_float(o[cc][c + 2]), __uint_as_float(o[cc][c + 3]));
+              dst[size_t(h * (D / 8) + (cc * 32 + c) / 4) * 128] =
+                  make_float4(__uint_as_float(o[cc][c]), __uint_as_float(o[cc][c + 1]),
+                              __uint_as_float(o[cc][c + 2]), __uint_as_float(o[cc][c + 3]));
         }
         p.scratch.stats[slot_row] = make_float4(m_ref, mx, l, lr);
         wg_bar(1 + wg);
@@ -787,7 +821,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ring_kernel(const __grid_const
       const bool any = mx != kNegInf;
       const float corr = any ? ex2(m_ref - mx * c2) : 0.f;
       const float fo = p.stats_mode ? corr * (lr > 0.f ? l / lr : 0.f) : (lr > 0.f ? 1.f / lr : 0.f);
-      const int64_t orow = int64_t(U.b) * p.o_sb + int64_t(U.hq) * p.o_sh + int64_t(grow) * p.o_sr;
+      // this warp's 32 output rows start at row wrow0; rows past Sq are not written
+      const int wrow0 = U.qrow0 + wg * 128 + sub * 32;
+      const int wvalid = min(32, max(0, p.Sq - wrow0));
+      const int64_t wbase = int64_t(U.b) * p.o_sb + int64_t(U.hq) * p.o_sh + int64_t(wrow0) * p.o_sr;
+      uint8_t* const stage = gbase + C::kStageOff + (warp - 4) * 4096;
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         uint32_t o[kHalf][32];
@@ -819,12 +857,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ring_kernel(const __grid_const
             const size_t prow = (size_t(c) * 2 + wg) * 128 + r;
             const float4 st = __ldcg(p.scratch.stats + prow);
             const float bp = (st.x == kNegInf) ? 0.f : ex2(st.x - m_ref);
-            const float4* src = reinterpret_cast<const float4*>(p.scratch.o + prow * D) + h * (D / 8);
+            const float4* src = reinterpret_cast<const float4*>(p.scratch.o) + (size_t(c) * 2 + wg) * kSlotF4 + r;
 #pragma unroll
             for (int cc = 0; cc < kHalf; ++cc)
 #pragma unroll
               for (int c4 = 0; c4 < 32; c4 += 4) {
-                const float4 v = __ldcg(src + (cc * 32 + c4) / 4);
+                const float4 v = __ldcg(src + size_t(h * (D / 8) + (cc * 32 + c4) / 4) * 128);
                 o[cc][c4] = __float_as_uint(fmaf(bp, v.x, __uint_as_float(o[cc][c4])));
                 o[cc][c4 + 1] = __float_as_uint(fmaf(bp, v.y, __uint_as_float(o[cc][c4 + 1])));
                 o[cc][c4 + 2] = __float_as_uint(fmaf(bp, v.z, __uint_as_float(o[cc][c4 + 2])));
@@ -832,31 +870,35 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ring_kernel(const __grid_const
               }
           }
         }
-        if (rvalid) {
-          if (p.o_fp32) {
-            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + orow) + h * (D / 8);
+        // write this half through the warp's staging area (coalesced rows)
+        if (p.o_fp32) {
 #pragma unroll
-            for (int cc = 0; cc < kHalf; ++cc)
+          for (int cc = 0; cc < kHalf; ++cc) {
+            uint4 ch[8];
 #pragma unroll
-              for (int c = 0; c < 32; c += 4)
-                dst[(cc * 32 + c) / 4] = make_float4(__uint_as_float(o[cc][c]) * fo,
-                                                     __uint_as_float(o[cc][c + 1]) * fo,
-                                                     __uint_as_float(o[cc][c + 2]) * fo,
-                                                     __uint_as_float(o[cc][c + 3]) * fo);
-          } else {
-            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + orow) + h * (D / 16);
-#pragma unroll
-            for (int cc = 0; cc < kHalf; ++cc)
-#pragma unroll
-              for (int c = 0; c < 32; c += 8) {
-                uint4 v;
-                v.x = pack_bf16x2(__uint_as_float(o[cc][c]) * fo, __uint_as_float(o[cc][c + 1]) * fo);
-                v.y = pack_bf16x2(__uint_as_float(o[cc][c + 2]) * fo, __uint_as_float(o[cc][c + 3]) * fo);
-                v.z = pack_bf16x2(__uint_as_float(o[cc][c + 4]) * fo, __uint_as_float(o[cc][c + 5]) * fo);
-                v.w = pack_bf16x2(__uint_as_float(o[cc][c + 6]) * fo, __uint_as_float(o[cc][c + 7]) * fo);
-                dst[(cc * 32 + c) / 8] = v;
-              }
+            for (int k = 0; k < 8; ++k)
+              ch[k] = make_uint4(__float_as_uint(__uint_as_float(o[cc][4 * k]) * fo),
+                                 __float_as_uint(__uint_as_float(o[cc][4 * k + 1]) * fo),
+                                 __float_as_uint(__uint_as_float(o[cc][4 * k + 2]) * fo),
+                                 __float_as_uint(__uint_as_float(o[cc][4 * k + 3]) * fo));
+            warp_store_staged<8>(stage, ch, lane,
+                                 reinterpret_cast<char*>(static_cast<float*>(p.out) + wbase + h * (D / 2) + cc * 32),
+                                 p.o_sr * 4, wvalid);
           }
+        } else {
+          constexpr int NC = kHalf * 4;
+          uint4 ch[NC];
+#pragma unroll
+          for (int k = 0; k < NC; ++k) {
+            const int cc = k >> 2, c = (k & 3) * 8;
+            ch[k].x = pack_bf16x2(__uint_as_float(o[cc][c]) * fo, __uint_as_float(o[cc][c + 1]) * fo);
+            ch[k].y = pack_bf16x2(__uint_as_float(o[cc][c + 2]) * fo, __uint_as_float(o[cc][c + 3]) * fo);
+            ch[k].z = pack_bf16x2(__uint_as_float(o[cc][c + 4]) * fo, __uint_as_float(o[cc][c + 5]) * fo);
+            ch[k].w = pack_bf16x2(__uint_as_float(o[cc][c + 6]) * fo, __uint_as_float(o[cc][c + 7]) * fo);
+          }
+          warp_store_staged<NC>(stage, ch, lane,
+                                reinterpret_cast<char*>(static_cast<uint16_t*>(p.out) + wbase + h * (D / 2)),
+                                p.o_sr * 2, wvalid);
         }
       }
       if (rvalid) {
