@@ -18,10 +18,10 @@
 //
 // Warp roles (384 threads):
 //   warp 0      TMA producer: Q tiles once per unit, then K_j, V_j into a ring
-//               of shared-memory stages. The pages' "receive the next shard
-//               while computing the current one" (blog, "A simple forward
-//               schedule"; glossary "Communication overlap") becomes this
-//               multi-stage prefetch with full/empty mbarriers.
+//               of shared-memory stages. The pages overlap the transfer of the
+//               next key/value shard with work on the current one (blog, "A
+//               simple forward schedule"; glossary "Communication overlap");
+//               here that is this multi-stage prefetch with full/empty mbarriers.
 //   warp 1      MMA issuer (the warp waits, one elected lane issues) and TMEM
 //               owner.
 //   warps 4-7   softmax warpgroup for query tile 0 (TMEM lanes 0-127)
