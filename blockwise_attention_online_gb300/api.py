@@ -55,7 +55,7 @@ def _segments(q: torch.Tensor, q_segments):
     return arr, len(q_segments)
 
 
-def _chunks(k_chunks, v_chunks, chunk_spans):
+def _chunks(k_chunks, v_chunks, chunk_spans, host=False):
     if len(k_chunks) != len(v_chunks):
         raise ValueError("need as many value chunks as key chunks")
     if chunk_spans is None:
@@ -65,7 +65,8 @@ def _chunks(k_chunks, v_chunks, chunk_spans):
             p += k.shape[2]
     arr = (KvChunk * max(1, len(k_chunks)))()
     for i, (k, v) in enumerate(zip(k_chunks, v_chunks)):
-        _check_cuda(k, "k"); _check_cuda(v, "v")
+        if not host:
+            _check_cuda(k, "k"); _check_cuda(v, "v")
         if k.shape != v.shape:
             raise ValueError("k and v chunks must have the same shape")
         arr[i].k = k.data_ptr()
@@ -123,6 +124,45 @@ def ring_attention(q, k_chunks, v_chunks, *, chunk_spans=None, q_segments=None,
     chs, nch = _chunks(k_chunks, v_chunks, chunk_spans)
     check(lib.ra_ring_attention(ctypes.byref(pb), q.data_ptr(), segs, nsegs, chs, nch,
                                 out.data_ptr(), m.data_ptr(), l.data_ptr(), _stream(stream)))
+    return out, m, l
+
+
+def ring_attention_host(q, k_chunks, v_chunks, *, chunk_spans=None, q_segments=None,
+                        causal=False, scale=None, out=None, m=None, l=None, out_dtype=None,
+                        stream=None):
+    """ring_attention with every tensor in host memory (pinned for full speed).
+
+    The library copies the inputs to the device, runs the ring kernel and
+    copies O, m, l back, all enqueued on ``stream`` (default: the current CUDA
+    stream). The results are valid, and the inputs may be changed, only after
+    that stream has been synchronised. All tensors must be contiguous CPU
+    tensors; calls on different streams overlap copies with kernels.
+    Returns (O, m, l) as host tensors.
+    """
+    lib = load()
+    for t in [q, *k_chunks, *v_chunks]:
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError("ring_attention_host takes contiguous CPU tensors")
+    B, Hq, Sq, D = q.shape
+    Hkv = k_chunks[0].shape[1] if k_chunks else Hq
+    pin = q.is_pinned()
+    if out is None:
+        out = torch.empty(q.shape, dtype=out_dtype or q.dtype, pin_memory=pin)
+    if out.dtype not in (q.dtype, torch.float32):
+        raise TypeError("O must have the dtype of q or float32")
+    if m is None:
+        m = torch.empty(B, Hq, Sq, dtype=torch.float32, pin_memory=pin)
+    if l is None:
+        l = torch.empty(B, Hq, Sq, dtype=torch.float32, pin_memory=pin)
+    for t in (out, m, l):
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError("outputs must be contiguous CPU tensors")
+    pb = _problem(q, Hkv, causal, scale, _strides(out))
+    pb.o_fp32 = 1 if (out.dtype == torch.float32 and q.dtype != torch.float32) else 0
+    segs, nsegs = _segments(q, q_segments)
+    chs, nch = _chunks(k_chunks, v_chunks, chunk_spans, host=True)
+    check(lib.ra_ring_attention_host(ctypes.byref(pb), q.data_ptr(), segs, nsegs, chs, nch,
+                                     out.data_ptr(), m.data_ptr(), l.data_ptr(), _stream(stream)))
     return out, m, l
 
 

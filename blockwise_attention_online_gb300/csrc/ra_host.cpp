@@ -2,7 +2,9 @@
 // building (position spans, ring visit order, causal work per query tile
 // pair, longest-first order), TMA tensor-map creation and kernel launches.
 //
-// No device memory is allocated here: plans travel as kernel parameters.
+// Plans travel as kernel parameters. Device memory is allocated only for the
+// scratch of split units and for the device copies of the host-buffer entry
+// point, stream-ordered, from one library pool per device.
 #include "ra.h"
 
 #include <cuda.h>
@@ -16,6 +18,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <functional>
 #include <mutex>
 #include <numeric>
 #include <vector>
@@ -257,6 +260,49 @@ ra_status cuda_status(int err, const char* what) {
   return fail(RA_ERR_CUDA, "%s: %s", what, cudaGetErrorString((cudaError_t)err));
 }
 
+// ----------------------------------------------------------- memory pool
+// Stream-ordered allocations of the library come from one pool per device.
+// The pool keeps up to kPoolKeepBytes mapped across synchronisations (the
+// default pool would return everything at each synchronisation, and the next
+// call would wait while memory is mapped again).
+constexpr uint64_t kPoolKeepBytes = uint64_t(4) << 30;
+
+ra_status lib_pool(cudaMemPool_t* out) {
+  constexpr int kMaxDevices = 64;
+  static std::mutex mu;
+  static cudaMemPool_t pools[kMaxDevices] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_status(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(RA_ERR_UNSUPPORTED, "device %d out of range", dev);
+  std::lock_guard<std::mutex> lock(mu);
+  if (!pools[dev]) {
+    cudaMemPoolProps props;
+    std::memset(&props, 0, sizeof(props));
+    props.allocType = cudaMemAllocationTypePinned;
+    props.handleTypes = cudaMemHandleTypeNone;
+    props.location.type = cudaMemLocationTypeDevice;
+    props.location.id = dev;
+    cudaMemPool_t pool = nullptr;
+    e = cudaMemPoolCreate(&pool, &props);
+    if (e != cudaSuccess) return cuda_status(e, "creating the library memory pool");
+    uint64_t keep = kPoolKeepBytes;
+    e = cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep);
+    if (e != cudaSuccess) {
+      cudaMemPoolDestroy(pool);
+      return cuda_status(e, "configuring the library memory pool");
+    }
+    pools[dev] = pool;
+  }
+  *out = pools[dev];
+  return RA_OK;
+}
+
+// Enqueued on the launch stream after every check and plan has succeeded and
+// right before the kernel launch (the host-buffer entry point copies its
+// inputs here). Empty for the device-pointer entry points.
+using BeforeLaunch = std::function<ra_status()>;
+
 void fill_q_pieces(const Common& c, ra::QPiece* qp, int32_t* n) {
   *n = (int32_t)c.qspans.size();
   for (size_t i = 0; i < c.qspans.size(); ++i) {
@@ -272,8 +318,8 @@ enum class ScratchSource { kAllocate, kStatic };
 
 ra_status run_tc(const Common& c, const ra_problem& p, const void* q,
                  const ra_kv_chunk* chunks, void* out, float* m, float* l,
-                 bool stats_mode, void* stream,
-                 ScratchSource source = ScratchSource::kAllocate) {
+                 bool stats_mode, void* stream, ScratchSource source,
+                 const BeforeLaunch& before_launch) {
   if (c.nchunks > ra::kTcMaxChunks)
     return fail(RA_ERR_UNSUPPORTED, "bf16 path handles at most %d chunks, got %d",
                 ra::kTcMaxChunks, c.nchunks);
@@ -413,6 +459,7 @@ ra_status run_tc(const Common& c, const ra_problem& p, const void* q,
       return fail(RA_ERR_UNSUPPORTED, "split needs %zu bytes of scratch, the fixed array holds %zu",
                   bytes, cap);
     ra::tc_scratch_carve(base, int(G), int(c.D), &plan.scratch);
+    if (before_launch && (st = before_launch()) != RA_OK) return st;
     // the array keeps the previous call's contents: clear the flags
     e = cudaMemsetAsync(plan.scratch.flags, 0, size_t(G) * 2 * sizeof(unsigned), cs);
     if (e != cudaSuccess) return cuda_status(e, "clearing stream-K flags");
@@ -420,14 +467,22 @@ ra_status run_tc(const Common& c, const ra_problem& p, const void* q,
   }
   if (split) {
     const size_t bytes = ra::tc_scratch_bytes(int(G), int(c.D));
-    cudaError_t e = cudaMallocAsync(&scratch, bytes, cs);
+    cudaMemPool_t pool = nullptr;
+    if ((st = lib_pool(&pool)) != RA_OK) return st;
+    cudaError_t e = cudaMallocFromPoolAsync(&scratch, bytes, pool, cs);
     if (e != cudaSuccess) return cuda_status(e, "allocating stream-K scratch");
     ra::tc_scratch_carve(scratch, int(G), int(c.D), &plan.scratch);
+    if (before_launch && (st = before_launch()) != RA_OK) {
+      cudaFreeAsync(scratch, cs);
+      return st;
+    }
     e = cudaMemsetAsync(plan.scratch.flags, 0, size_t(G) * 2 * sizeof(unsigned), cs);
     if (e != cudaSuccess) {
       cudaFreeAsync(scratch, cs);
       return cuda_status(e, "clearing stream-K flags");
     }
+  } else if (before_launch && (st = before_launch()) != RA_OK) {
+    return st;
   }
   const int err = ra::launch_tc_bf16(plan, int(c.D), stream);
   if (scratch) cudaFreeAsync(scratch, cs);
@@ -437,7 +492,7 @@ ra_status run_tc(const Common& c, const ra_problem& p, const void* q,
 // ----------------------------------------------------------- fp32 plan
 ra_status run_simt(const Common& c, const ra_problem& p, const void* q,
                    const ra_kv_chunk* chunks, void* out, float* m, float* l,
-                   bool stats_mode, void* stream) {
+                   bool stats_mode, void* stream, const BeforeLaunch& before_launch) {
   if (c.nchunks > ra::kSimtMaxChunks)
     return fail(RA_ERR_UNSUPPORTED, "fp32 path handles at most %d chunks, got %d",
                 ra::kSimtMaxChunks, c.nchunks);
@@ -470,20 +525,115 @@ ra_status run_simt(const Common& c, const ra_problem& p, const void* q,
                   ch.v_strides.batch, ch.v_strides.head, ch.v_strides.row};
   }
   if (c.Sq == 0) return ok();
+  if (before_launch) {
+    const ra_status hs = before_launch();
+    if (hs != RA_OK) return hs;
+  }
   return cuda_status(ra::launch_simt_f32(plan, stream), "fp32 ring kernel launch");
 }
 
 ra_status run(const ra_problem* pb, const void* q, const ra_q_segment* segs, int32_t nsegs,
               const ra_kv_chunk* chunks, int32_t nchunks, void* out, float* m, float* l,
               bool stats_mode, void* stream,
-              ScratchSource source = ScratchSource::kAllocate) {
+              ScratchSource source = ScratchSource::kAllocate,
+              const BeforeLaunch& before_launch = BeforeLaunch()) {
   Common c;
   ra_status st = validate(pb, q, segs, nsegs, chunks, nchunks, &c);
   if (st != RA_OK) return st;
   if (c.Sq == 0) return ok();
   if (!out || !m || !l) return fail(RA_ERR_INVALID, "output pointer is NULL");
-  if (c.dtype == RA_BF16) return run_tc(c, *pb, q, chunks, out, m, l, stats_mode, stream, source);
-  return run_simt(c, *pb, q, chunks, out, m, l, stats_mode, stream);
+  if (c.dtype == RA_BF16)
+    return run_tc(c, *pb, q, chunks, out, m, l, stats_mode, stream, source, before_launch);
+  return run_simt(c, *pb, q, chunks, out, m, l, stats_mode, stream, before_launch);
+}
+
+// Dense strides of a [B, H, rows, D] tensor; axes of extent 1 accept any stride.
+bool is_dense(const ra_strides& s, int64_t B, int64_t H, int64_t rows, int64_t D) {
+  return (rows <= 1 || s.row == D) && (H <= 1 || s.head == rows * D) &&
+         (B <= 1 || s.batch == H * rows * D);
+}
+
+ra_status run_host(const ra_problem* pb, const void* q, const ra_q_segment* segs, int32_t nsegs,
+                   const ra_kv_chunk* chunks, int32_t nchunks, void* o, float* m, float* l,
+                   void* stream) {
+  Common c;
+  ra_status st = validate(pb, q, segs, nsegs, chunks, nchunks, &c);
+  if (st != RA_OK) return st;
+  if (c.Sq == 0) return ok();
+  if (!o || !m || !l) return fail(RA_ERR_INVALID, "output pointer is NULL");
+  const ra_problem& p = *pb;
+  if (!is_dense(p.q_strides, c.B, c.Hq, c.Sq, c.D)) return fail(RA_ERR_INVALID, "host q must be dense");
+  if (!is_dense(p.o_strides, c.B, c.Hq, c.Sq, c.D)) return fail(RA_ERR_INVALID, "host o must be dense");
+  for (int32_t k = 0; k < nchunks; ++k) {
+    const ra_kv_chunk& ch = chunks[k];
+    if (ch.len > 0 && (!is_dense(ch.k_strides, c.B, c.Hkv, ch.len, c.D) ||
+                       !is_dense(ch.v_strides, c.B, c.Hkv, ch.len, c.D)))
+      return fail(RA_ERR_INVALID, "host chunk %d: k and v must be dense", k);
+  }
+  const size_t es = p.dtype == RA_BF16 ? 2 : 4;
+  const size_t oes = (p.dtype == RA_BF16 && p.o_fp32 == 1) ? 4 : es;
+  auto up = [](size_t n) { return (n + 255) & ~size_t(255); };
+  const size_t rows = size_t(c.B * c.Hq * c.Sq);
+  const size_t q_bytes = rows * size_t(c.D) * es, o_bytes = rows * size_t(c.D) * oes;
+  size_t total = up(q_bytes) + up(o_bytes) + 2 * up(rows * 4);
+  std::vector<size_t> kv_bytes(nchunks, 0);
+  for (int32_t k = 0; k < nchunks; ++k) {
+    kv_bytes[k] = size_t(c.B * c.Hkv * chunks[k].len) * size_t(c.D) * es;
+    total += 2 * up(kv_bytes[k]);
+  }
+  cudaMemPool_t pool = nullptr;
+  if ((st = lib_pool(&pool)) != RA_OK) return st;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  char* base = nullptr;
+  cudaError_t e = cudaMallocFromPoolAsync(reinterpret_cast<void**>(&base), total, pool, cs);
+  if (e != cudaSuccess) return cuda_status(e, "allocating device copies");
+  // carve: q, o, m, l, then k and v of every chunk
+  char* at = base;
+  auto take = [&](size_t n) { char* r = at; at += up(n); return r; };
+  void* dq = take(q_bytes);
+  void* dout = take(o_bytes);
+  float* dm = reinterpret_cast<float*>(take(rows * 4));
+  float* dl = reinterpret_cast<float*>(take(rows * 4));
+  std::vector<ra_kv_chunk> dch(chunks, chunks + nchunks);
+  std::vector<void*> dk(nchunks, nullptr), dv(nchunks, nullptr);
+  for (int32_t k = 0; k < nchunks; ++k) {
+    if (chunks[k].len > 0) {
+      dk[k] = take(kv_bytes[k]);
+      dv[k] = take(kv_bytes[k]);
+    }
+    dch[k].k = dk[k];
+    dch[k].v = dv[k];
+  }
+  ra_problem dp = p;
+  const ra_strides dense_q = {c.Hq * c.Sq * c.D, c.Sq * c.D, c.D};
+  dp.q_strides = dense_q;
+  dp.o_strides = dense_q;
+  for (int32_t k = 0; k < nchunks; ++k) {
+    const ra_strides ds = {c.Hkv * chunks[k].len * c.D, chunks[k].len * c.D, c.D};
+    dch[k].k_strides = ds;
+    dch[k].v_strides = ds;
+  }
+  // one copy per buffer, issued only once the plan has been accepted
+  const BeforeLaunch copy_in = [&]() -> ra_status {
+    cudaError_t err = cudaMemcpyAsync(dq, q, q_bytes, cudaMemcpyHostToDevice, cs);
+    for (int32_t k = 0; err == cudaSuccess && k < nchunks; ++k) {
+      if (kv_bytes[k] == 0) continue;
+      err = cudaMemcpyAsync(dk[k], chunks[k].k, kv_bytes[k], cudaMemcpyHostToDevice, cs);
+      if (err == cudaSuccess)
+        err = cudaMemcpyAsync(dv[k], chunks[k].v, kv_bytes[k], cudaMemcpyHostToDevice, cs);
+    }
+    return cuda_status(err, "copying inputs to the device");
+  };
+  st = run(&dp, dq, segs, nsegs, dch.data(), nchunks, dout, dm, dl, false, stream,
+           ScratchSource::kAllocate, copy_in);
+  if (st == RA_OK) {
+    e = cudaMemcpyAsync(o, dout, o_bytes, cudaMemcpyDeviceToHost, cs);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(m, dm, rows * 4, cudaMemcpyDeviceToHost, cs);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(l, dl, rows * 4, cudaMemcpyDeviceToHost, cs);
+    st = cuda_status(e, "copying outputs to the host");
+  }
+  cudaFreeAsync(base, cs);
+  return st;
 }
 
 }  // namespace
@@ -511,6 +661,13 @@ ra_status ra_ring_attention_noalloc(const ra_problem* problem, const void* q,
                                     float* m, float* l, void* stream) {
   return run(problem, q, segs, nsegs, chunks, nchunks, o, m, l, false, stream,
              ScratchSource::kStatic);
+}
+
+ra_status ra_ring_attention_host(const ra_problem* problem, const void* q,
+                                 const ra_q_segment* segs, int32_t nsegs,
+                                 const ra_kv_chunk* chunks, int32_t nchunks, void* o,
+                                 float* m, float* l, void* stream) {
+  return run_host(problem, q, segs, nsegs, chunks, nchunks, o, m, l, stream);
 }
 
 ra_status ra_merge_stats(int64_t rows, int64_t D, float* u_acc, float* l_acc, float* m_acc,

@@ -14,10 +14,12 @@
  * Common conventions
  * ------------------
  * - Every pointer passed to a compute entry point is a DEVICE pointer owned
- *   by the caller; the library never frees or retains it. The only memory
- *   the library itself allocates is ra_ring_attention's per-call scratch
- *   (see there). Descriptor structs are read on the host during the call
- *   only.
+ *   by the caller (ra_ring_attention_host alone takes host pointers); the
+ *   library never frees or retains it. The only device memory the library
+ *   itself allocates is the per-call scratch of ra_ring_attention and the
+ *   device copies of ra_ring_attention_host, stream-ordered, from one library
+ *   memory pool per device. Descriptor structs are read on the host during
+ *   the call only.
  * - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
  *   stream). A returned RA_OK means the work was validated and enqueued.
  * - Every argument is validated before anything is enqueued. On any non-OK
@@ -167,8 +169,9 @@ ra_status ra_merge_stats(int64_t rows, int64_t D,
  * Causal key/value tiles that lie entirely in a query tile's future are
  * skipped; only tiles that straddle the diagonal are masked elementwise.
  * When the last rounds of work are split across CTAs (bf16 path), the call
- * allocates a scratch buffer of up to about 21 MB with cudaMallocAsync on
- * `stream` and frees it with cudaFreeAsync on the same stream.
+ * allocates a scratch buffer of up to about 21 MB from the library's memory
+ * pool on `stream` (cudaMallocFromPoolAsync) and frees it with cudaFreeAsync
+ * on the same stream.
  * Limits of this build (RA_ERR_UNSUPPORTED beyond them): bf16 at most 32
  * non-empty chunks and 64 spans over all chunks; fp32 at most 256 chunks and
  * 320 spans; at most 64 spans over all query segments.
@@ -211,6 +214,33 @@ ra_status ra_ring_attention_noalloc(const ra_problem* problem, const void* q,
                                     const ra_q_segment* segs, int32_t nsegs,
                                     const ra_kv_chunk* chunks, int32_t nchunks,
                                     void* o, float* m, float* l, void* stream);
+
+/*
+ * ra_ring_attention_host - ra_ring_attention with every input and output in
+ * HOST memory. (The pages have no counterpart: this is the end-to-end form of
+ * the same pass, for callers whose tensors live on the host.)
+ *
+ * All work is stream-ordered on `stream`: the library takes device buffers
+ * for Q, the chunks, O, m and l from its memory pool, copies the inputs in
+ * (one cudaMemcpyAsync per buffer, issued only after the problem has been
+ * validated and planned), runs the kernel of ra_ring_attention, copies O, m
+ * and l out and releases the buffers. The call returns once all of that is
+ * enqueued. The host buffers must stay valid and unchanged until `stream` has
+ * passed this call (cudaStreamSynchronize, an event); page-locked (pinned)
+ * host memory gives full copy bandwidth and truly asynchronous copies. Calls
+ * on different streams overlap one call's copies with another call's kernel.
+ *
+ * Arguments, positions and results are those of ra_ring_attention, with two
+ * differences: every pointer (q, chunks[k].k, chunks[k].v, o, m, l) is a host
+ * pointer, and every tensor must be dense: q and o as [B, Hq, Sq, D], the k
+ * and v of chunk k as [B, Hkv, len_k, D] (strides of axes with extent 1 are
+ * ignored); RA_ERR_INVALID otherwise. The pool keeps up to 4 GiB mapped
+ * between calls.
+ */
+ra_status ra_ring_attention_host(const ra_problem* problem, const void* q,
+                                 const ra_q_segment* segs, int32_t nsegs,
+                                 const ra_kv_chunk* chunks, int32_t nchunks,
+                                 void* o, float* m, float* l, void* stream);
 
 /*
  * ra_segment_work - host-only bookkeeping for comparing sequence layouts

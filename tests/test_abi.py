@@ -150,3 +150,33 @@ def test_segment_work_is_exact(kind, causal):
     assert all(t * 128 * 128 >= pr for t, pr in zip(tiles, pairs))
     if causal and kind == "zigzag":
         assert max(pairs) == min(pairs)
+
+
+def _call_host(p, segs, nsegs, chunks, nchunks, q=4096, o=4096, m=4096, l=4096):
+    lib = _lib.load()
+    return lib.ra_ring_attention_host(ctypes.byref(p), q, segs, nsegs, chunks, nchunks,
+                                      o, m, l, None)
+
+
+def test_host_entry_rejects_before_touching_the_device():
+    """ra_ring_attention_host validates everything, including that host
+    tensors are dense, before it allocates or copies anything."""
+    p = _problem()
+    # the same descriptor checks as the device entry point
+    assert _call_host(p, _segs([(200, [(200, 0, 1)])]), 1, _chunks(GOOD_CHUNKS), 2) == _lib.RA_ERR_INVALID
+    assert _call_host(p, _segs(GOOD_SEGS), 1, _chunks(GOOD_CHUNKS), 2, o=None) == _lib.RA_ERR_INVALID
+    # q padded between rows: not dense
+    p2 = _problem()
+    p2.q_strides = _lib.Strides(2 * 256 * 136, 256 * 136, 136)
+    assert _call_host(p2, _segs(GOOD_SEGS), 1, _chunks(GOOD_CHUNKS), 2) == _lib.RA_ERR_INVALID
+    assert "dense" in _lib.load().ra_last_error().decode()
+    # O with a foreign head stride
+    p3 = _problem()
+    p3.o_strides = _lib.Strides(2 * 256 * 128, 512 * 128, 128)
+    assert _call_host(p3, _segs(GOOD_SEGS), 1, _chunks(GOOD_CHUNKS), 2) == _lib.RA_ERR_INVALID
+    # a chunk whose k rows are strided
+    ch = _chunks(GOOD_CHUNKS)
+    ch[1].k_strides = _lib.Strides(128 * 256, 128 * 256, 256)
+    assert _call_host(p, _segs(GOOD_SEGS), 1, ch, 2) == _lib.RA_ERR_INVALID
+    # an empty problem is a valid no-op
+    assert _call_host(_problem(Sq=0), _segs([(0, [(0, 0, 1)])]), 1, _chunks(GOOD_CHUNKS), 2) == _lib.RA_OK
