@@ -10,9 +10,10 @@ upcast exactly to float64 before any arithmetic.
 Sources (web pages; cited by title and section):
 
 * [EX]  Ring-attention exercise page "systems-distributed-ring-attention-online-
-        softmax": task statement (the three functions, their outputs, the
-        invariance "for any way of splitting ... even chunks of size 1") and
-        its two hints (max subtraction; the exp(own_max - new_max) rescale).
+        softmax": task statement (the three functions, their outputs, and the
+        requirement that the result not depend on how the keys are split,
+        down to chunks of one key) and its two hints (max subtraction; the
+        exp(own_max - new_max) rescale).
 * [BLOG] "Ring Attention: Distributed Reads with Online Softmax":
         sections "Partition the sequence across devices", "Do not average
         independently normalized shard outputs", "A simple forward schedule",
@@ -136,9 +137,9 @@ def normalize(u, l):
 def full_attention(q, k, v, q_pos, k_pos, causal, scale):
     """Ordinary softmax attention over the whole key/value sequence at once.
 
-    This is the plain definition the chunked method must equal exactly ([EX]
-    task statement: "the exact same result as computing ordinary attention over
-    the full, concatenated key/value sequence"). Per row: m = max of visible
+    This is the plain definition the chunked method must equal exactly: the
+    [EX] task statement asks for the result of ordinary attention over all
+    key/value chunks joined into one sequence. Per row: m = max of visible
     scaled scores, l = sum exp(s - m), O = sum exp(s - m) v / l.
 
     Returns O [B, Hq, Sq, D], m [B, Hq, Sq], l [B, Hq, Sq].

@@ -5,8 +5,8 @@ tests, smoke() and bench.py's CPU legs.
 
 * contiguous: [BLOG] "Partition the sequence across devices": device r holds
   roughly n/P consecutive positions.
-* zigzag: [BLOG] "Causal masks depend on global positions": "paired
-  early/late chunks" balance causal work. Reading: the sequence is cut into
+* zigzag: [BLOG] "Causal masks depend on global positions": pairing an early
+  chunk with a late one balances causal work. Reading: the sequence is cut into
   2P equal blocks and device r owns block r followed by block 2P-1-r.
 * striped: [GLOS] "Variants (1) Striped attention": tokens are reordered so
   each chunk holds positions from all over the sequence. Reading: device r
