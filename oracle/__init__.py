@@ -1,4 +1,4 @@
-"""fp64 CPU oracle for ring attention's chunked forward pass.
+"""fp64 CPU oracle for ring attention's chunked forward pass and its backward.
 
 TEST INFRASTRUCTURE ONLY: imported by tests/, __graft_entry__.smoke() and the
 CPU legs of bench.py, never by the library. See ``oracle.attention``.
@@ -6,8 +6,9 @@ CPU legs of bench.py, never by the library. See ``oracle.attention``.
 from .attention import (NEG_INF, attention_rows, chunk_stats, full_attention,
                         merge_stats, normalize, ring_attention, ring_order,
                         unmasked_pairs)
+from .backward import attention_backward, ring_attention_backward
 from . import layouts
 
 __all__ = ["NEG_INF", "attention_rows", "chunk_stats", "full_attention",
            "merge_stats", "normalize", "ring_attention", "ring_order",
-           "unmasked_pairs", "layouts"]
+           "unmasked_pairs", "layouts", "attention_backward", "ring_attention_backward"]
