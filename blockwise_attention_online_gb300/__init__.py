@@ -4,8 +4,9 @@ torch binding. The binding loads the library on first use and raises if it
 has not been built; there is no CPU fallback.
 """
 from .api import (chunk_stats, default_scale, device_status, merge_stats,
-                  ring_attention, ring_attention_host, segment_work)
+                  ring_attention, ring_attention_bwd, ring_attention_host, segment_work)
 from ._lib import RaError
 
 __all__ = ["chunk_stats", "default_scale", "device_status", "merge_stats",
-           "ring_attention", "ring_attention_host", "segment_work", "RaError"]
+           "ring_attention", "ring_attention_bwd", "ring_attention_host", "segment_work",
+           "RaError"]

@@ -21,8 +21,8 @@ STATUS_NAMES = {0: "RA_OK", 1: "RA_ERR_INVALID", 2: "RA_ERR_UNSUPPORTED",
 
 # every symbol include/ra.h declares
 EXPORTED = ("ra_chunk_stats", "ra_merge_stats", "ra_ring_attention",
-            "ra_ring_attention_noalloc", "ra_ring_attention_host", "ra_segment_work",
-            "ra_device_status", "ra_last_error", "ra_version")
+            "ra_ring_attention_noalloc", "ra_ring_attention_host", "ra_ring_attention_bwd",
+            "ra_segment_work", "ra_device_status", "ra_last_error", "ra_version")
 
 
 class Span(ctypes.Structure):
@@ -40,6 +40,10 @@ class Strides(ctypes.Structure):
 class KvChunk(ctypes.Structure):
     _fields_ = [("k", c_void_p), ("v", c_void_p), ("len", c_int64),
                 ("k_strides", Strides), ("v_strides", Strides), ("pos", Positions)]
+
+
+class KvGrad(ctypes.Structure):
+    _fields_ = [("dk", c_void_p), ("dv", c_void_p)]
 
 
 class QSegment(ctypes.Structure):
@@ -86,6 +90,9 @@ def load():
                                           c_void_p]
         lib.ra_ring_attention_noalloc.argtypes = lib.ra_ring_attention.argtypes
         lib.ra_ring_attention_host.argtypes = lib.ra_ring_attention.argtypes
+        lib.ra_ring_attention_bwd.argtypes = [P(Problem), c_void_p, P(QSegment), c_int32,
+                                              P(KvChunk), c_int32, c_void_p, c_void_p, c_void_p,
+                                              c_void_p, c_void_p, P(KvGrad), c_void_p]
         lib.ra_segment_work.argtypes = [P(Problem), P(QSegment), c_int32, P(KvChunk), c_int32,
                                         c_void_p, c_void_p]
         lib.ra_device_status.argtypes = [c_void_p]
@@ -94,8 +101,8 @@ def load():
         lib.ra_version.restype = c_int32
         lib.ra_version.argtypes = []
         for name in ("ra_chunk_stats", "ra_merge_stats", "ra_ring_attention",
-                     "ra_ring_attention_noalloc", "ra_ring_attention_host", "ra_segment_work",
-                     "ra_device_status"):
+                     "ra_ring_attention_noalloc", "ra_ring_attention_host",
+                     "ra_ring_attention_bwd", "ra_segment_work", "ra_device_status"):
             getattr(lib, name).restype = c_int32
         _lib = lib
         return lib

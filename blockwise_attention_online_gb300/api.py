@@ -166,6 +166,48 @@ def ring_attention_host(q, k_chunks, v_chunks, *, chunk_spans=None, q_segments=N
     return out, m, l
 
 
+def ring_attention_bwd(q, k_chunks, v_chunks, o, dout, m, l, *, chunk_spans=None,
+                       q_segments=None, causal=False, scale=None, dq=None, dk=None, dv=None,
+                       stream=None):
+    """Gradients of ``ring_attention``'s O: (dq, [dk per chunk], [dv per chunk]).
+
+    q, k_chunks, v_chunks, chunk_spans, q_segments, causal, scale: exactly as
+    given to the forward call; o, m, l: its outputs; dout: bf16 gradient of O
+    with o's strides. Gradients are fp32: dq like q, dk/dv like each chunk
+    (dense). bf16 inputs only.
+    """
+    lib = load()
+    for t in (q, o, dout, m, l):
+        _check_cuda(t, "tensors")
+    if dout.shape != o.shape or dout.stride() != o.stride():
+        raise ValueError("dout must have o's shape and strides")
+    if dout.dtype != torch.bfloat16:
+        raise TypeError("dout must be bfloat16")
+    B, Hq, Sq, D = q.shape
+    Hkv = k_chunks[0].shape[1] if k_chunks else Hq
+    if dq is None:
+        dq = torch.empty(B, Hq, Sq, D, device=q.device, dtype=torch.float32)
+    if dk is None:
+        dk = [torch.empty(k.shape, device=q.device, dtype=torch.float32) for k in k_chunks]
+    if dv is None:
+        dv = [torch.empty(v.shape, device=q.device, dtype=torch.float32) for v in v_chunks]
+    for t in [dq, *dk, *dv]:
+        if t.dtype != torch.float32 or not t.is_contiguous():
+            raise ValueError("gradients are dense fp32 tensors")
+    pb = _problem(q, Hkv, causal, scale, _strides(o))
+    pb.o_fp32 = 1 if (o.dtype == torch.float32 and q.dtype != torch.float32) else 0
+    segs, nsegs = _segments(q, q_segments)
+    chs, nch = _chunks(k_chunks, v_chunks, chunk_spans)
+    grads = (_lib.KvGrad * max(1, nch))()
+    for i in range(nch):
+        grads[i].dk = dk[i].data_ptr()
+        grads[i].dv = dv[i].data_ptr()
+    check(lib.ra_ring_attention_bwd(ctypes.byref(pb), q.data_ptr(), segs, nsegs, chs, nch,
+                                    o.data_ptr(), dout.data_ptr(), m.data_ptr(), l.data_ptr(),
+                                    dq.data_ptr(), grads, _stream(stream)))
+    return dq, dk, dv
+
+
 def chunk_stats(q, k, v, *, spans=None, q_segments=None, causal=False, scale=None,
                 u=None, l=None, m=None, stream=None):
     """(u, l, m) of one key/value chunk, as if it were the only one.

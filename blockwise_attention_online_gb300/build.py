@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(BUILD, "libra.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["ra_tc.cu", "ra_simt.cu", "ra_host.cpp"]
+SOURCES = ["ra_tc.cu", "ra_bwd.cu", "ra_simt.cu", "ra_host.cpp"]
 
 
 def _nvcc():

@@ -1,0 +1,723 @@
+// Backward pass of the ring forward on the 5th-generation tensor cores:
+// dQ, and dK, dV of every key/value chunk, in fp32.
+//
+// "Ring Attention: Distributed Reads with Online Softmax", section "Backward
+// must aggregate shared dependencies": a query row's gradient reaches every
+// key/value shard it attended to and has to be summed per shard for the
+// shard's owner; the probability tiles may be recomputed, with the forward's
+// scale and masks. Here the forward's row statistics (m, l) fix every
+// probability, P = exp(s - m) / l = exp2(s * scale * log2(e) - lse2), so each
+// tile is recomputed independently of the visit order:
+//
+//   dV_c = P_c^T dO              dP_c = dO V_c^T
+//   dS_c = P_c * (dP_c - delta)  delta = rowsum(dO * O)
+//   dK_c = scale dS_c^T Q        dQ   = scale sum_c dS_c K_c
+//
+// Three launches on the caller's stream:
+//   bwd_prep_kernel / bwd_qtile_kernel  lse2 and delta per query row; lowest
+//                                       and highest position of each
+//                                       128-row query tile
+//   bwd_dkv_kernel<D>  one CTA per (batch, key/value head, 128-row key tile):
+//                      walks every live query tile of the heads that read it
+//                      and accumulates dK, dV in TMEM (the per-shard sum)
+//   bwd_dq_kernel<D>   one CTA per (batch, query head, 128-row query tile):
+//                      walks every live key tile and accumulates dQ in TMEM
+//
+// Warp roles of both tcgen05 kernels (256 threads): warp 0 TMA producer,
+// warp 1 MMA warp (waits warp-uniformly, one elected lane issues), warps 2-3
+// idle, warps 4-7 one TMEM lane (= tile row) per thread for the elementwise
+// work. Every mbarrier wait is bounded (see ra_wait.cuh).
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "ra.h"
+#include "ra_plan.h"
+#include "ra_ptx.cuh"
+#include "ra_wait.cuh"
+
+namespace ra {
+namespace {
+
+using namespace ptx;
+
+constexpr int kBwdThreads = 256;
+constexpr float kInf = __builtin_huge_valf();
+constexpr float kLog2e = 1.4426950408889634f;
+
+enum : int {
+  kSiteBwdKv = 31, kSiteBwdStage = 32, kSiteBwdEmpty = 33, kSiteBwdSdp = 34, kSiteBwdDs = 35,
+  kSiteBwdAcc = 36
+};
+
+template <int D>
+struct BwdCfg {
+  static constexpr int kTileBytes = 128 * D * 2;  // one 128-row bf16 tile
+  static constexpr int kBoxBytes = 128 * 128;     // 128 rows x 64 bf16 (one swizzle atom wide)
+  static constexpr int kBoxes = D / 64;
+  // shared memory: two resident tiles, two stages of two tiles, per-stage
+  // column data (three arrays of 128 words), barriers
+  static constexpr int kRes0 = 0, kRes1 = kTileBytes;
+  static constexpr int kStage0 = 2 * kTileBytes;
+  static constexpr int kStageBytes = 2 * kTileBytes;
+  static constexpr int kAux0 = kStage0 + 2 * kStageBytes;
+  static constexpr int kAuxBytes = 3 * 128 * 4;
+  static constexpr int kBar = kAux0 + 2 * kAuxBytes;
+  static constexpr int kBarBytes = 256;
+  static constexpr int kSmemBytes = kBar + kBarBytes + 1024;  // + alignment slack
+  static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+};
+
+__device__ __forceinline__ int bwd_row_position(const BwdPlan& p, int row) {
+  int lo = 0, hi = p.n_qpieces - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (p.qp[mid].row0 <= row) lo = mid; else hi = mid - 1;
+  }
+  const QPiece& q = p.qp[lo];
+  return q.pos0 + q.step * (row - q.row0);
+}
+
+// Key tiles of span k not entirely in the future of position qmax.
+__device__ __forceinline__ int bwd_live_tiles(const BwdPlan& p, int k, int qmax) {
+  const KvSeg& s = p.ks[k];
+  if (!p.causal) return s.ntiles;
+  if (qmax < s.pos0) return 0;
+  return min(s.ntiles, ((qmax - s.pos0) / s.step) / 128 + 1);
+}
+
+// ------------------------------------------------------------ preparation
+// One thread per query row: delta = sum_d dO * O (O as the forward wrote it)
+// and lse2 = m log2(e) + log2(l), +inf for a row that sees no key.
+__global__ void bwd_prep_kernel(const void* o, int o_fp32, int64_t o_sb, int64_t o_sh,
+                                int64_t o_sr, const uint16_t* dout, const float* m,
+                                const float* l, int B, int Hq, int Sq, int D, float* lse2,
+                                float* delta) {
+  const int64_t row = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t rows = int64_t(B) * Hq * Sq;
+  if (row >= rows) return;
+  const int64_t bh = row / Sq, i = row - bh * Sq;
+  const int64_t b = bh / Hq, h = bh - b * Hq;
+  const int64_t off = b * o_sb + h * o_sh + i * o_sr;
+  const uint4* d4 = reinterpret_cast<const uint4*>(dout + off);
+  float acc = 0.f;
+  if (o_fp32) {
+    const float4* o4 = reinterpret_cast<const float4*>(static_cast<const float*>(o) + off);
+    for (int c = 0; c < D / 8; ++c) {
+      const uint4 g = d4[c];
+      const float4 a = o4[2 * c], bq = o4[2 * c + 1];
+      const uint32_t w[4] = {g.x, g.y, g.z, g.w};
+      const float ov[8] = {a.x, a.y, a.z, a.w, bq.x, bq.y, bq.z, bq.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        acc = fmaf(__uint_as_float(w[k] << 16), ov[2 * k], acc);
+        acc = fmaf(__uint_as_float(w[k] & 0xffff0000u), ov[2 * k + 1], acc);
+      }
+    }
+  } else {
+    const uint4* o4 = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(o) + off);
+    for (int c = 0; c < D / 8; ++c) {
+      const uint4 g = d4[c], a = o4[c];
+      const uint32_t w[4] = {g.x, g.y, g.z, g.w}, v[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        acc = fmaf(__uint_as_float(w[k] << 16), __uint_as_float(v[k] << 16), acc);
+        acc = fmaf(__uint_as_float(w[k] & 0xffff0000u), __uint_as_float(v[k] & 0xffff0000u), acc);
+      }
+    }
+  }
+  delta[row] = acc;
+  const float lr = l[row];
+  lse2[row] = lr > 0.f ? fmaf(m[row], kLog2e, log2f(lr)) : kInf;
+}
+
+// One thread per 128-row query tile: its lowest and highest position.
+__global__ void bwd_qtile_kernel(const __grid_constant__ BwdPlan p, int2* out) {
+  const int t = blockIdx.x * blockDim.x + threadIdx.x;
+  if (t >= p.n_qtiles) return;
+  int lo = 0x7fffffff, hi = -1;
+  const int r1 = min(p.Sq, 128 * t + 128);
+  for (int r = 128 * t; r < r1; ++r) {
+    const int pos = bwd_row_position(p, r);
+    lo = min(lo, pos);
+    hi = max(hi, pos);
+  }
+  out[t] = make_int2(lo, hi);
+}
+
+// ------------------------------------------------------------ shared pieces
+struct BwdBars {
+  uint32_t res_full, st_full0, st_empty0, sdp_full, ew_done, acc_full, done;  // stage s: + 8 s
+  uint32_t* tmem_slot;
+  volatile int* abort_flag;
+};
+
+template <int D>
+__device__ __forceinline__ void bwd_setup(uint8_t* smem_raw, uint32_t& base, uint8_t*& gbase,
+                                          BwdBars& bb) {
+  using C = BwdCfg<D>;
+  const uint32_t raw = smem_addr(smem_raw);
+  base = (raw + 1023u) & ~1023u;
+  gbase = smem_raw + (base - raw);
+  const uint32_t bars = base + C::kBar;
+  bb.res_full = bars;
+  bb.st_full0 = bars + 8;
+  bb.st_empty0 = bars + 24;
+  bb.sdp_full = bars + 40;
+  bb.ew_done = bars + 48;
+  bb.acc_full = bars + 56;
+  bb.done = bars + 64;
+  bb.tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::kBar + 72);
+  bb.abort_flag = reinterpret_cast<volatile int*>(gbase + C::kBar + 76);
+  if (threadIdx.x == 0) {
+    mbar_init(bb.res_full, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bb.st_full0 + 8 * s, 1 + 32);  // the copies' transaction count + 32 producer lanes
+      mbar_init(bb.st_empty0 + 8 * s, 1);
+    }
+    mbar_init(bb.sdp_full, 1);
+    mbar_init(bb.ew_done, 128);
+    mbar_init(bb.acc_full, 1);
+    mbar_init(bb.done, 1);
+    *bb.abort_flag = 0;
+    fence_mbar_init();
+  }
+  if ((threadIdx.x >> 5) == 1) {
+    tmem_alloc(smem_addr(bb.tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+}
+
+__device__ __forceinline__ void bwd_teardown(uint32_t tmem) {
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if ((threadIdx.x >> 5) == 1) tmem_dealloc(tmem, 512);
+}
+
+// Issue one 128 x 128 x D product D[tmem] = A B^T, both operands K-major in
+// shared memory (the layout TMA writes for a [rows, D] tile).
+template <int D>
+__device__ __forceinline__ void issue_abt(uint32_t d_tmem, uint32_t sa, uint32_t sb) {
+  using C = BwdCfg<D>;
+  constexpr uint32_t kId = idesc_bf16_f32(128, 128, 0, 0);
+  const uint64_t ad = sdesc_sw128(sa, 16, 1024), bd = sdesc_sw128(sb, 16, 1024);
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint64_t off = uint64_t(((kk >> 2) * C::kBoxBytes + (kk & 3) * 32) >> 4);
+    mma_ss(d_tmem, ad + off, bd + off, kId, kk > 0 ? 1u : 0u);
+  }
+}
+
+// D[tmem] (+)= A[tmem] B with A 128 x 128 bf16 in TMEM (64 columns) and B a
+// [128 rows (the contraction), D] tile in shared memory (MN-major).
+template <int D>
+__device__ __forceinline__ void issue_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint32_t sb,
+                                             bool acc) {
+  using C = BwdCfg<D>;
+  constexpr uint32_t kId = idesc_bf16_f32(128, D, 0, 1);
+  const uint64_t bd = sdesc_sw128(sb, C::kBoxBytes, 1024);
+#pragma unroll
+  for (int kk = 0; kk < 128 / 16; ++kk)
+    mma_ts(d_tmem, a_tmem + kk * 8, bd + uint64_t((kk * 16 * 128) >> 4), kId,
+           (acc || kk > 0) ? 1u : 0u);
+}
+
+// ------------------------------------------------------------ dK, dV
+// The query tiles a key tile sees: heads hkv*g .. hkv*g + g - 1, every tile
+// whose highest position reaches the key tile's lowest (all when not causal).
+struct QWalk {
+  int idx, n, nqt, h0;
+  __device__ __forceinline__ bool next(const BwdPlan& p, int kmin, int& h, int& qt) {
+    while (idx < n) {
+      const int i = idx++;
+      qt = i % nqt;
+      h = h0 + i / nqt;
+      if (!p.causal || p.qtile_pos[qt].y >= kmin) return true;
+    }
+    return false;
+  }
+};
+
+template <int D>
+__global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkv_kernel(const __grid_constant__ BwdPlan p) {
+  using C = BwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint32_t base;
+  uint8_t* gbase;
+  BwdBars bb;
+  bwd_setup<D>(smem_raw, base, gbase, bb);
+  const uint32_t tmem = *bb.tmem_slot;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const unsigned long long budget = p.timeout_ns;
+
+  // this CTA's key tile
+  int u = blockIdx.x;
+  const int gt = u % p.n_ktiles;
+  u /= p.n_ktiles;
+  const int hkv = u % p.Hkv, b = u / p.Hkv;
+  int ks = 0;
+  while (ks + 1 < p.n_kvsegs && p.kseg_tile_begin[ks + 1] <= gt) ++ks;
+  const KvSeg& sg = p.ks[ks];
+  const int kt = gt - p.kseg_tile_begin[ks];
+  const int krow0 = sg.row0 + 128 * kt;                 // first row within the chunk
+  const int kvalid = min(128, sg.len - 128 * kt);       // rows of the tile that exist
+  const int kmin = sg.pos0 + sg.step * (128 * kt);
+  const int kmax = sg.pos0 + sg.step * (128 * kt + kvalid - 1);
+  const int g = p.Hq / p.Hkv;
+  const uint32_t sK = base + C::kRes0, sV = base + C::kRes1;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------- producer
+    const bool leader = elect_one();
+    if (leader) {
+      mbar_arrive_expect_tx(bb.res_full, 2 * C::kTileBytes);
+#pragma unroll
+      for (int bx = 0; bx < C::kBoxes; ++bx) {
+        tma_load_4d(sK + bx * C::kBoxBytes, &p.kmap[sg.chunk], bb.res_full, bx * 64, krow0, hkv, b);
+        tma_load_4d(sV + bx * C::kBoxBytes, &p.vmap[sg.chunk], bb.res_full, bx * 64, krow0, hkv, b);
+      }
+    }
+    QWalk w{0, g * p.n_qtiles, p.n_qtiles, hkv * g};
+    int h, qt, j = 0;
+    bool ok = true;
+    while (ok && w.next(p, kmin, h, qt)) {
+      const int st = j & 1;
+      ok = warp_wait(bb.st_empty0 + 8 * st, ((j >> 1) & 1) ^ 1, bb.abort_flag, budget, kSiteBwdEmpty);
+      if (!ok) break;
+      const uint32_t sQ = base + C::kStage0 + st * C::kStageBytes, sDO = sQ + C::kTileBytes;
+      if (leader) {
+        mbar_arrive_expect_tx(bb.st_full0 + 8 * st, 2 * C::kTileBytes);
+#pragma unroll
+        for (int bx = 0; bx < C::kBoxes; ++bx) {
+          tma_load_4d(sQ + bx * C::kBoxBytes, &p.qmap, bb.st_full0 + 8 * st, bx * 64, 128 * qt, h, b);
+          tma_load_4d(sDO + bx * C::kBoxBytes, &p.domap, bb.st_full0 + 8 * st, bx * 64, 128 * qt, h, b);
+        }
+      }
+      // per-column data of this query tile: lse2, delta, position
+      float* aux = reinterpret_cast<float*>(gbase + C::kAux0 + st * C::kAuxBytes);
+      const int64_t rowbase = (int64_t(b) * p.Hq + h) * p.Sq;
+      for (int i = lane; i < 128; i += 32) {
+        const int row = 128 * qt + i;
+        const bool valid = row < p.Sq;
+        aux[i] = valid ? p.lse2[rowbase + row] : kInf;
+        aux[128 + i] = valid ? p.delta[rowbase + row] : 0.f;
+        reinterpret_cast<int*>(aux)[256 + i] = valid ? bwd_row_position(p, row) : int(0x80000000);
+      }
+      mbar_arrive(bb.st_full0 + 8 * st);
+      ++j;
+    }
+    if (!ok) {
+      // let the copies in flight land before the CTA goes away
+      drain_wait(bb.res_full, 0, budget);
+      for (int s = 0; s < 2; ++s) {
+        const int last = (j - 1 - s) >= 0 ? ((j - 1 - s) & ~1) + s : -1;
+        if (last >= 0 && last < j) drain_wait(bb.st_full0 + 8 * s, (last >> 1) & 1, budget);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA warp
+    const bool leader = elect_one();
+    const uint32_t tS = tmem, tP = tmem + 128, tdV = tmem + 256, tdK = tmem + 384;
+    bool ok = warp_wait(bb.res_full, 0, bb.abort_flag, budget, kSiteBwdKv);
+    QWalk w{0, g * p.n_qtiles, p.n_qtiles, hkv * g};
+    int h, qt, j = 0;
+    while (ok && w.next(p, kmin, h, qt)) {
+      const int st = j & 1;
+      const uint32_t sQ = base + C::kStage0 + st * C::kStageBytes, sDO = sQ + C::kTileBytes;
+      ok = warp_wait(bb.st_full0 + 8 * st, (j >> 1) & 1, bb.abort_flag, budget, kSiteBwdStage);
+      if (!ok) break;
+      tc_fence_after();
+      if (leader) {
+        issue_abt<D>(tS, sK, sQ);   // S^T  = K Q^T
+        issue_abt<D>(tP, sV, sDO);  // dP^T = V dO^T
+        mma_commit(bb.sdp_full);
+      }
+      __syncwarp();
+      ok = warp_wait(bb.ew_done, j & 1, bb.abort_flag, budget, kSiteBwdDs);
+      if (!ok) break;
+      tc_fence_after();
+      if (leader) {
+        issue_tmem_a<D>(tdV, tS, sDO, j > 0);  // dV += P^T dO
+        issue_tmem_a<D>(tdK, tP, sQ, j > 0);   // dK += dS^T Q
+        mma_commit(bb.st_empty0 + 8 * st);
+      }
+      __syncwarp();
+      ++j;
+    }
+    if (leader) {
+      if (ok && j > 0) mma_commit(bb.acc_full);
+      mma_commit(bb.done);
+    }
+    __syncwarp();
+    drain_wait(bb.done, 0, budget);
+  } else if (warp >= 4) {
+    // ---------------------------------------------------------- elementwise
+    const int r = (warp - 4) * 32 + lane;       // key row of the tile
+    const bool krow_ok = r < kvalid;
+    const int kpos = sg.pos0 + sg.step * (128 * kt + r);
+    const uint32_t lane_off = uint32_t((warp - 4) * 32) << 16;
+    const uint32_t tS = tmem + lane_off, tP = tmem + 128 + lane_off;
+    const uint32_t tdV = tmem + 256 + lane_off, tdK = tmem + 384 + lane_off;
+    const float c2 = p.scale_log2;
+    const uint64_t c2x2 = f2(c2, c2);
+    QWalk w{0, g * p.n_qtiles, p.n_qtiles, hkv * g};
+    int h, qt, j = 0;
+    bool ok = true;
+    while (ok && w.next(p, kmin, h, qt)) {
+      const int st = j & 1;
+      ok = warp_wait(bb.st_full0 + 8 * st, (j >> 1) & 1, bb.abort_flag, budget, kSiteBwdStage) &&
+           warp_wait(bb.sdp_full, j & 1, bb.abort_flag, budget, kSiteBwdSdp);
+      if (!ok) break;
+      tc_fence_after();
+      const float* aux = reinterpret_cast<const float*>(gbase + C::kAux0 + st * C::kAuxBytes);
+      const int* apos = reinterpret_cast<const int*>(aux) + 256;
+      // a mask is needed only where some key of the tile lies after some
+      // query of the query tile, or where the key tile is ragged
+      const bool masked = (p.causal && kmax > p.qtile_pos[qt].x) || kvalid < 128;
+#pragma unroll 1
+      for (int i = 0; i < 4; ++i) {
+        uint32_t s[32], dp[32];
+        tmem_ld32(tS + 32 * i, s);
+        tmem_ld32(tP + 32 * i, dp);
+        tmem_ld_wait();
+        reg_fence(s);
+        reg_fence(dp);
+        uint32_t pp[16], pd[16];
+#pragma unroll
+        for (int c = 0; c < 32; c += 4) {
+          const float4 lse = *reinterpret_cast<const float4*>(aux + 32 * i + c);
+          const float4 del = *reinterpret_cast<const float4*>(aux + 128 + 32 * i + c);
+          const uint64_t x01 = fma2(f2(__uint_as_float(s[c]), __uint_as_float(s[c + 1])), c2x2,
+                                    f2(-lse.x, -lse.y));
+          const uint64_t x23 = fma2(f2(__uint_as_float(s[c + 2]), __uint_as_float(s[c + 3])), c2x2,
+                                    f2(-lse.z, -lse.w));
+          float x0, x1, x2, x3;
+          f2_split(x01, x0, x1);
+          f2_split(x23, x2, x3);
+          float p0 = ex2(x0), p1 = ex2(x1), p2 = ex2(x2), p3 = ex2(x3);
+          if (masked) {
+            const int4 qp4 = *reinterpret_cast<const int4*>(apos + 32 * i + c);
+            const bool vis_any = krow_ok;
+            if (!vis_any || (p.causal && kpos > qp4.x)) p0 = 0.f;
+            if (!vis_any || (p.causal && kpos > qp4.y)) p1 = 0.f;
+            if (!vis_any || (p.causal && kpos > qp4.z)) p2 = 0.f;
+            if (!vis_any || (p.causal && kpos > qp4.w)) p3 = 0.f;
+          }
+          const uint64_t t01 = add2(f2(__uint_as_float(dp[c]), __uint_as_float(dp[c + 1])), f2(-del.x, -del.y));
+          const uint64_t t23 = add2(f2(__uint_as_float(dp[c + 2]), __uint_as_float(dp[c + 3])), f2(-del.z, -del.w));
+          float d0, d1, d2, d3;
+          f2_split(mul2(f2(p0, p1), t01), d0, d1);
+          f2_split(mul2(f2(p2, p3), t23), d2, d3);
+          pp[c / 2] = pack_bf16x2(p0, p1);
+          pp[c / 2 + 1] = pack_bf16x2(p2, p3);
+          pd[c / 2] = pack_bf16x2(d0, d1);
+          pd[c / 2 + 1] = pack_bf16x2(d2, d3);
+        }
+        // P^T over S^T's columns, dS^T over dP^T's, both already read
+        tmem_st16(tS + 16 * i, pp);
+        tmem_st16(tP + 16 * i, pd);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bb.ew_done);
+      ++j;
+    }
+    if (ok) {
+      // ---- epilogue: dK (times scale) and dV rows of this key tile
+      const bool any = j > 0;
+      if (any) {
+        ok = warp_wait(bb.acc_full, 0, bb.abort_flag, budget, kSiteBwdAcc);
+        tc_fence_after();
+      }
+      if (ok) {
+        const int64_t row = (int64_t(b) * p.Hkv + hkv) * p.chunk_len[sg.chunk] + krow0 + r;
+        float* dkr = p.dk[sg.chunk] + row * D;
+        float* dvr = p.dv[sg.chunk] + row * D;
+#pragma unroll 1
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t a[32], v[32];
+          if (any) {
+            tmem_ld32(tdK + 32 * cc, a);
+            tmem_ld32(tdV + 32 * cc, v);
+            tmem_ld_wait();
+            reg_fence(a);
+            reg_fence(v);
+          } else {
+#pragma unroll
+            for (int c = 0; c < 32; ++c) a[c] = v[c] = 0u;
+          }
+          if (krow_ok) {
+#pragma unroll
+            for (int c = 0; c < 32; c += 4) {
+              reinterpret_cast<float4*>(dkr + 32 * cc)[c / 4] =
+                  make_float4(__uint_as_float(a[c]) * p.scale, __uint_as_float(a[c + 1]) * p.scale,
+                              __uint_as_float(a[c + 2]) * p.scale, __uint_as_float(a[c + 3]) * p.scale);
+              reinterpret_cast<float4*>(dvr + 32 * cc)[c / 4] =
+                  make_float4(__uint_as_float(v[c]), __uint_as_float(v[c + 1]),
+                              __uint_as_float(v[c + 2]), __uint_as_float(v[c + 3]));
+            }
+          }
+        }
+      }
+    }
+  }
+  bwd_teardown(tmem);
+}
+
+// ------------------------------------------------------------ dQ
+template <int D>
+__global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_constant__ BwdPlan p) {
+  using C = BwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint32_t base;
+  uint8_t* gbase;
+  BwdBars bb;
+  bwd_setup<D>(smem_raw, base, gbase, bb);
+  const uint32_t tmem = *bb.tmem_slot;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const unsigned long long budget = p.timeout_ns;
+
+  // this CTA's query tile; with a causal mask the later tiles (more keys)
+  // are started first
+  int u = blockIdx.x;
+  int qt = u % p.n_qtiles;
+  if (p.causal) qt = p.n_qtiles - 1 - qt;
+  u /= p.n_qtiles;
+  const int hq = u % p.Hq, b = u / p.Hq;
+  const int hkv = hq / (p.Hq / p.Hkv);
+  const int qmax = p.qtile_pos[qt].y;
+  const uint32_t sQ = base + C::kRes0, sDO = base + C::kRes1;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------- producer
+    const bool leader = elect_one();
+    if (leader) {
+      mbar_arrive_expect_tx(bb.res_full, 2 * C::kTileBytes);
+#pragma unroll
+      for (int bx = 0; bx < C::kBoxes; ++bx) {
+        tma_load_4d(sQ + bx * C::kBoxBytes, &p.qmap, bb.res_full, bx * 64, 128 * qt, hq, b);
+        tma_load_4d(sDO + bx * C::kBoxBytes, &p.domap, bb.res_full, bx * 64, 128 * qt, hq, b);
+      }
+    }
+    int j = 0;
+    bool ok = true;
+    for (int k = 0; ok && k < p.n_kvsegs; ++k) {
+      const KvSeg& sg = p.ks[k];
+      const int nl = bwd_live_tiles(p, k, qmax);
+      for (int t = 0; t < nl; ++t) {
+        const int st = j & 1;
+        ok = warp_wait(bb.st_empty0 + 8 * st, ((j >> 1) & 1) ^ 1, bb.abort_flag, budget, kSiteBwdEmpty);
+        if (!ok) break;
+        const uint32_t sK = base + C::kStage0 + st * C::kStageBytes, sV = sK + C::kTileBytes;
+        if (leader) {
+          mbar_arrive_expect_tx(bb.st_full0 + 8 * st, 2 * C::kTileBytes);
+#pragma unroll
+          for (int bx = 0; bx < C::kBoxes; ++bx) {
+            tma_load_4d(sK + bx * C::kBoxBytes, &p.kmap[sg.chunk], bb.st_full0 + 8 * st, bx * 64,
+                        sg.row0 + 128 * t, hkv, b);
+            tma_load_4d(sV + bx * C::kBoxBytes, &p.vmap[sg.chunk], bb.st_full0 + 8 * st, bx * 64,
+                        sg.row0 + 128 * t, hkv, b);
+          }
+        }
+        mbar_arrive(bb.st_full0 + 8 * st);
+        ++j;
+      }
+    }
+    if (!ok) {
+      drain_wait(bb.res_full, 0, budget);
+      for (int s = 0; s < 2; ++s) {
+        const int last = (j - 1 - s) >= 0 ? ((j - 1 - s) & ~1) + s : -1;
+        if (last >= 0 && last < j) drain_wait(bb.st_full0 + 8 * s, (last >> 1) & 1, budget);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA warp
+    const bool leader = elect_one();
+    const uint32_t tS = tmem, tP = tmem + 128, tdQ = tmem + 256;
+    bool ok = warp_wait(bb.res_full, 0, bb.abort_flag, budget, kSiteBwdKv);
+    int j = 0;
+    for (int k = 0; ok && k < p.n_kvsegs; ++k) {
+      const int nl = bwd_live_tiles(p, k, qmax);
+      for (int t = 0; t < nl; ++t) {
+        const int st = j & 1;
+        const uint32_t sK = base + C::kStage0 + st * C::kStageBytes, sV = sK + C::kTileBytes;
+        ok = warp_wait(bb.st_full0 + 8 * st, (j >> 1) & 1, bb.abort_flag, budget, kSiteBwdStage);
+        if (!ok) break;
+        tc_fence_after();
+        if (leader) {
+          issue_abt<D>(tS, sQ, sK);   // S  = Q K^T
+          issue_abt<D>(tP, sDO, sV);  // dP = dO V^T
+          mma_commit(bb.sdp_full);
+        }
+        __syncwarp();
+        ok = warp_wait(bb.ew_done, j & 1, bb.abort_flag, budget, kSiteBwdDs);
+        if (!ok) break;
+        tc_fence_after();
+        if (leader) {
+          issue_tmem_a<D>(tdQ, tS, sK, j > 0);  // dQ += dS K
+          mma_commit(bb.st_empty0 + 8 * st);
+        }
+        __syncwarp();
+        ++j;
+      }
+    }
+    if (leader) {
+      if (ok && j > 0) mma_commit(bb.acc_full);
+      mma_commit(bb.done);
+    }
+    __syncwarp();
+    drain_wait(bb.done, 0, budget);
+  } else if (warp >= 4) {
+    // ---------------------------------------------------------- elementwise
+    const int r = (warp - 4) * 32 + lane;       // query row of the tile
+    const int grow = 128 * qt + r;
+    const bool rvalid = grow < p.Sq;
+    const int64_t srow = (int64_t(b) * p.Hq + hq) * p.Sq + grow;
+    const float lse = rvalid ? p.lse2[srow] : kInf;
+    const float del = rvalid ? p.delta[srow] : 0.f;
+    const int qpos = rvalid ? bwd_row_position(p, grow) : 0x7ffffffe;
+    const uint32_t lane_off = uint32_t((warp - 4) * 32) << 16;
+    const uint32_t tS = tmem + lane_off, tP = tmem + 128 + lane_off, tdQ = tmem + 256 + lane_off;
+    const uint64_t c2x2 = f2(p.scale_log2, p.scale_log2), nlse = f2(-lse, -lse), ndel = f2(-del, -del);
+    int j = 0;
+    bool ok = true;
+    for (int k = 0; ok && k < p.n_kvsegs; ++k) {
+      const KvSeg& sg = p.ks[k];
+      const int nl = bwd_live_tiles(p, k, qmax);
+      for (int t = 0; t < nl; ++t) {
+        // visible keys of this row: a prefix [0, L) of the key tile
+        int L = min(128, sg.len - 128 * t);
+        if (p.causal) {
+          const int first = sg.pos0 + sg.step * (128 * t);
+          L = qpos < first ? 0 : min(L, (qpos - first) / sg.step + 1);
+        }
+        ok = warp_wait(bb.sdp_full, j & 1, bb.abort_flag, budget, kSiteBwdSdp);
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll 1
+        for (int i = 0; i < 4; ++i) {
+          uint32_t s[32], dp[32];
+          tmem_ld32(tS + 32 * i, s);
+          tmem_ld32(tP + 32 * i, dp);
+          tmem_ld_wait();
+          reg_fence(s);
+          reg_fence(dp);
+          if (L < 128) {
+#pragma unroll
+            for (int c = 0; c < 32; ++c)
+              if (32 * i + c >= L) s[c] = 0xff800000u;  // -inf: p = 0
+          }
+          uint32_t pd[16];
+#pragma unroll
+          for (int c = 0; c < 32; c += 2) {
+            float x0, x1;
+            f2_split(fma2(f2(__uint_as_float(s[c]), __uint_as_float(s[c + 1])), c2x2, nlse), x0, x1);
+            const uint64_t pr = f2(ex2(x0), ex2(x1));
+            float d0, d1;
+            f2_split(mul2(pr, add2(f2(__uint_as_float(dp[c]), __uint_as_float(dp[c + 1])), ndel)), d0, d1);
+            pd[c / 2] = pack_bf16x2(d0, d1);
+          }
+          tmem_st16(tS + 16 * i, pd);  // dS over S's columns, already read
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(bb.ew_done);
+        ++j;
+      }
+    }
+    if (ok) {
+      // ---- epilogue: dQ row times scale
+      const bool any = j > 0;
+      if (any) {
+        ok = warp_wait(bb.acc_full, 0, bb.abort_flag, budget, kSiteBwdAcc);
+        tc_fence_after();
+      }
+      if (ok) {
+        // the TMEM loads are warp-collective: every lane takes part, rows
+        // past Sq just do not store
+        float* dqr = p.dq + srow * D;
+#pragma unroll 1
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t a[32];
+          if (any) {
+            tmem_ld32(tdQ + 32 * cc, a);
+            tmem_ld_wait();
+            reg_fence(a);
+          } else {
+#pragma unroll
+            for (int c = 0; c < 32; ++c) a[c] = 0u;
+          }
+          if (rvalid) {
+#pragma unroll
+            for (int c = 0; c < 32; c += 4)
+              reinterpret_cast<float4*>(dqr + 32 * cc)[c / 4] =
+                  make_float4(__uint_as_float(a[c]) * p.scale, __uint_as_float(a[c + 1]) * p.scale,
+                              __uint_as_float(a[c + 2]) * p.scale, __uint_as_float(a[c + 3]) * p.scale);
+          }
+        }
+      }
+    }
+  }
+  bwd_teardown(tmem);
+}
+
+template <int D>
+int launch_bwd_d(const BwdPlan& plan, const void* o, int o_fp32, int64_t o_sb, int64_t o_sh,
+                 int64_t o_sr, const void* dout, const float* m, const float* l, float* lse2,
+                 float* delta, int2* qtile_pos, void* stream) {
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  const int64_t rows = int64_t(plan.B) * plan.Hq * plan.Sq;
+  bwd_prep_kernel<<<unsigned((rows + 127) / 128), 128, 0, cs>>>(
+      o, o_fp32, o_sb, o_sh, o_sr, static_cast<const uint16_t*>(dout), m, l, plan.B, plan.Hq,
+      plan.Sq, D, lse2, delta);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  bwd_qtile_kernel<<<unsigned((plan.n_qtiles + 127) / 128), 128, 0, cs>>>(plan, qtile_pos);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  constexpr int kSmem = BwdCfg<D>::kSmemBytes;
+  if ((e = cudaFuncSetAttribute(bwd_dkv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                kSmem)) != cudaSuccess)
+    return e;
+  if ((e = cudaFuncSetAttribute(bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                kSmem)) != cudaSuccess)
+    return e;
+  const int64_t kv_ctas = int64_t(plan.n_ktiles) * plan.Hkv * plan.B;
+  const int64_t q_ctas = int64_t(plan.n_qtiles) * plan.Hq * plan.B;
+  if (kv_ctas > 0) {
+    bwd_dkv_kernel<D><<<unsigned(kv_ctas), kBwdThreads, kSmem, cs>>>(plan);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  if (q_ctas > 0) {
+    bwd_dq_kernel<D><<<unsigned(q_ctas), kBwdThreads, kSmem, cs>>>(plan);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+}  // namespace
+
+int launch_bwd_bf16(const BwdPlan& plan, int D, const void* o, int o_fp32, int64_t o_sb,
+                    int64_t o_sh, int64_t o_sr, const void* dout, const float* m,
+                    const float* l, float* lse2, float* delta, int2* qtile_pos, void* stream) {
+  return D == 128 ? launch_bwd_d<128>(plan, o, o_fp32, o_sb, o_sh, o_sr, dout, m, l, lse2, delta,
+                                      qtile_pos, stream)
+                  : launch_bwd_d<64>(plan, o, o_fp32, o_sb, o_sh, o_sr, dout, m, l, lse2, delta,
+                                     qtile_pos, stream);
+}
+
+int read_and_clear_bwd_error(int* code) {
+  int v = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_ra_device_error, sizeof(int));
+  if (e != cudaSuccess) return e;
+  *code = v;
+  if (v != 0) {
+    const int zero = 0;
+    e = cudaMemcpyToSymbol(g_ra_device_error, &zero, sizeof(int));
+  }
+  return e;
+}
+
+}  // namespace ra

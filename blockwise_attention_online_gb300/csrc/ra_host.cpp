@@ -547,6 +547,122 @@ ra_status run(const ra_problem* pb, const void* q, const ra_q_segment* segs, int
   return run_simt(c, *pb, q, chunks, out, m, l, stats_mode, stream, before_launch);
 }
 
+// ----------------------------------------------------------- backward
+ra_status run_bwd(const ra_problem* pb, const void* q, const ra_q_segment* segs, int32_t nsegs,
+                  const ra_kv_chunk* chunks, int32_t nchunks, const void* o, const void* dout,
+                  const float* m, const float* l, float* dq, const ra_kv_grad* grads,
+                  void* stream) {
+  Common c;
+  ra_status st = validate(pb, q, segs, nsegs, chunks, nchunks, &c);
+  if (st != RA_OK) return st;
+  const ra_problem& p = *pb;
+  if (c.dtype != RA_BF16)
+    return fail(RA_ERR_UNSUPPORTED, "the backward pass is implemented for bf16 inputs only");
+  if (nchunks > 0 && !grads) return fail(RA_ERR_INVALID, "grads is NULL");
+  for (int32_t k = 0; k < nchunks; ++k)
+    if (chunks[k].len > 0 && (!grads[k].dk || !grads[k].dv))
+      return fail(RA_ERR_INVALID, "chunk %d: NULL dk or dv", k);
+  if (c.nchunks > ra::kTcMaxChunks)
+    return fail(RA_ERR_UNSUPPORTED, "bf16 path handles at most %d chunks, got %d",
+                ra::kTcMaxChunks, c.nchunks);
+  if ((int)c.kvspans.size() > ra::kTcMaxKvSegs)
+    return fail(RA_ERR_UNSUPPORTED, "bf16 path handles at most %d chunk spans, got %zu",
+                ra::kTcMaxKvSegs, c.kvspans.size());
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  if (c.Sq > 0) {
+    if (!o || !dout || !m || !l || !dq) return fail(RA_ERR_INVALID, "o, dout, m, l or dq is NULL");
+    if (!aligned16(q) || !aligned16(o) || !aligned16(dout) || !aligned16(dq))
+      return fail(RA_ERR_INVALID, "q, o, dout and dq must be 16-byte aligned");
+    if ((st = check_bf16_strides(p.q_strides, c.Sq, c.Hq, c.B, "q_strides")) != RA_OK) return st;
+    // dO (bf16) shares O's element strides; they must suit both
+    if ((st = check_bf16_strides(p.o_strides, c.Sq, c.Hq, c.B, "o_strides (dout)")) != RA_OK)
+      return st;
+  }
+  for (int k = 0; k < c.nchunks; ++k) {
+    const ra_kv_chunk& ch = chunks[k];
+    if (ch.len == 0) continue;
+    if (!aligned16(ch.k) || !aligned16(ch.v) || !aligned16(grads[k].dk) || !aligned16(grads[k].dv))
+      return fail(RA_ERR_INVALID, "chunk %d: k, v, dk and dv must be 16-byte aligned", k);
+    if ((st = check_bf16_strides(ch.k_strides, ch.len, c.Hkv, c.B, "chunk k_strides")) != RA_OK) return st;
+    if ((st = check_bf16_strides(ch.v_strides, ch.len, c.Hkv, c.B, "chunk v_strides")) != RA_OK) return st;
+  }
+  if (c.Sq == 0) {
+    // no query: every key and value gradient is zero
+    for (int k = 0; k < c.nchunks; ++k) {
+      if (chunks[k].len == 0) continue;
+      const size_t bytes = size_t(c.B * c.Hkv * chunks[k].len) * size_t(c.D) * 4;
+      cudaError_t e = cudaMemsetAsync(grads[k].dk, 0, bytes, cs);
+      if (e == cudaSuccess) e = cudaMemsetAsync(grads[k].dv, 0, bytes, cs);
+      if (e != cudaSuccess) return cuda_status(e, "clearing dk, dv");
+    }
+    return ok();
+  }
+  if ((st = get_encoder()) != RA_OK) return st;
+
+  static thread_local ra::BwdPlan plan;
+  std::memset(&plan, 0, sizeof(plan));
+  if ((st = make_map(&plan.qmap, q, c.D, c.Sq, c.Hq, c.B, p.q_strides, "q")) != RA_OK) return st;
+  if ((st = make_map(&plan.domap, dout, c.D, c.Sq, c.Hq, c.B, p.o_strides, "dout")) != RA_OK)
+    return st;
+  for (int k = 0; k < c.nchunks; ++k) {
+    const ra_kv_chunk& ch = chunks[k];
+    plan.chunk_len[k] = int32_t(ch.len);
+    if (ch.len == 0) continue;
+    if ((st = make_map(&plan.kmap[k], ch.k, c.D, ch.len, c.Hkv, c.B, ch.k_strides, "k")) != RA_OK) return st;
+    if ((st = make_map(&plan.vmap[k], ch.v, c.D, ch.len, c.Hkv, c.B, ch.v_strides, "v")) != RA_OK) return st;
+    plan.dk[k] = grads[k].dk;
+    plan.dv[k] = grads[k].dv;
+  }
+  plan.dq = dq;
+  plan.timeout_ns = 2000000000ull;
+  if (const char* env = std::getenv("RA_WAIT_BUDGET_NS")) {
+    const unsigned long long v = std::strtoull(env, nullptr, 10);
+    if (v > 0) plan.timeout_ns = v;
+  }
+  plan.B = int32_t(c.B); plan.Hq = int32_t(c.Hq); plan.Hkv = int32_t(c.Hkv); plan.Sq = int32_t(c.Sq);
+  plan.causal = c.causal; plan.n_chunks = c.nchunks;
+  plan.scale = c.scale;
+  plan.scale_log2 = float(double(c.scale) * 1.4426950408889634);
+  fill_q_pieces(c, plan.qp, &plan.n_qpieces);
+  plan.n_kvsegs = int32_t(c.kvspans.size());
+  int32_t tiles = 0;
+  for (size_t i = 0; i < c.kvspans.size(); ++i) {
+    const Span& sp = c.kvspans[i];
+    plan.ks[i] = {sp.owner, int32_t(sp.row0), int32_t(sp.len), int32_t(sp.pos0), int32_t(sp.step),
+                  int32_t((sp.len + 127) / 128)};
+    plan.kseg_tile_begin[i] = tiles;
+    tiles += plan.ks[i].ntiles;
+  }
+  plan.kseg_tile_begin[c.kvspans.size()] = tiles;
+  plan.n_ktiles = tiles;
+  plan.n_qtiles = int32_t((c.Sq + 127) / 128);
+  if (int64_t(plan.n_ktiles) * c.Hkv * c.B > (int64_t(1) << 31) - 1 ||
+      int64_t(plan.n_qtiles) * c.Hq * c.B > (int64_t(1) << 31) - 1)
+    return fail(RA_ERR_UNSUPPORTED, "too many tiles for one launch");
+
+  // per query row: lse2, delta; per query tile: position range
+  const size_t rows = size_t(c.B * c.Hq * c.Sq);
+  auto up = [](size_t n) { return (n + 255) & ~size_t(255); };
+  const size_t bytes = 2 * up(rows * 4) + up(size_t(plan.n_qtiles) * 8);
+  cudaMemPool_t pool = nullptr;
+  if ((st = lib_pool(&pool)) != RA_OK) return st;
+  char* scratch = nullptr;
+  cudaError_t e = cudaMallocFromPoolAsync(reinterpret_cast<void**>(&scratch), bytes, pool, cs);
+  if (e != cudaSuccess) return cuda_status(e, "allocating backward scratch");
+  float* lse2 = reinterpret_cast<float*>(scratch);
+  float* delta = reinterpret_cast<float*>(scratch + up(rows * 4));
+  int2* qtile_pos = reinterpret_cast<int2*>(scratch + 2 * up(rows * 4));
+  plan.lse2 = lse2;
+  plan.delta = delta;
+  plan.qtile_pos = qtile_pos;
+  const bool o_f32 = p.o_fp32 == 1;
+  const int err = ra::launch_bwd_bf16(plan, int(c.D), o, o_f32 ? 1 : 0, p.o_strides.batch,
+                                      p.o_strides.head, p.o_strides.row, dout, m, l, lse2, delta,
+                                      qtile_pos, stream);
+  cudaFreeAsync(scratch, cs);
+  return cuda_status(err, "backward kernel launch");
+}
+
 // Dense strides of a [B, H, rows, D] tensor; axes of extent 1 accept any stride.
 bool is_dense(const ra_strides& s, int64_t B, int64_t H, int64_t rows, int64_t D) {
   return (rows <= 1 || s.row == D) && (H <= 1 || s.head == rows * D) &&
@@ -663,6 +779,14 @@ ra_status ra_ring_attention_noalloc(const ra_problem* problem, const void* q,
              ScratchSource::kStatic);
 }
 
+ra_status ra_ring_attention_bwd(const ra_problem* problem, const void* q,
+                                const ra_q_segment* segs, int32_t nsegs,
+                                const ra_kv_chunk* chunks, int32_t nchunks, const void* o,
+                                const void* dout, const float* m, const float* l, float* dq,
+                                const ra_kv_grad* grads, void* stream) {
+  return run_bwd(problem, q, segs, nsegs, chunks, nchunks, o, dout, m, l, dq, grads, stream);
+}
+
 ra_status ra_ring_attention_host(const ra_problem* problem, const void* q,
                                  const ra_q_segment* segs, int32_t nsegs,
                                  const ra_kv_chunk* chunks, int32_t nchunks, void* o,
@@ -742,9 +866,11 @@ ra_status ra_segment_work(const ra_problem* problem, const ra_q_segment* segs, i
 ra_status ra_device_status(void* stream) {
   cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(RA_ERR_CUDA, "stream: %s", cudaGetErrorString(e));
-  int code = 0;
+  int code = 0, code_bwd = 0;
   int err = ra::read_and_clear_device_error(&code);
+  if (err == cudaSuccess) err = ra::read_and_clear_bwd_error(&code_bwd);
   if (err != cudaSuccess) return cuda_status(err, "reading the device status word");
+  if (code == 0) code = code_bwd;
   if (code != 0)
     return fail(RA_ERR_TIMEOUT, "a kernel gave up waiting (code %d): its outputs are invalid",
                 code);

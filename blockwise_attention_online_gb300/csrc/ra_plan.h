@@ -71,6 +71,36 @@ struct alignas(128) TcPlan {
 };
 static_assert(sizeof(TcPlan) <= 32000, "bf16 plan must fit the parameter space");
 
+// ------------------------------------------------------- bf16 backward pass
+// Gradients of the ring pass (dQ, and dK, dV of every chunk) in fp32. The
+// row statistics of the forward are turned into lse2 = m log2(e) + log2(l)
+// (so that P = exp2(s * scale * log2(e) - lse2)) and delta = sum_d dO * O by a
+// preparation kernel; two tcgen05 kernels then recompute the probability
+// tiles: one per key tile (dK, dV; every query row that sees the tile) and
+// one per query tile (dQ; every key tile the rows see).
+struct alignas(128) BwdPlan {
+  CUtensorMap qmap;                  // Q  [B, Hq, Sq, D] bf16, box 64 x 128
+  CUtensorMap domap;                 // dO [B, Hq, Sq, D] bf16
+  CUtensorMap kmap[kTcMaxChunks];    // K chunk c [B, Hkv, len, D]
+  CUtensorMap vmap[kTcMaxChunks];    // V chunk c
+  const float* lse2;                 // [B, Hq, Sq]; +inf where the row sees no key
+  const float* delta;                // [B, Hq, Sq]
+  const int2* qtile_pos;             // [n_qtiles]: lowest, highest position of its rows
+  float* dq;                         // [B, Hq, Sq, D] fp32, dense
+  float* dk[kTcMaxChunks];           // [B, Hkv, len_c, D] fp32, dense
+  float* dv[kTcMaxChunks];
+  unsigned long long timeout_ns;
+  int32_t B, Hq, Hkv, Sq;
+  int32_t causal, n_chunks, n_qtiles, n_ktiles;
+  float scale, scale_log2;
+  int32_t n_qpieces, n_kvsegs;
+  int32_t chunk_len[kTcMaxChunks];            // rows of chunk c (dk, dv row count)
+  int32_t kseg_tile_begin[kTcMaxKvSegs + 1];  // first global key tile of span i
+  QPiece qp[kMaxQPieces];
+  KvSeg ks[kTcMaxKvSegs];
+};
+static_assert(sizeof(BwdPlan) <= 32000, "backward plan must fit the parameter space");
+
 // ---------------------------------------------------------------- fp32 path
 constexpr int kSimtMaxChunks = 256;
 constexpr int kSimtMaxKvSegs = 320;
@@ -110,5 +140,11 @@ int launch_merge_f32(int64_t rows, int64_t D, float* u_acc, float* l_acc,
                      float* m_acc, const float* u_new, const float* l_new,
                      const float* m_new, int num_sms, void* stream);
 int read_and_clear_device_error(int* code);
+// Backward: the preparation kernels (lse2, delta, query-tile position ranges),
+// then the dK/dV and dQ kernels; all on `stream`.
+int launch_bwd_bf16(const BwdPlan& plan, int D, const void* o, int o_fp32, int64_t o_sb,
+                    int64_t o_sh, int64_t o_sr, const void* dout, const float* m,
+                    const float* l, float* lse2, float* delta, int2* qtile_pos, void* stream);
+int read_and_clear_bwd_error(int* code);
 
 }  // namespace ra

@@ -257,6 +257,12 @@ __device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
   return d;
 }
 
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
 // acc + (low bf16 of w) and acc2 + (high bf16 of w), exactly, in fp32.
 __device__ __forceinline__ void add_bf16x2_halves(float& acc_lo, float& acc_hi, uint32_t w) {
   asm("{\n\t.reg .b16 lo, hi;\n\t"

@@ -45,10 +45,9 @@
 #include "ra.h"
 #include "ra_plan.h"
 #include "ra_ptx.cuh"
+#include "ra_wait.cuh"
 
 namespace ra {
-
-__device__ int g_ra_device_error = 0;
 
 // Scratch of ra_ring_attention_noalloc: one fixed array per device, part of
 // the library's device image (zero at load, kept until the process exits).
@@ -86,7 +85,7 @@ struct Cfg {
 // Wait sites, reported in the status word as 0x100 | site.
 enum : int {
   kSiteProdQ = 1, kSiteProdKv = 2, kSiteMmaQ = 3, kSiteMmaKv = 4, kSiteMmaP = 5,
-  kSiteMmaO = 6, kSiteSoftS = 7, kSiteSoftO = 8, kSiteDrain = 9, kSiteTest = 10,
+  kSiteMmaO = 6, kSiteSoftS = 7, kSiteSoftO = 8, kSiteTest = 10,
   kSitePartial = 11
 };
 
@@ -241,50 +240,6 @@ struct Walker {
     return true;
   }
 };
-
-__device__ __forceinline__ void record_error(int code) { atomicCAS(&g_ra_device_error, 0, code); }
-
-// Bounded wait on an mbarrier phase. Returns false (and stops the CTA) when the
-// budget runs out or another warp already gave up. Each try may sleep up to
-// 1 ms until the phase completes, so a waiting warp does not take issue slots
-// from the warps that share its scheduler; the clock is read only after an
-// unsuccessful try.
-__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                         unsigned long long budget, int site) {
-  if (mbar_try_wait_sleep(bar, parity, 1000000u)) return true;
-  const unsigned long long t0 = globaltimer();
-  while (true) {
-    if (mbar_try_wait_sleep(bar, parity, 1000000u)) return true;
-    if (*abort_flag) return false;
-    if (globaltimer() - t0 > budget) {
-      *abort_flag = 1;
-      record_error(0x100 | site);
-      return false;
-    }
-  }
-}
-
-// Warp-uniform version: every lane waits, the warp agrees on the outcome.
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                          unsigned long long budget, int site) {
-  const bool ok = wait_bar(bar, parity, abort_flag, budget, site);
-  return __all_sync(0xffffffffu, ok);
-}
-
-// Wait used while tearing down after an abort: ignores the abort flag and
-// has its own generous budget (copies and MMAs already issued always finish;
-// the CTA must not exit before they do, whatever the normal wait budget is).
-constexpr unsigned long long kDrainBudgetNs = 2000000000ull;
-
-__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, unsigned long long) {
-  const unsigned long long t0 = globaltimer();
-  while (!mbar_try_wait(bar, parity)) {
-    if (globaltimer() - t0 > kDrainBudgetNs) {
-      record_error(0x100 | kSiteDrain);
-      return;
-    }
-  }
-}
 
 // One warp writes NC 16-byte chunks of each of its 32 output rows (a row piece
 // of NC * 16 bytes) through its shared-memory staging area. Each lane deposits

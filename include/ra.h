@@ -181,6 +181,43 @@ ra_status ra_ring_attention(const ra_problem* problem, const void* q,
                             const ra_kv_chunk* chunks, int32_t nchunks,
                             void* o, float* m, float* l, void* stream);
 
+/* Gradient outputs of one key/value chunk (ra_ring_attention_bwd): fp32,
+ * dense [B, Hkv, len, D], caller-owned device memory. */
+typedef struct {
+  float* dk;
+  float* dv;
+} ra_kv_grad;
+
+/*
+ * ra_ring_attention_bwd - gradients of ra_ring_attention's O with respect to
+ * Q and to the K and V of every chunk, given dO ([BLOG] "Backward must
+ * aggregate shared dependencies": a query row's gradient reaches every chunk
+ * it attended to; each chunk's dK, dV sum the contributions of all query rows
+ * for the chunk's owner; probability tiles are recomputed with the forward's
+ * scale and masks):
+ *
+ *   P = softmax of the visible scaled scores (fixed by the forward's m, l)
+ *   dV = P^T dO;  dS = P * (dO V^T - rowsum(dO * O));  dQ = scale dS K;
+ *   dK = scale dS^T Q;  with grouped heads, K/V head g sums over its query heads.
+ *
+ * problem, q, segs, chunks: exactly as given to ra_ring_attention (same
+ * positions, mask, scale). o, m, l: that call's outputs (o bf16, or fp32 when
+ * problem->o_fp32, with problem->o_strides). dout: bf16 [B, Hq, Sq, D] with
+ * problem->o_strides (multiples of 8 elements). Outputs, fp32 and dense: dq
+ * [B, Hq, Sq, D]; grads[k].dk, grads[k].dv [B, Hkv, len_k, D] for every chunk
+ * with len_k > 0 (all zero when no query sees the chunk). The call takes a
+ * small scratch (two floats per query row, 8 bytes per 128-row query tile)
+ * from the library's memory pool on `stream` and frees it again.
+ * bf16 inputs only (RA_ERR_UNSUPPORTED for RA_F32); head_dim 64 or 128; the
+ * chunk and span limits of ra_ring_attention's bf16 path.
+ */
+ra_status ra_ring_attention_bwd(const ra_problem* problem, const void* q,
+                                const ra_q_segment* segs, int32_t nsegs,
+                                const ra_kv_chunk* chunks, int32_t nchunks,
+                                const void* o, const void* dout, const float* m,
+                                const float* l, float* dq, const ra_kv_grad* grads,
+                                void* stream);
+
 /*
  * ra_ring_attention_noalloc - ra_ring_attention for callers that must not
  * allocate device memory. (The pages have no counterpart: this is a
