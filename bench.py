@@ -285,6 +285,119 @@ def run_gpu(args):
     return line
 
 
+def run_gpu_bwd(args):
+    """The backward pass of the same workload: one step = ra_ring_attention_bwd
+    (preparation, dK/dV and dQ kernels) on the forward's O, m, l and a seeded
+    dO. FLOPs count the standard five products of the backward (2.5 x the
+    forward's), causal-adjusted like the forward; the two-kernel design
+    executes seven (S and dP are recomputed once per kernel)."""
+    import torch
+    from blockwise_attention_online_gb300 import device_status, ring_attention, ring_attention_bwd
+
+    world, rank, local = _dist()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    w, qs, kc, vc, rs, segs = build_workload(args.workload, args.layout, dev)
+    flops = 2.5 * w.flops()
+    O, m, l = ring_attention(qs, kc, vc, chunk_spans=rs, q_segments=segs, causal=w.causal)
+    g = torch.Generator(device=dev).manual_seed(99)
+    dout = torch.randn(qs.shape, device=dev, generator=g).to(torch.bfloat16)
+    dq = torch.empty(qs.shape, device=dev, dtype=torch.float32)
+    dk = [torch.empty(k.shape, device=dev, dtype=torch.float32) for k in kc]
+    dv = [torch.empty(v.shape, device=dev, dtype=torch.float32) for v in vc]
+    flush = torch.empty(L2_FLUSH_BYTES // 4, device=dev, dtype=torch.float32)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        ring_attention_bwd(qs, kc, vc, O, dout, m, l, chunk_spans=rs, q_segments=segs,
+                           causal=w.causal, dq=dq, dk=dk, dv=dv)
+
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        step()
+    torch.cuda.synchronize()
+    device_status()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index) as clk:
+        for i in range(args.steps):
+            flush.fill_(float(i & 7))
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    device_status()
+    total_ms = sum(s_.elapsed_time(e_) for s_, e_ in zip(starts, ends))
+    max_ms = max_over_ranks(total_ms, dev)
+    value = whole_job_tflops(flops, args.steps, world, max_ms)
+    if world > 1:
+        dist.destroy_process_group()
+    if rank != 0:
+        return None
+    peak_b, _, _, src = _peaks()
+    achieved = flops / (total_ms / args.steps * 1e-3) / 1e12
+    line = {
+        "metric": "ring_attention bwd TFLOP/s (bf16, causal-adjusted, 2.5x the forward's FLOPs)",
+        "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(max_ms / args.steps, 6),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic: seeded N(0,1) Q/K/V and dO (bf16), no dataset",
+        "config": {"workload": w.name, "pass": "backward", "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv,
+                   "S": w.S, "D": w.D, "causal": w.causal, "chunks": w.n_chunks,
+                   "layout": w.layout, "flops_per_step": flops,
+                   "l2": f"flushed before every step ({L2_FLUSH_BYTES >> 20} MiB write)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "pct_of_peak": round(100 * value / world / peak_b, 2),
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 3), "peak": peak_b,
+                     "unit": "TFLOP/s", "frac": round(achieved / peak_b, 4), "traffic": None,
+                     "kernel": "bwd_dkv_kernel<128> + bwd_dq_kernel<128> (one step)",
+                     "peak_source": f"{src} bf16 burst (MEASURED_PEAKS.json)"},
+        "clocks": clk.summary(),
+        "gpu_launches": 4 * args.steps,
+        "e2e": None,
+    }
+    if not args.no_cpu_baseline and world == 1:
+        line["cpu_baseline"] = cpu_baseline_bwd(w, args.cpu_seconds)
+    return line
+
+
+def cpu_baseline_bwd(w, seconds):
+    """The backward oracle timed on a bounded sample: the first query rows of
+    head 0 against all keys (their dQ exactly, their share of dK and dV)."""
+    import numpy as np
+    import oracle
+    from blockwise_attention_online_gb300 import workloads
+    q, k, v = workloads.make_qkv(w, device="cpu")
+    rng = np.random.default_rng(7)
+    rows = 64
+    done_flops, t0, n = 0.0, time.perf_counter(), 0
+    g = w.Hq // w.Hkv
+    while time.perf_counter() - t0 < seconds:
+        r0 = int(rng.integers(0, max(1, w.S - rows)))
+        qs = q[:, :1, r0:r0 + rows].double().numpy()
+        ks = k[:, :1].double().numpy()
+        vs = v[:, :1].double().numpy()
+        do = rng.standard_normal(qs.shape)
+        pos_q, pos_k = np.arange(r0, r0 + rows), np.arange(w.S)
+        oracle.attention_backward(qs, ks, vs, do, pos_q, pos_k, w.causal, w.D ** -0.5)
+        keys = np.minimum(pos_q + 1, w.S).sum() if w.causal else rows * w.S
+        done_flops += 10.0 * keys * w.D
+        n += 1
+    el = time.perf_counter() - t0
+    return {"value": round(done_flops / el / 1e12, 6), "unit": "TFLOP/s", "cores": os.cpu_count(),
+            "kind": "oracle", "sample": f"{n} blocks of {rows} query rows of head 0 against all "
+                                        f"keys (group {g}), {el:.1f} s"}
+
+
 def _oracle_sample(w, rows_per_head, seed=1234):
     import numpy as np
     from blockwise_attention_online_gb300 import workloads
@@ -371,11 +484,15 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--pass", dest="which", default="fwd", choices=["fwd", "bwd"],
+                    help="time the forward (default) or the backward pass")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     if args.impl == "reference":
         line = run_reference(args)
+    elif args.which == "bwd":
+        line = run_gpu_bwd(args)
     else:
         line = run_gpu(args)
     if line is not None:
