@@ -23,10 +23,12 @@
 //   bwd_dq_kernel<D>   one CTA per (batch, query head, 128-row query tile):
 //                      walks every live key tile and accumulates dQ in TMEM
 //
-// Warp roles of both tcgen05 kernels (256 threads): warp 0 TMA producer,
+// Warp roles of both tcgen05 kernels (384 threads): warp 0 TMA producer,
 // warp 1 MMA warp (waits warp-uniformly, one elected lane issues), warps 2-3
-// idle, warps 4-7 one TMEM lane (= tile row) per thread for the elementwise
-// work. Every mbarrier wait is bounded (see ra_wait.cuh).
+// idle, warps 4-11 the elementwise work: one TMEM lane (= tile row) per
+// thread, warpgroup h on columns [64h, 64h + 64) of every 128-column tile (no
+// step of the backward reduces across columns, so the halves never meet).
+// Every mbarrier wait is bounded (see ra_wait.cuh).
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -40,7 +42,7 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kBwdThreads = 256;
+constexpr int kBwdThreads = 384;
 constexpr float kInf = __builtin_huge_valf();
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -175,7 +177,7 @@ __device__ __forceinline__ void bwd_setup(uint8_t* smem_raw, uint32_t& base, uin
       mbar_init(bb.st_empty0 + 8 * s, 1);
     }
     mbar_init(bb.sdp_full, 1);
-    mbar_init(bb.ew_done, 128);
+    mbar_init(bb.ew_done, 256);
     mbar_init(bb.acc_full, 1);
     mbar_init(bb.done, 1);
     *bb.abort_flag = 0;
@@ -211,8 +213,10 @@ __device__ __forceinline__ void issue_abt(uint32_t d_tmem, uint32_t sa, uint32_t
   }
 }
 
-// D[tmem] (+)= A[tmem] B with A 128 x 128 bf16 in TMEM (64 columns) and B a
-// [128 rows (the contraction), D] tile in shared memory (MN-major).
+// D[tmem] (+)= A[tmem] B with A 128 x 128 bf16 in TMEM and B a [128 rows (the
+// contraction), D] tile in shared memory (MN-major). Contraction index
+// 64h + x of A sits in column a_tmem + 64h + x/2: each elementwise warpgroup
+// h writes its half inside the columns it read.
 template <int D>
 __device__ __forceinline__ void issue_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint32_t sb,
                                              bool acc) {
@@ -221,7 +225,7 @@ __device__ __forceinline__ void issue_tmem_a(uint32_t d_tmem, uint32_t a_tmem, u
   const uint64_t bd = sdesc_sw128(sb, C::kBoxBytes, 1024);
 #pragma unroll
   for (int kk = 0; kk < 128 / 16; ++kk)
-    mma_ts(d_tmem, a_tmem + kk * 8, bd + uint64_t((kk * 16 * 128) >> 4), kId,
+    mma_ts(d_tmem, a_tmem + 64 * (kk >> 2) + 8 * (kk & 3), bd + uint64_t((kk * 16 * 128) >> 4), kId,
            (acc || kk > 0) ? 1u : 0u);
 }
 
@@ -296,14 +300,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkv_kernel(const __grid_co
           tma_load_4d(sDO + bx * C::kBoxBytes, &p.domap, bb.st_full0 + 8 * st, bx * 64, 128 * qt, h, b);
         }
       }
-      // per-column data of this query tile: lse2, delta, position
+      // per-column data of this query tile: -lse2, -delta, position
       float* aux = reinterpret_cast<float*>(gbase + C::kAux0 + st * C::kAuxBytes);
       const int64_t rowbase = (int64_t(b) * p.Hq + h) * p.Sq;
       for (int i = lane; i < 128; i += 32) {
         const int row = 128 * qt + i;
         const bool valid = row < p.Sq;
-        aux[i] = valid ? p.lse2[rowbase + row] : kInf;
-        aux[128 + i] = valid ? p.delta[rowbase + row] : 0.f;
+        aux[i] = valid ? -p.lse2[rowbase + row] : -kInf;
+        aux[128 + i] = valid ? -p.delta[rowbase + row] : 0.f;
         reinterpret_cast<int*>(aux)[256 + i] = valid ? bwd_row_position(p, row) : int(0x80000000);
       }
       mbar_arrive(bb.st_full0 + 8 * st);
@@ -355,10 +359,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkv_kernel(const __grid_co
     drain_wait(bb.done, 0, budget);
   } else if (warp >= 4) {
     // ---------------------------------------------------------- elementwise
-    const int r = (warp - 4) * 32 + lane;       // key row of the tile
+    const int hw = (warp - 4) >> 2;              // column half of this warpgroup
+    const int sub = warp & 3;
+    const int r = sub * 32 + lane;               // key row of the tile
     const bool krow_ok = r < kvalid;
     const int kpos = sg.pos0 + sg.step * (128 * kt + r);
-    const uint32_t lane_off = uint32_t((warp - 4) * 32) << 16;
+    const uint32_t lane_off = uint32_t(sub * 32) << 16;
     const uint32_t tS = tmem + lane_off, tP = tmem + 128 + lane_off;
     const uint32_t tdV = tmem + 256 + lane_off, tdK = tmem + 384 + lane_off;
     const float c2 = p.scale_log2;
@@ -378,7 +384,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkv_kernel(const __grid_co
       // query of the query tile, or where the key tile is ragged
       const bool masked = (p.causal && kmax > p.qtile_pos[qt].x) || kvalid < 128;
 #pragma unroll 1
-      for (int i = 0; i < 4; ++i) {
+      for (int i = 2 * hw; i < 2 * hw + 2; ++i) {
+        // the chunk's column data first (shared-memory broadcasts), so that
+        // their latency overlaps the TMEM loads' wait
+        float4 nl[8], nd[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          nl[k] = *reinterpret_cast<const float4*>(aux + 32 * i + 4 * k);
+          nd[k] = *reinterpret_cast<const float4*>(aux + 128 + 32 * i + 4 * k);
+        }
         uint32_t s[32], dp[32];
         tmem_ld32(tS + 32 * i, s);
         tmem_ld32(tP + 32 * i, dp);
@@ -388,26 +402,24 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkv_kernel(const __grid_co
         uint32_t pp[16], pd[16];
 #pragma unroll
         for (int c = 0; c < 32; c += 4) {
-          const float4 lse = *reinterpret_cast<const float4*>(aux + 32 * i + c);
-          const float4 del = *reinterpret_cast<const float4*>(aux + 128 + 32 * i + c);
+          const float4 lse = nl[c / 4], del = nd[c / 4];   // negated
           const uint64_t x01 = fma2(f2(__uint_as_float(s[c]), __uint_as_float(s[c + 1])), c2x2,
-                                    f2(-lse.x, -lse.y));
+                                    f2(lse.x, lse.y));
           const uint64_t x23 = fma2(f2(__uint_as_float(s[c + 2]), __uint_as_float(s[c + 3])), c2x2,
-                                    f2(-lse.z, -lse.w));
+                                    f2(lse.z, lse.w));
           float x0, x1, x2, x3;
           f2_split(x01, x0, x1);
           f2_split(x23, x2, x3);
           float p0 = ex2(x0), p1 = ex2(x1), p2 = ex2(x2), p3 = ex2(x3);
           if (masked) {
             const int4 qp4 = *reinterpret_cast<const int4*>(apos + 32 * i + c);
-            const bool vis_any = krow_ok;
-            if (!vis_any || (p.causal && kpos > qp4.x)) p0 = 0.f;
-            if (!vis_any || (p.causal && kpos > qp4.y)) p1 = 0.f;
-            if (!vis_any || (p.causal && kpos > qp4.z)) p2 = 0.f;
-            if (!vis_any || (p.causal && kpos > qp4.w)) p3 = 0.f;
+            if (!krow_ok || (p.causal && kpos > qp4.x)) p0 = 0.f;
+            if (!krow_ok || (p.causal && kpos > qp4.y)) p1 = 0.f;
+            if (!krow_ok || (p.causal && kpos > qp4.z)) p2 = 0.f;
+            if (!krow_ok || (p.causal && kpos > qp4.w)) p3 = 0.f;
           }
-          const uint64_t t01 = add2(f2(__uint_as_float(dp[c]), __uint_as_float(dp[c + 1])), f2(-del.x, -del.y));
-          const uint64_t t23 = add2(f2(__uint_as_float(dp[c + 2]), __uint_as_float(dp[c + 3])), f2(-del.z, -del.w));
+          const uint64_t t01 = add2(f2(__uint_as_float(dp[c]), __uint_as_float(dp[c + 1])), f2(del.x, del.y));
+          const uint64_t t23 = add2(f2(__uint_as_float(dp[c + 2]), __uint_as_float(dp[c + 3])), f2(del.z, del.w));
           float d0, d1, d2, d3;
           f2_split(mul2(f2(p0, p1), t01), d0, d1);
           f2_split(mul2(f2(p2, p3), t23), d2, d3);
@@ -416,9 +428,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkv_kernel(const __grid_co
           pd[c / 2] = pack_bf16x2(d0, d1);
           pd[c / 2 + 1] = pack_bf16x2(d2, d3);
         }
-        // P^T over S^T's columns, dS^T over dP^T's, both already read
-        tmem_st16(tS + 16 * i, pp);
-        tmem_st16(tP + 16 * i, pd);
+        // P^T over S^T's columns, dS^T over dP^T's: inside this half, already read
+        tmem_st16(tS + 64 * hw + 16 * (i - 2 * hw), pp);
+        tmem_st16(tP + 64 * hw + 16 * (i - 2 * hw), pd);
       }
       tmem_st_wait();
       tc_fence_before();
@@ -437,7 +449,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkv_kernel(const __grid_co
         float* dkr = p.dk[sg.chunk] + row * D;
         float* dvr = p.dv[sg.chunk] + row * D;
 #pragma unroll 1
-        for (int cc = 0; cc < D / 32; ++cc) {
+        for (int cc = hw * (D / 64); cc < (hw + 1) * (D / 64); ++cc) {
           uint32_t a[32], v[32];
           if (any) {
             tmem_ld32(tdK + 32 * cc, a);
@@ -572,14 +584,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
     drain_wait(bb.done, 0, budget);
   } else if (warp >= 4) {
     // ---------------------------------------------------------- elementwise
-    const int r = (warp - 4) * 32 + lane;       // query row of the tile
+    const int hw = (warp - 4) >> 2;              // column half of this warpgroup
+    const int sub = warp & 3;
+    const int r = sub * 32 + lane;               // query row of the tile
     const int grow = 128 * qt + r;
     const bool rvalid = grow < p.Sq;
     const int64_t srow = (int64_t(b) * p.Hq + hq) * p.Sq + grow;
     const float lse = rvalid ? p.lse2[srow] : kInf;
     const float del = rvalid ? p.delta[srow] : 0.f;
     const int qpos = rvalid ? bwd_row_position(p, grow) : 0x7ffffffe;
-    const uint32_t lane_off = uint32_t((warp - 4) * 32) << 16;
+    const uint32_t lane_off = uint32_t(sub * 32) << 16;
     const uint32_t tS = tmem + lane_off, tP = tmem + 128 + lane_off, tdQ = tmem + 256 + lane_off;
     const uint64_t c2x2 = f2(p.scale_log2, p.scale_log2), nlse = f2(-lse, -lse), ndel = f2(-del, -del);
     int j = 0;
@@ -597,30 +611,41 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
         ok = warp_wait(bb.sdp_full, j & 1, bb.abort_flag, budget, kSiteBwdSdp);
         if (!ok) break;
         tc_fence_after();
-#pragma unroll 1
-        for (int i = 0; i < 4; ++i) {
-          uint32_t s[32], dp[32];
-          tmem_ld32(tS + 32 * i, s);
-          tmem_ld32(tP + 32 * i, dp);
+        {
+          // this warpgroup's 64 key columns, one TMEM wait
+          const int hh = hw;
+          uint32_t s[2][32], dp[2][32];
+          tmem_ld32(tS + 64 * hh, s[0]);
+          tmem_ld32(tS + 64 * hh + 32, s[1]);
+          tmem_ld32(tP + 64 * hh, dp[0]);
+          tmem_ld32(tP + 64 * hh + 32, dp[1]);
           tmem_ld_wait();
-          reg_fence(s);
-          reg_fence(dp);
-          if (L < 128) {
+          reg_fence(s[0]);
+          reg_fence(s[1]);
+          reg_fence(dp[0]);
+          reg_fence(dp[1]);
 #pragma unroll
-            for (int c = 0; c < 32; ++c)
-              if (32 * i + c >= L) s[c] = 0xff800000u;  // -inf: p = 0
-          }
-          uint32_t pd[16];
+          for (int q = 0; q < 2; ++q) {
+            const int i = 2 * hh + q;
+            if (L < 128) {
 #pragma unroll
-          for (int c = 0; c < 32; c += 2) {
-            float x0, x1;
-            f2_split(fma2(f2(__uint_as_float(s[c]), __uint_as_float(s[c + 1])), c2x2, nlse), x0, x1);
-            const uint64_t pr = f2(ex2(x0), ex2(x1));
-            float d0, d1;
-            f2_split(mul2(pr, add2(f2(__uint_as_float(dp[c]), __uint_as_float(dp[c + 1])), ndel)), d0, d1);
-            pd[c / 2] = pack_bf16x2(d0, d1);
+              for (int c = 0; c < 32; ++c)
+                if (32 * i + c >= L) s[q][c] = 0xff800000u;  // -inf: p = 0
+            }
+            uint32_t pd[16];
+#pragma unroll
+            for (int c = 0; c < 32; c += 2) {
+              float x0, x1;
+              f2_split(fma2(f2(__uint_as_float(s[q][c]), __uint_as_float(s[q][c + 1])), c2x2, nlse),
+                       x0, x1);
+              const uint64_t pr = f2(ex2(x0), ex2(x1));
+              float d0, d1;
+              f2_split(mul2(pr, add2(f2(__uint_as_float(dp[q][c]), __uint_as_float(dp[q][c + 1])), ndel)),
+                       d0, d1);
+              pd[c / 2] = pack_bf16x2(d0, d1);
+            }
+            tmem_st16(tS + 64 * hh + 16 * q, pd);  // dS inside this half of S, already read
           }
-          tmem_st16(tS + 16 * i, pd);  // dS over S's columns, already read
         }
         tmem_st_wait();
         tc_fence_before();
@@ -640,7 +665,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
         // past Sq just do not store
         float* dqr = p.dq + srow * D;
 #pragma unroll 1
-        for (int cc = 0; cc < D / 32; ++cc) {
+        for (int cc = hw * (D / 64); cc < (hw + 1) * (D / 64); ++cc) {
           uint32_t a[32];
           if (any) {
             tmem_ld32(tdQ + 32 * cc, a);
