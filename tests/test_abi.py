@@ -180,3 +180,41 @@ def test_host_entry_rejects_before_touching_the_device():
     assert _call_host(p, _segs(GOOD_SEGS), 1, ch, 2) == _lib.RA_ERR_INVALID
     # an empty problem is a valid no-op
     assert _call_host(_problem(Sq=0), _segs([(0, [(0, 0, 1)])]), 1, _chunks(GOOD_CHUNKS), 2) == _lib.RA_OK
+
+
+def _call_bwd(p, segs, nsegs, chunks, nchunks, grads, q=4096, o=4096, dout=4096, m=4096, l=4096,
+              dq=4096):
+    lib = _lib.load()
+    return lib.ra_ring_attention_bwd(ctypes.byref(p), q, segs, nsegs, chunks, nchunks, o, dout,
+                                     m, l, dq, grads, None)
+
+
+def _grads(n, ptr=4096):
+    g = (_lib.KvGrad * n)()
+    for i in range(n):
+        g[i].dk = ptr
+        g[i].dv = ptr
+    return g
+
+
+def test_backward_entry_rejects_before_launch():
+    p = _problem()
+    segs, ch = _segs(GOOD_SEGS), _chunks(GOOD_CHUNKS)
+    # fp32 inputs: the backward is bf16 only
+    assert _call_bwd(_problem(dtype=_lib.RA_F32, D=64), segs, 1, _chunks(GOOD_CHUNKS, D=64), 2,
+                     _grads(2)) == _lib.RA_ERR_UNSUPPORTED
+    # gradient outputs missing
+    assert _call_bwd(p, segs, 1, ch, 2, None) == _lib.RA_ERR_INVALID
+    g = _grads(2)
+    g[1].dv = None
+    assert _call_bwd(p, segs, 1, ch, 2, g) == _lib.RA_ERR_INVALID
+    # dout, dq or the statistics missing or misaligned
+    assert _call_bwd(p, segs, 1, ch, 2, _grads(2), dout=None) == _lib.RA_ERR_INVALID
+    assert _call_bwd(p, segs, 1, ch, 2, _grads(2), dq=None) == _lib.RA_ERR_INVALID
+    assert _call_bwd(p, segs, 1, ch, 2, _grads(2), dout=4100) == _lib.RA_ERR_INVALID
+    assert _call_bwd(p, segs, 1, ch, 2, _grads(2, ptr=4104)) == _lib.RA_ERR_INVALID
+    # the forward's descriptor checks apply
+    assert _call_bwd(p, _segs([(200, [(200, 0, 1)])]), 1, ch, 2, _grads(2)) == _lib.RA_ERR_INVALID
+    many = [(1, [(1, i, 1)]) for i in range(33)]
+    assert _call_bwd(_problem(Sq=33), _segs([(33, [(33, 0, 1)])]), 1, _chunks(many), 33,
+                     _grads(33)) == _lib.RA_ERR_UNSUPPORTED
