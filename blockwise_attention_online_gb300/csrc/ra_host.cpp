@@ -110,8 +110,8 @@ ra_status validate(const ra_problem* pb, const void* q, const ra_q_segment* segs
   if (p.causal != 0 && p.causal != 1) return fail(RA_ERR_INVALID, "causal must be 0 or 1");
   if (p.o_fp32 != 0 && p.o_fp32 != 1) return fail(RA_ERR_INVALID, "o_fp32 must be 0 or 1");
   if (!std::isfinite(p.scale)) return fail(RA_ERR_INVALID, "scale is not finite");
-  if (p.dtype == RA_BF16 && p.D != 64 && p.D != 128)
-    return fail(RA_ERR_UNSUPPORTED, "bf16 path supports head_dim 64 or 128, got %lld",
+  if (p.dtype == RA_BF16 && p.D != 64 && p.D != 96 && p.D != 128)
+    return fail(RA_ERR_UNSUPPORTED, "bf16 path supports head_dim 64, 96 or 128, got %lld",
                 (long long)p.D);
   if (p.dtype == RA_F32 && p.D > 128)
     return fail(RA_ERR_UNSUPPORTED, "fp32 path supports head_dim <= 128, got %lld",
@@ -558,6 +558,9 @@ ra_status run_bwd(const ra_problem* pb, const void* q, const ra_q_segment* segs,
   const ra_problem& p = *pb;
   if (c.dtype != RA_BF16)
     return fail(RA_ERR_UNSUPPORTED, "the backward pass is implemented for bf16 inputs only");
+  if (c.D != 64 && c.D != 128)
+    return fail(RA_ERR_UNSUPPORTED, "the backward pass supports head_dim 64 or 128, got %lld",
+                (long long)c.D);
   if (nchunks > 0 && !grads) return fail(RA_ERR_INVALID, "grads is NULL");
   for (int32_t k = 0; k < nchunks; ++k)
     if (chunks[k].len > 0 && (!grads[k].dk || !grads[k].dv))

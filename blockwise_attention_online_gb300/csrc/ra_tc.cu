@@ -67,10 +67,10 @@ constexpr float kRescaleLog2 = 8.0f;
 
 template <int D>
 struct Cfg {
-  static constexpr int kTileBytes = 128 * D * 2;  // one 128-row bf16 tile
   static constexpr int kBoxBytes = 128 * 128;     // 128 rows x 64 bf16 (one swizzle atom wide)
-  static constexpr int kBoxes = D / 64;
-  static constexpr int kStages = (D == 128) ? 4 : 8;
+  static constexpr int kBoxes = (D + 63) / 64;    // D = 96: the second box is half zero fill
+  static constexpr int kTileBytes = kBoxes * kBoxBytes;  // one 128-row bf16 tile
+  static constexpr int kStages = (kBoxes == 2) ? 4 : 8;
   static constexpr int kQOff = 0;
   static constexpr int kKvOff = 2 * kTileBytes;
   static constexpr int kBarOff = kKvOff + kStages * kTileBytes;
@@ -673,7 +673,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ring_kernel(const __grid_const
         ++oc;
         tc_fence_after();
       }
-      constexpr int kHalf = D / 64;  // 32-column chunks per half of O
+      // O is read and written in kParts parts of kHalf 32-column chunks: two
+      // halves when D is a multiple of 64, else one 32-column chunk per part
+      constexpr int kParts = (D % 64 == 0) ? 2 : D / 32;
+      constexpr int kHalf = D / 32 / kParts;
       const size_t slot_row = (size_t(blockIdx.x) * 2 + wg) * 128 + r;
       // A scratch slot (one per CTA and warpgroup) holds raw O as [D/4][128]
       // float4: lane r touches element (k, r), so every warp access covers
@@ -683,14 +686,14 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ring_kernel(const __grid_const
         // ---- publish this part's raw partial results for the unit's head
         float4* const dst = reinterpret_cast<float4*>(p.scratch.o) + (size_t(blockIdx.x) * 2 + wg) * kSlotF4 + r;
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
+        for (int h = 0; h < kParts; ++h) {
           uint32_t o[kHalf][32];
 #pragma unroll
           for (int cc = 0; cc < kHalf; ++cc) tmem_ld32(tO + 32 * (h * kHalf + cc), o[cc]);
           tmem_ld_wait();
 #pragma unroll
           for (int cc = 0; cc < kHalf; ++cc) reg_fence(o[cc]);
-          if (h == 1) {
+          if (h == kParts - 1) {
             tc_fence_before();
             mbar_arrive(b_ofree);
           }
@@ -698,7 +701,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ring_kernel(const __grid_const
           for (int cc = 0; cc < kHalf; ++cc)
 #pragma unroll
             for (int c = 0; c < 32; c += 4)
-              dst[size_t(h * (D / 8) + (cc * 32 + c) / 4) * 128] =
+              dst[size_t((h * kHalf * 32 + cc * 32 + c) / 4) * 128] =
                   make_float4(__uint_as_float(o[cc][c]), __uint_as_float(o[cc][c + 1]),
                               __uint_as_float(o[cc][c + 2]), __uint_as_float(o[cc][c + 3]));
         }
@@ -782,7 +785,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ring_kernel(const __grid_const
       const int64_t wbase = int64_t(U.b) * p.o_sb + int64_t(U.hq) * p.o_sh + int64_t(wrow0) * p.o_sr;
       uint8_t* const stage = gbase + C::kStageOff + (warp - 4) * 4096;
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
+      for (int h = 0; h < kParts; ++h) {
         uint32_t o[kHalf][32];
         if (n > 0) {
 #pragma unroll
@@ -790,7 +793,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ring_kernel(const __grid_const
           tmem_ld_wait();
 #pragma unroll
           for (int cc = 0; cc < kHalf; ++cc) reg_fence(o[cc]);
-          if (h == 1) {
+          if (h == kParts - 1) {
             tc_fence_before();
             mbar_arrive(b_ofree);
           }
@@ -817,7 +820,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ring_kernel(const __grid_const
             for (int cc = 0; cc < kHalf; ++cc)
 #pragma unroll
               for (int c4 = 0; c4 < 32; c4 += 4) {
-                const float4 v = __ldcg(src + size_t(h * (D / 8) + (cc * 32 + c4) / 4) * 128);
+                const float4 v = __ldcg(src + size_t((h * kHalf * 32 + cc * 32 + c4) / 4) * 128);
                 o[cc][c4] = __float_as_uint(fmaf(bp, v.x, __uint_as_float(o[cc][c4])));
                 o[cc][c4 + 1] = __float_as_uint(fmaf(bp, v.y, __uint_as_float(o[cc][c4 + 1])));
                 o[cc][c4 + 2] = __float_as_uint(fmaf(bp, v.z, __uint_as_float(o[cc][c4 + 2])));
@@ -837,7 +840,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ring_kernel(const __grid_const
                                  __float_as_uint(__uint_as_float(o[cc][4 * k + 2]) * fo),
                                  __float_as_uint(__uint_as_float(o[cc][4 * k + 3]) * fo));
             warp_store_staged<8>(stage, ch, lane,
-                                 reinterpret_cast<char*>(static_cast<float*>(p.out) + wbase + h * (D / 2) + cc * 32),
+                                 reinterpret_cast<char*>(static_cast<float*>(p.out) + wbase + h * kHalf * 32 + cc * 32),
                                  p.o_sr * 4, wvalid);
           }
         } else {
@@ -852,7 +855,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ring_kernel(const __grid_const
             ch[k].w = pack_bf16x2(__uint_as_float(o[cc][c + 6]) * fo, __uint_as_float(o[cc][c + 7]) * fo);
           }
           warp_store_staged<NC>(stage, ch, lane,
-                                reinterpret_cast<char*>(static_cast<uint16_t*>(p.out) + wbase + h * (D / 2)),
+                                reinterpret_cast<char*>(static_cast<uint16_t*>(p.out) + wbase + h * kHalf * 32),
                                 p.o_sr * 2, wvalid);
         }
       }
@@ -908,7 +911,11 @@ static int launch_d(const TcPlan& plan, void* stream) {
 
 int launch_tc_bf16(const TcPlan& plan, int D, void* stream) {
   if (plan.grid <= 0) return cudaSuccess;
-  return D == 128 ? launch_d<128>(plan, stream) : launch_d<64>(plan, stream);
+  switch (D) {
+    case 128: return launch_d<128>(plan, stream);
+    case 96: return launch_d<96>(plan, stream);
+    default: return launch_d<64>(plan, stream);
+  }
 }
 
 int tc_static_scratch(void** ptr, size_t* bytes) {

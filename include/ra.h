@@ -35,7 +35,7 @@
  *   Positions are described per chunk / query segment by spans.
  * - A row that sees no key gets O = 0 (or u = 0), l = 0, m = -inf.
  * - dtype RA_BF16: Q, K, V and O are bfloat16; products are accumulated in
- *   fp32 on the tensor cores; head_dim must be 64 or 128.
+ *   fp32 on the tensor cores; head_dim must be 64, 96 or 128.
  *   dtype RA_F32: everything is fp32 on CUDA cores (no TF32); head_dim
  *   1..128.
  */

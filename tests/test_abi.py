@@ -78,7 +78,7 @@ GOOD_CHUNKS = [(128, [(128, 0, 1)]), (128, [(128, 128, 1)])]
 
 @pytest.mark.parametrize("bad", [
     dict(Hq=3, Hkv=2),                 # Hq not a multiple of Hkv
-    dict(D=96),                        # bf16 head_dim outside {64, 128}
+    dict(D=80),                        # bf16 head_dim outside {64, 96, 128}
     dict(dtype=7),
     dict(causal=2),
     dict(o_fp32=2),
@@ -200,6 +200,9 @@ def _grads(n, ptr=4096):
 def test_backward_entry_rejects_before_launch():
     p = _problem()
     segs, ch = _segs(GOOD_SEGS), _chunks(GOOD_CHUNKS)
+    # head_dim 96: forward only
+    assert _call_bwd(_problem(D=96), segs, 1, _chunks(GOOD_CHUNKS, D=96), 2,
+                     _grads(2)) == _lib.RA_ERR_UNSUPPORTED
     # fp32 inputs: the backward is bf16 only
     assert _call_bwd(_problem(dtype=_lib.RA_F32, D=64), segs, 1, _chunks(GOOD_CHUNKS, D=64), 2,
                      _grads(2)) == _lib.RA_ERR_UNSUPPORTED

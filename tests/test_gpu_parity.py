@@ -150,7 +150,7 @@ def _bf16_inputs(B, Hq, Hkv, S, D, seed, Sq=None):
     return q, k, v
 
 
-@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("D", [64, 96, 128])
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("S,lens", [(1, [1]), (128, [128]), (300, [1, 127, 129, 43]),
                                     (520, [520]), (700, [256, 200, 244])])
@@ -236,3 +236,41 @@ def test_bf16_cfg2_full_oracle():
     # bitwise repeatable
     O2, m2, l2 = layout_run(q.to(DEV), k.to(DEV), v.to(DEV), 8, "contiguous", False)
     assert torch.equal(O, O2) and torch.equal(m, m2) and torch.equal(l, l2)
+
+
+@pytest.mark.parametrize("kind", ["zigzag", "striped"])
+def test_bf16_head_dim_96_layouts(kind):
+    """head_dim 96 (a non-power-of-two width; the second 64-column box of every
+    tile is half zero fill): GQA 4:1 over 4 virtual ranks, causal."""
+    q, k, v = _bf16_inputs(1, 8, 2, 1024, 96, seed=19)
+    ref = _full_ref(q, k, v, True, 1 / math.sqrt(96))
+    O, m, l = layout_run(q.to(DEV), k.to(DEV), v.to(DEV), 4, kind, True)
+    device_status()
+    assert_bf16(O, m, l, *ref, what=f"D=96 {kind}")
+
+
+@pytest.mark.parametrize("out_dtype", [None, torch.float32])
+def test_bf16_head_dim_96_split_units(out_dtype):
+    """Enough units that the last rounds are split across CTAs (partial results
+    published and merged), head_dim 96, bf16 and fp32 O."""
+    q, k, v = _bf16_inputs(1, 4, 4, 2304, 96, seed=23)
+    ref = _full_ref(q, k, v, False, 1 / math.sqrt(96))
+    kc = _split(k.to(DEV), [1024, 1280])
+    vc = _split(v.to(DEV), [1024, 1280])
+    O, m, l = ring_attention(q.to(DEV), kc, vc, causal=False, out_dtype=out_dtype)
+    device_status()
+    assert_bf16(O, m, l, *ref, what="D=96 split")
+
+
+def test_bf16_head_dim_96_chunk_stats():
+    q, k, v = _bf16_inputs(1, 2, 1, 384, 96, seed=29)
+    pos = np.arange(384)
+    u, l, m = chunk_stats(q.to(DEV), k[:, :, 128:].contiguous().to(DEV),
+                          v[:, :, 128:].contiguous().to(DEV), spans=[(256, 128, 1)], causal=True)
+    device_status()
+    u_r, l_r, m_r = oracle.chunk_stats(f64(q), f64(k[:, :, 128:]), f64(v[:, :, 128:]), pos,
+                                       pos[128:], True, 1 / math.sqrt(96))
+    fin = np.isfinite(m_r)
+    assert np.array_equal(np.isfinite(f64(m)), fin)
+    assert (np.abs(f64(u) - u_r) <= 1e-2 * np.maximum(1.0, l_r)[..., None]).all()
+    assert (np.abs(f64(l) - l_r) <= 1e-3 * np.maximum(1.0, l_r)).all()
