@@ -22,7 +22,8 @@ STATUS_NAMES = {0: "RA_OK", 1: "RA_ERR_INVALID", 2: "RA_ERR_UNSUPPORTED",
 # every symbol include/ra.h declares
 EXPORTED = ("ra_chunk_stats", "ra_merge_stats", "ra_ring_attention",
             "ra_ring_attention_noalloc", "ra_ring_attention_host", "ra_ring_attention_bwd",
-            "ra_segment_work", "ra_device_status", "ra_last_error", "ra_version")
+            "ra_merge_lse", "ra_stats_to_lse", "ra_segment_work", "ra_device_status",
+            "ra_last_error", "ra_version")
 
 
 class Span(ctypes.Structure):
@@ -93,6 +94,9 @@ def load():
         lib.ra_ring_attention_bwd.argtypes = [P(Problem), c_void_p, P(QSegment), c_int32,
                                               P(KvChunk), c_int32, c_void_p, c_void_p, c_void_p,
                                               c_void_p, c_void_p, P(KvGrad), c_void_p]
+        lib.ra_merge_lse.argtypes = [c_int64, c_int64, c_void_p, c_void_p, c_void_p, c_void_p,
+                                     c_void_p]
+        lib.ra_stats_to_lse.argtypes = [c_int64, c_void_p, c_void_p, c_void_p, c_void_p]
         lib.ra_segment_work.argtypes = [P(Problem), P(QSegment), c_int32, P(KvChunk), c_int32,
                                         c_void_p, c_void_p]
         lib.ra_device_status.argtypes = [c_void_p]
@@ -102,7 +106,8 @@ def load():
         lib.ra_version.argtypes = []
         for name in ("ra_chunk_stats", "ra_merge_stats", "ra_ring_attention",
                      "ra_ring_attention_noalloc", "ra_ring_attention_host",
-                     "ra_ring_attention_bwd", "ra_segment_work", "ra_device_status"):
+                     "ra_ring_attention_bwd", "ra_merge_lse", "ra_stats_to_lse",
+                     "ra_segment_work", "ra_device_status"):
             getattr(lib, name).restype = c_int32
         _lib = lib
         return lib

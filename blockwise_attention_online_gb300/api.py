@@ -250,6 +250,35 @@ def merge_stats(u_acc, l_acc, m_acc, u_new, l_new, m_new, stream=None):
     return u_acc, l_acc, m_acc
 
 
+def merge_lse(o_acc, lse_acc, o_new, lse_new, stream=None):
+    """In-place log-sum-exp merge of (o_new, lse_new) into (o_acc, lse_acc)."""
+    lib = load()
+    for t in (o_acc, lse_acc, o_new, lse_new):
+        _check_cuda(t, "lse merge")
+        if t.dtype != torch.float32 or not t.is_contiguous():
+            raise ValueError("outputs and log-sum-exps must be contiguous fp32 tensors")
+    D = o_acc.shape[-1]
+    rows = o_acc.numel() // D
+    if o_new.numel() != o_acc.numel() or lse_acc.numel() != rows or lse_new.numel() != rows:
+        raise ValueError("shape mismatch between the two outputs")
+    check(lib.ra_merge_lse(rows, D, o_acc.data_ptr(), lse_acc.data_ptr(), o_new.data_ptr(),
+                           lse_new.data_ptr(), _stream(stream)))
+    return o_acc, lse_acc
+
+
+def stats_to_lse(m, l, lse=None, stream=None):
+    """lse = m + log(l) per row (-inf where l = 0)."""
+    lib = load()
+    for t in (m, l):
+        _check_cuda(t, "statistics")
+        if t.dtype != torch.float32 or not t.is_contiguous():
+            raise ValueError("statistics must be contiguous fp32 tensors")
+    if lse is None:
+        lse = torch.empty_like(m)
+    check(lib.ra_stats_to_lse(m.numel(), m.data_ptr(), l.data_ptr(), lse.data_ptr(), _stream(stream)))
+    return lse
+
+
 def segment_work(B, Hq, Hkv, D, q_segments, chunk_lens, chunk_spans, causal, dtype=_lib.RA_BF16):
     """Per query segment: visible (query, key) pairs per head and scheduled
     128x128 tile products (host-side bookkeeping, no GPU needed)."""

@@ -812,6 +812,27 @@ ra_status ra_merge_stats(int64_t rows, int64_t D, float* u_acc, float* l_acc, fl
                      "merge kernel launch");
 }
 
+ra_status ra_merge_lse(int64_t rows, int64_t D, float* o_acc, float* lse_acc, const float* o_new,
+                       const float* lse_new, void* stream) {
+  if (rows < 0 || D < 1) return fail(RA_ERR_INVALID, "need rows >= 0 and D >= 1");
+  if (rows == 0) return ok();
+  if (!o_acc || !lse_acc || !o_new || !lse_new) return fail(RA_ERR_INVALID, "NULL pointer");
+  if (rows > (int64_t(1) << 40) / D) return fail(RA_ERR_UNSUPPORTED, "too many elements");
+  const int sms = num_sms();
+  if (sms <= 0) return cuda_status(cudaErrorNoDevice, "querying the SM count");
+  return cuda_status(ra::launch_merge_lse_f32(rows, D, o_acc, lse_acc, o_new, lse_new, sms, stream),
+                     "lse merge kernel launch");
+}
+
+ra_status ra_stats_to_lse(int64_t rows, const float* m, const float* l, float* lse, void* stream) {
+  if (rows < 0) return fail(RA_ERR_INVALID, "need rows >= 0");
+  if (rows == 0) return ok();
+  if (!m || !l || !lse) return fail(RA_ERR_INVALID, "NULL pointer");
+  const int sms = num_sms();
+  if (sms <= 0) return cuda_status(cudaErrorNoDevice, "querying the SM count");
+  return cuda_status(ra::launch_stats_to_lse(rows, m, l, lse, sms, stream), "lse kernel launch");
+}
+
 ra_status ra_segment_work(const ra_problem* problem, const ra_q_segment* segs, int32_t nsegs,
                           const ra_kv_chunk* chunks, int32_t nchunks, int64_t* pairs,
                           int64_t* tiles) {

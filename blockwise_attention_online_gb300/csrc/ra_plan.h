@@ -139,6 +139,10 @@ int launch_simt_f32(const SimtPlan& plan, void* stream);
 int launch_merge_f32(int64_t rows, int64_t D, float* u_acc, float* l_acc,
                      float* m_acc, const float* u_new, const float* l_new,
                      const float* m_new, int num_sms, void* stream);
+int launch_merge_lse_f32(int64_t rows, int64_t D, float* o_acc, float* lse_acc, const float* o_new,
+                         const float* lse_new, int num_sms, void* stream);
+int launch_stats_to_lse(int64_t rows, const float* m, const float* l, float* lse, int num_sms,
+                        void* stream);
 int read_and_clear_device_error(int* code);
 // Backward: the preparation kernels (lse2, delta, query-tile position ranges),
 // then the dK/dV and dQ kernels; all on `stream`.

@@ -207,6 +207,83 @@ int launch_simt_f32(const SimtPlan& plan, void* stream) {
   return cudaGetLastError();
 }
 
+// Log-sum-exp form of the merge: two normalised outputs O_a, O_b with their
+// row log-sum-exps (natural log of the row's softmax denominator, in the units
+// of the scaled scores). lse = log(e^lse_a + e^lse_b); O = w_a O_a + w_b O_b
+// with w_x = e^(lse_x - lse). A side with lse = -inf weighs nothing; two such
+// sides give O = 0, lse = -inf.
+__device__ __forceinline__ void lse_coeffs(float la, float lb, float& wa, float& wb, float& ls) {
+  const float mx = fmaxf(la, lb);
+  if (mx == -__builtin_huge_valf()) {
+    wa = wb = 0.f;
+    ls = mx;
+    return;
+  }
+  const float ea = (la == -__builtin_huge_valf()) ? 0.f : expf(la - mx);
+  const float eb = (lb == -__builtin_huge_valf()) ? 0.f : expf(lb - mx);
+  const float sum = ea + eb;
+  wa = ea / sum;
+  wb = eb / sum;
+  ls = mx + logf(sum);
+}
+
+__global__ void __launch_bounds__(256) merge_lse_kernel(int64_t rows, int64_t D, float* o_acc,
+                                                        float* lse_acc, const float* o_new,
+                                                        const float* lse_new, int vec4) {
+  const int lane = threadIdx.x & 31;
+  const int64_t w0 = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nw = (int64_t(gridDim.x) * blockDim.x) >> 5;
+  for (int64_t row = w0; row < rows; row += nw) {
+    float wa, wb, ls;
+    lse_coeffs(lse_acc[row], lse_new[row], wa, wb, ls);
+    if (vec4) {
+      float4* oa = reinterpret_cast<float4*>(o_acc + row * D);
+      const float4* on = reinterpret_cast<const float4*>(o_new + row * D);
+      for (int64_t i = lane; i < D / 4; i += 32) {
+        const float4 x = oa[i], y = on[i];
+        oa[i] = make_float4(fmaf(wa, x.x, wb * y.x), fmaf(wa, x.y, wb * y.y), fmaf(wa, x.z, wb * y.z),
+                            fmaf(wa, x.w, wb * y.w));
+      }
+    } else {
+      float* oa = o_acc + row * D;
+      const float* on = o_new + row * D;
+      for (int64_t i = lane; i < D; i += 32) oa[i] = fmaf(wa, oa[i], wb * on[i]);
+    }
+    __syncwarp();
+    if (lane == 0) lse_acc[row] = ls;
+  }
+}
+
+// lse = m + log(l) per row, -inf where l = 0 (the row saw no key).
+__global__ void __launch_bounds__(256) stats_to_lse_kernel(int64_t rows, const float* m,
+                                                           const float* l, float* lse) {
+  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < rows;
+       i += int64_t(gridDim.x) * blockDim.x)
+    lse[i] = l[i] > 0.f ? m[i] + logf(l[i]) : -__builtin_huge_valf();
+}
+
+int launch_merge_lse_f32(int64_t rows, int64_t D, float* o_acc, float* lse_acc, const float* o_new,
+                         const float* lse_new, int num_sms, void* stream) {
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int64_t blocks = (rows + 7) / 8;
+  const int64_t cap = int64_t(num_sms) * 16;
+  if (blocks > cap) blocks = cap;
+  const int vec = (D % 4 == 0) &&
+                  ((reinterpret_cast<uintptr_t>(o_acc) | reinterpret_cast<uintptr_t>(o_new)) & 15u) == 0;
+  merge_lse_kernel<<<unsigned(blocks), 256, 0, st>>>(rows, D, o_acc, lse_acc, o_new, lse_new, vec);
+  return cudaGetLastError();
+}
+
+int launch_stats_to_lse(int64_t rows, const float* m, const float* l, float* lse, int num_sms,
+                        void* stream) {
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int64_t blocks = (rows + 255) / 256;
+  const int64_t cap = int64_t(num_sms) * 16;
+  if (blocks > cap) blocks = cap;
+  stats_to_lse_kernel<<<unsigned(blocks), 256, 0, st>>>(rows, m, l, lse);
+  return cudaGetLastError();
+}
+
 int launch_merge_f32(int64_t rows, int64_t D, float* u_acc, float* l_acc, float* m_acc,
                      const float* u_new, const float* l_new, const float* m_new, int num_sms,
                      void* stream) {

@@ -154,6 +154,31 @@ ra_status ra_merge_stats(int64_t rows, int64_t D,
                          const float* m_new, void* stream);
 
 /*
+ * ra_merge_lse - the same merge in log-sum-exp form, for composing with
+ * kernels that return a normalised output and its row log-sum-exp ([GLOS]
+ * "Online softmax": outputs of different key/value blocks are combined with
+ * the log-sum-exp trick). In place into the accumulator:
+ *
+ *   lse' = log(exp(lse_acc) + exp(lse_new))
+ *   o_acc = exp(lse_acc - lse') o_acc + exp(lse_new - lse') o_new
+ *
+ * lse is the natural log of a row's softmax denominator in the units of the
+ * scaled scores (lse = m + log(l)); a side with lse = -inf weighs nothing and
+ * two such sides give o = 0, lse = -inf. fp32, contiguous: o [rows, D], lse
+ * [rows]. The _new arrays may not overlap the _acc arrays unless identical.
+ */
+ra_status ra_merge_lse(int64_t rows, int64_t D, float* o_acc, float* lse_acc,
+                       const float* o_new, const float* lse_new, void* stream);
+
+/*
+ * ra_stats_to_lse - lse = m + log(l) per row (-inf where l = 0), from the
+ * m, l of ra_ring_attention or ra_chunk_stats. fp32, contiguous [rows]; lse
+ * may alias m or l.
+ */
+ra_status ra_stats_to_lse(int64_t rows, const float* m, const float* l, float* lse,
+                          void* stream);
+
+/*
  * ra_ring_attention - the whole chunked forward pass in one persistent
  * kernel: each query tile walks the key/value chunks in its segment's ring
  * order, keeping m, l and the output accumulator on chip across all chunks,

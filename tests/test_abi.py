@@ -221,3 +221,13 @@ def test_backward_entry_rejects_before_launch():
     many = [(1, [(1, i, 1)]) for i in range(33)]
     assert _call_bwd(_problem(Sq=33), _segs([(33, [(33, 0, 1)])]), 1, _chunks(many), 33,
                      _grads(33)) == _lib.RA_ERR_UNSUPPORTED
+
+
+def test_lse_entries_reject_bad_arguments():
+    lib = _lib.load()
+    assert lib.ra_merge_lse(4, 0, 1, 1, 1, 1, None) == _lib.RA_ERR_INVALID
+    assert lib.ra_merge_lse(-1, 8, 1, 1, 1, 1, None) == _lib.RA_ERR_INVALID
+    assert lib.ra_merge_lse(4, 8, None, 16, 16, 16, None) == _lib.RA_ERR_INVALID
+    assert lib.ra_merge_lse(0, 8, None, None, None, None, None) == _lib.RA_OK
+    assert lib.ra_stats_to_lse(4, None, 16, 16, None) == _lib.RA_ERR_INVALID
+    assert lib.ra_stats_to_lse(0, None, None, None, None) == _lib.RA_OK

@@ -10,8 +10,9 @@ import pytest
 import torch
 
 import oracle
-from blockwise_attention_online_gb300 import (chunk_stats, device_status, layouts,
-                                              merge_stats, ring_attention, workloads)
+from blockwise_attention_online_gb300 import (chunk_stats, device_status, layouts, merge_lse,
+                                              merge_stats, ring_attention, stats_to_lse,
+                                              workloads)
 from _util import (assert_bf16, assert_f32, f64, layout_run)
 
 pytestmark = pytest.mark.gpu
@@ -274,3 +275,45 @@ def test_bf16_head_dim_96_chunk_stats():
     assert np.array_equal(np.isfinite(f64(m)), fin)
     assert (np.abs(f64(u) - u_r) <= 1e-2 * np.maximum(1.0, l_r)[..., None]).all()
     assert (np.abs(f64(l) - l_r) <= 1e-3 * np.maximum(1.0, l_r)).all()
+
+
+@pytest.mark.parametrize("D", [5, 128])
+def test_merge_lse_matches_oracle(D):
+    rng = np.random.default_rng(D)
+    rows = 1000
+    oa = rng.standard_normal((rows, D)).astype(np.float32)
+    ob = rng.standard_normal((rows, D)).astype(np.float32)
+    la = rng.normal(0, 6, rows).astype(np.float32)
+    lb = rng.normal(0, 6, rows).astype(np.float32)
+    la[:7] = -np.inf                      # empty accumulator rows
+    lb[3:10] = -np.inf                    # empty new rows (3..6 empty on both sides)
+    ref_o, ref_l = oracle.merge_lse((oa, la), (ob, lb))
+    o_acc, l_acc = torch.tensor(oa, device=DEV), torch.tensor(la, device=DEV)
+    merge_lse(o_acc, l_acc, torch.tensor(ob, device=DEV), torch.tensor(lb, device=DEV))
+    device_status()
+    got_l = f64(l_acc)
+    fin = np.isfinite(ref_l)
+    assert np.array_equal(np.isfinite(got_l), fin)
+    assert np.abs(got_l[fin] - ref_l[fin]).max() <= 1e-5 * max(1.0, np.abs(ref_l[fin]).max())
+    assert np.abs(f64(o_acc) - ref_o).max() <= 1e-5
+
+
+def test_lse_composes_ring_outputs():
+    """Two groups of chunks attended separately, each (O, lse) from the ring
+    kernel, merged in log-sum-exp form: equal to one call over all chunks."""
+    q, k, v = _bf16_inputs(1, 4, 2, 1024, 128, seed=31)
+    qd = q.to(DEV)
+    kc = _split(k.to(DEV), [256, 256, 512])
+    vc = _split(v.to(DEV), [256, 256, 512])
+    spans = [[(256, 0, 1)], [(256, 256, 1)], [(512, 512, 1)]]
+    O1, m1, l1 = ring_attention(qd, kc[:2], vc[:2], chunk_spans=spans[:2], causal=True,
+                                out_dtype=torch.float32)
+    O2, m2, l2 = ring_attention(qd, kc[2:], vc[2:], chunk_spans=spans[2:], causal=True,
+                                out_dtype=torch.float32)
+    lse1, lse2 = stats_to_lse(m1, l1), stats_to_lse(m2, l2)
+    merge_lse(O1, lse1, O2, lse2)
+    device_status()
+    ref = _full_ref(q, k, v, True, 1 / math.sqrt(128))
+    assert np.abs(f64(O1) - ref[0]).max() <= 1e-2
+    lse_ref = oracle.stats_to_lse(ref[1], ref[2])
+    assert np.abs(f64(lse1) - lse_ref).max() <= 1e-3 * max(1.0, np.abs(lse_ref).max())
