@@ -33,6 +33,12 @@ design notes):
   positions ([BLOG] "Causal masks depend on global positions").
 * A row that sees no key has u = 0, l = 0, m = -inf, and its output is 0.
   In a merge a side with m = -inf contributes nothing (no exp(-inf + inf)).
+* Documents (packed variable-length sequences; the pages do not treat them,
+  this is the plainest extension of the global-position mask): ``docs`` is a
+  strictly increasing list of boundaries b_0 < b_1 < ... < b_n, document d
+  holds the positions [b_d, b_{d+1}), and a key is visible to a query only if
+  both lie in the same document (and, when causal, the key is not in the
+  query's future). ``docs=None`` is one document holding every position.
 """
 from __future__ import annotations
 
@@ -45,18 +51,39 @@ def _f64(x):
     return np.asarray(x, dtype=np.float64)
 
 
-def _visible(q_pos, k_pos, causal):
+def document_of(pos, docs):
+    """Index d of the document [b_d, b_{d+1}) that holds each position.
+
+    Raises ValueError for a position outside [b_0, b_n) or for boundaries
+    that are not strictly increasing.
+    """
+    pos = np.asarray(pos, dtype=np.int64)
+    b = np.asarray(docs, dtype=np.int64)
+    if b.ndim != 1 or b.size < 2 or (np.diff(b) <= 0).any():
+        raise ValueError("document boundaries must be >= 2 strictly increasing values")
+    d = np.searchsorted(b, pos, side="right") - 1
+    if pos.size and ((d < 0).any() or (d >= b.size - 1).any()):
+        raise ValueError("a position lies outside every document")
+    return d
+
+
+def _visible(q_pos, k_pos, causal, docs=None):
     """Boolean [Sq, Sk] visibility matrix from global positions.
 
     [BLOG] "Causal masks depend on global positions": a query may not read a
     key that lies in its future, judged by global position, not by local
-    row/column index.
+    row/column index. With documents, also only keys of the query's own
+    document (the module's reading).
     """
     q_pos = np.asarray(q_pos, dtype=np.int64)
     k_pos = np.asarray(k_pos, dtype=np.int64)
     if not causal:
-        return np.ones((q_pos.shape[0], k_pos.shape[0]), dtype=bool)
-    return k_pos[None, :] <= q_pos[:, None]
+        vis = np.ones((q_pos.shape[0], k_pos.shape[0]), dtype=bool)
+    else:
+        vis = k_pos[None, :] <= q_pos[:, None]
+    if docs is not None:
+        vis &= document_of(q_pos, docs)[:, None] == document_of(k_pos, docs)[None, :]
+    return vis
 
 
 def _head_group(Hq, Hkv):
@@ -65,7 +92,7 @@ def _head_group(Hq, Hkv):
     return Hq // Hkv
 
 
-def chunk_stats(q, k, v, q_pos, k_pos, causal, scale):
+def chunk_stats(q, k, v, q_pos, k_pos, causal, scale, docs=None):
     """Statistics of one key/value chunk, computed as if it were the only one.
 
     [EX] task statement: returns (chunk_output, chunk_sum, chunk_max) = the
@@ -80,7 +107,7 @@ def chunk_stats(q, k, v, q_pos, k_pos, causal, scale):
     B, Hq, Sq, D = q.shape
     Hkv, Sk = k.shape[1], k.shape[2]
     g = _head_group(Hq, Hkv)
-    vis = _visible(q_pos, k_pos, causal)
+    vis = _visible(q_pos, k_pos, causal, docs)
     u = np.zeros((B, Hq, Sq, v.shape[3]))
     l = np.zeros((B, Hq, Sq))
     m = np.full((B, Hq, Sq), NEG_INF)
@@ -134,7 +161,7 @@ def normalize(u, l):
     return o
 
 
-def full_attention(q, k, v, q_pos, k_pos, causal, scale):
+def full_attention(q, k, v, q_pos, k_pos, causal, scale, docs=None):
     """Ordinary softmax attention over the whole key/value sequence at once.
 
     This is the plain definition the chunked method must equal exactly: the
@@ -144,7 +171,7 @@ def full_attention(q, k, v, q_pos, k_pos, causal, scale):
 
     Returns O [B, Hq, Sq, D], m [B, Hq, Sq], l [B, Hq, Sq].
     """
-    u, l, m = chunk_stats(q, k, v, q_pos, k_pos, causal, scale)
+    u, l, m = chunk_stats(q, k, v, q_pos, k_pos, causal, scale, docs)
     return normalize(u, l), m, l
 
 
@@ -160,7 +187,7 @@ def ring_order(rank, world):
 
 
 def ring_attention(q, k_chunks, v_chunks, q_pos, k_pos_chunks, causal, scale,
-                   order=None):
+                   order=None, docs=None):
     """The pages' chunked algorithm, written out: stats per chunk + merges.
 
     [EX] task statement: visit key/value chunks one at a time, never forming
@@ -182,13 +209,13 @@ def ring_attention(q, k_chunks, v_chunks, q_pos, k_pos_chunks, causal, scale,
         order = range(len(k_chunks))
     for c in order:
         st = chunk_stats(q, k_chunks[c], v_chunks[c], q_pos, k_pos_chunks[c],
-                         causal, scale)
+                         causal, scale, docs)
         acc = merge_stats(acc, st)
     u, l, m = acc
     return normalize(u, l), m, l
 
 
-def attention_rows(q, k, v, q_pos, k_pos, causal, scale, rows):
+def attention_rows(q, k, v, q_pos, k_pos, causal, scale, rows, docs=None):
     """The definition of ``full_attention`` evaluated for selected rows only.
 
     ``rows`` is a list of (b, h, i) triples. Each row is computed on its own,
@@ -222,9 +249,8 @@ def attention_rows(q, k, v, q_pos, k_pos, causal, scale, rows):
             idx = np.array([it[0] for it in grp])
             qs = np.stack([_f64(q[b, h, i]) for _, h, i in grp])     # [R, D]
             s = scale * (qs @ kh.T)                                  # [R, Sk]
-            if causal:
-                qp = np.array([q_pos[i] for _, _, i in grp])
-                s = np.where(k_pos[None, :] <= qp[:, None], s, NEG_INF)
+            qp = np.array([q_pos[i] for _, _, i in grp])
+            s = np.where(_visible(qp, k_pos, causal, docs), s, NEG_INF)
             mrow = s.max(axis=1)
             seen = np.isfinite(mrow)
             shift = np.where(seen, mrow, 0.0)
@@ -237,12 +263,23 @@ def attention_rows(q, k, v, q_pos, k_pos, causal, scale, rows):
     return O, M, L
 
 
-def unmasked_pairs(q_pos, k_pos, causal):
+def unmasked_pairs(q_pos, k_pos, causal, docs=None):
     """Exact number of visible (query, key) pairs: the work a causal mask
     leaves ([BLOG] "Separate local compute from network traffic": attention
-    arithmetic counts query-key pairs)."""
+    arithmetic counts query-key pairs). With documents, a query counts the
+    keys of its own document only (up to its position when causal)."""
     q_pos = np.sort(np.asarray(q_pos, dtype=np.int64))
     k_pos = np.sort(np.asarray(k_pos, dtype=np.int64))
-    if not causal:
-        return int(q_pos.size) * int(k_pos.size)
-    return int(np.searchsorted(k_pos, q_pos, side="right").sum())
+    if docs is None:
+        if not causal:
+            return int(q_pos.size) * int(k_pos.size)
+        return int(np.searchsorted(k_pos, q_pos, side="right").sum())
+    b = np.asarray(docs, dtype=np.int64)
+    d = document_of(q_pos, b)
+    document_of(k_pos, b)
+    lo = np.searchsorted(k_pos, b[d], side="left")
+    if causal:
+        hi = np.searchsorted(k_pos, q_pos, side="right")
+    else:
+        hi = np.searchsorted(k_pos, b[d + 1], side="left")
+    return int((hi - lo).sum())

@@ -22,7 +22,8 @@ S = scale * Q K^T over the visible keys (global positions, as in the forward):
     dK = scale * dS^T Q
 
 With grouped heads, key/value head g receives the sum over the query heads
-h with h // (Hq / Hkv) == g (the forward's head mapping).
+h with h // (Hq / Hkv) == g (the forward's head mapping). ``docs`` restricts
+visibility to the query's own document, as in the forward.
 """
 from __future__ import annotations
 
@@ -31,7 +32,7 @@ import numpy as np
 from .attention import _f64, _head_group, _visible, full_attention
 
 
-def attention_backward(q, k, v, dout, q_pos, k_pos, causal, scale):
+def attention_backward(q, k, v, dout, q_pos, k_pos, causal, scale, docs=None):
     """Gradients of sum(dout * O) with respect to q, k, v, by the definition.
 
     Shapes: q, dout [B, Hq, Sq, D]; k, v [B, Hkv, Sk, D]. Returns dq, dk, dv
@@ -41,7 +42,7 @@ def attention_backward(q, k, v, dout, q_pos, k_pos, causal, scale):
     B, Hq, Sq, D = q.shape
     Hkv, Sk = k.shape[1], k.shape[2]
     g = _head_group(Hq, Hkv)
-    vis = _visible(q_pos, k_pos, causal)
+    vis = _visible(q_pos, k_pos, causal, docs)
     dq = np.zeros_like(q)
     dk = np.zeros_like(k)
     dv = np.zeros_like(v)
@@ -64,7 +65,8 @@ def attention_backward(q, k, v, dout, q_pos, k_pos, causal, scale):
     return dq, dk, dv
 
 
-def ring_attention_backward(q, k_chunks, v_chunks, dout, q_pos, k_pos_chunks, causal, scale):
+def ring_attention_backward(q, k_chunks, v_chunks, dout, q_pos, k_pos_chunks, causal, scale,
+                            docs=None):
     """The blog's aggregation, chunk by chunk.
 
     The forward's row statistics (max m and denominator l over ALL chunks)
@@ -84,7 +86,7 @@ def ring_attention_backward(q, k_chunks, v_chunks, dout, q_pos, k_pos_chunks, ca
     k_all = np.concatenate([_f64(x) for x in k_chunks], axis=2)
     v_all = np.concatenate([_f64(x) for x in v_chunks], axis=2)
     k_pos_all = np.concatenate([np.asarray(p, dtype=np.int64) for p in k_pos_chunks])
-    O, m, l = full_attention(q, k_all, v_all, q_pos, k_pos_all, causal, scale)
+    O, m, l = full_attention(q, k_all, v_all, q_pos, k_pos_all, causal, scale, docs)
     delta = (dout * O).sum(axis=3)                       # [B, Hq, Sq]
     Hkv = k_all.shape[1]
     g = _head_group(Hq, Hkv)
@@ -95,7 +97,7 @@ def ring_attention_backward(q, k_chunks, v_chunks, dout, q_pos, k_pos_chunks, ca
     dk_chunks, dv_chunks = [], []
     for kc, vc, kp in zip(k_chunks, v_chunks, k_pos_chunks):
         kc, vc = _f64(kc), _f64(vc)
-        vis = _visible(q_pos, kp, causal)
+        vis = _visible(q_pos, kp, causal, docs)
         dkc = np.zeros_like(kc)
         dvc = np.zeros_like(vc)
         for b in range(B):
