@@ -192,3 +192,16 @@ def test_bad_boundaries_rejected():
         oracle.document_of([5], [0, 4])
     with pytest.raises(ValueError):
         oracle.document_of([0], [3, 9])
+
+
+def test_planted_boundary_slip_is_caught(monkeypatch):
+    """A document lookup that puts each boundary position into the previous
+    document (an off-by-one at b_d) must fail the per-document pin."""
+    import oracle.attention as A
+
+    def bad_document_of(pos, docs):
+        b = np.asarray(docs, dtype=np.int64)
+        return np.clip(np.searchsorted(b, np.asarray(pos), side="left") - 1, 0, b.size - 2)
+    monkeypatch.setattr(A, "document_of", bad_document_of)
+    with pytest.raises(AssertionError):
+        test_packed_equals_documents_solved_separately(True, 2, 2)

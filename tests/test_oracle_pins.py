@@ -396,7 +396,7 @@ def test_planted_one_sided_rescale_is_caught(monkeypatch):
 def test_planted_causal_off_by_one_is_caught(monkeypatch):
     import oracle.attention as A
 
-    def bad_visible(q_pos, k_pos, causal):
+    def bad_visible(q_pos, k_pos, causal, docs=None):
         q_pos = np.asarray(q_pos); k_pos = np.asarray(k_pos)
         if not causal:
             return np.ones((q_pos.size, k_pos.size), dtype=bool)
@@ -410,12 +410,12 @@ def test_planted_transposed_head_group_is_caught(monkeypatch):
     import oracle.attention as A
     real = A.chunk_stats
 
-    def bad_stats(q, k, v, q_pos, k_pos, causal, scale):
+    def bad_stats(q, k, v, q_pos, k_pos, causal, scale, docs=None):
         Hq, Hkv = q.shape[1], k.shape[1]
         idx = [h % Hkv for h in range(Hq)]
         kk = np.asarray(k)[:, idx]
         vv = np.asarray(v)[:, idx]
-        return real(q, kk, vv, q_pos, k_pos, causal, scale)
+        return real(q, kk, vv, q_pos, k_pos, causal, scale, docs)
     monkeypatch.setattr(A, "chunk_stats", bad_stats)
     with pytest.raises(AssertionError):
         test_matches_torch_sdpa_fp64(False, 6, 3)
