@@ -45,17 +45,19 @@ def _peaks():
 
 def _traffic(kernel_key):
     """DRAM bytes per launch from a committed ncu summary, valid only while the
-    kernel source is unchanged (its hash is stored next to the counters)."""
+    kernel's sources are unchanged (their hash is stored next to the counters)."""
     import hashlib
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             tab = json.load(f)
         ent = tab[kernel_key]
-        src = os.path.join(ROOT, "blockwise_attention_online_gb300", "csrc", ent["source"])
-        with open(src, "rb") as f:
-            h = hashlib.sha256(f.read()).hexdigest()[:16]
-        return int(ent["bytes_per_launch"]) if h == ent["source_sha"] else None
+        srcs = ent["source"] if isinstance(ent["source"], list) else [ent["source"]]
+        h = hashlib.sha256()
+        for name in srcs:
+            with open(os.path.join(ROOT, "blockwise_attention_online_gb300", "csrc", name), "rb") as f:
+                h.update(f.read())
+        return int(ent["bytes_per_launch"]) if h.hexdigest()[:16] == ent["source_sha"] else None
     except Exception:
         return None
 
@@ -151,6 +153,21 @@ def build_workload(name, layout, device):
     return w, qs, kc, vc, rs, segs
 
 
+def _docs(w, mean_len):
+    """Packed documents for --docs: seeded boundaries over the workload's
+    positions, and the algorithmic FLOPs of one forward with them (exact
+    visible pairs: n^2 per document of n positions, n(n+1)/2 when causal)."""
+    from blockwise_attention_online_gb300 import workloads
+    if not mean_len:
+        return None, w.flops()
+    b = workloads.packed_documents(w.S, w.seed, mean_len)
+    pairs = 0
+    for a, z in zip(b[:-1], b[1:]):
+        n = z - a
+        pairs += n * (n + 1) // 2 if w.causal else n * n
+    return b, 4.0 * w.B * w.Hq * w.D * pairs
+
+
 def run_gpu(args):
     import torch
     import torch.distributed as dist
@@ -164,7 +181,7 @@ def run_gpu(args):
     torch.cuda.set_device(dev)
 
     w, qs, kc, vc, rs, segs = build_workload(args.workload, args.layout, dev)
-    flops = w.flops()
+    docs, flops = _docs(w, args.docs)
     out = torch.empty_like(qs)
     m = torch.empty(qs.shape[:3], device=dev, dtype=torch.float32)
     l = torch.empty_like(m)
@@ -173,7 +190,7 @@ def run_gpu(args):
 
     def step():
         ring_attention(qs, kc, vc, chunk_spans=rs, q_segments=segs, causal=w.causal,
-                       out=out, m=m, l=l)
+                       out=out, m=m, l=l, docs=docs)
 
     for _ in range(args.warmup):
         flush.fill_(1.0)
@@ -223,7 +240,7 @@ def run_gpu(args):
         def e2e_step(i):
             ho, hm, hl = outs[i % 2]
             ring_attention_host(hq, hk, hv, chunk_spans=rs, q_segments=segs, causal=w.causal,
-                                out=ho, m=hm, l=hl, stream=streams[i % 2])
+                                out=ho, m=hm, l=hl, docs=docs, stream=streams[i % 2])
 
         for i in range(4):
             e2e_step(i)
@@ -250,7 +267,7 @@ def run_gpu(args):
     peak_b, peak_s, hbm, src = _peaks()
     mean_ms = total_ms / args.steps
     achieved = flops / (mean_ms * 1e-3) / 1e12
-    kernel_key = f"tc_ring_kernel:{w.name}:{w.layout}"
+    kernel_key = f"tc_ring_kernel:{w.name}:{w.layout}" + (f":docs{args.docs}" if docs else "")
     line = {
         "metric": METRIC,
         "value": round(value, 3),
@@ -268,6 +285,9 @@ def run_gpu(args):
                    "D": w.D, "causal": w.causal, "chunks": w.n_chunks, "layout": w.layout,
                    "ring_order": "segment r visits chunks r, r-1, ...",
                    "flops_per_step": flops,
+                   "docs": ({"mean_len": args.docs, "n_docs": len(docs) - 1,
+                             "recipe": "workloads.packed_documents(S, seed, mean_len)"}
+                            if docs else None),
                    "l2": f"flushed before every step ({L2_FLUSH_BYTES >> 20} MiB write)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "pct_of_peak": round(100 * value / world / peak_b, 2),
@@ -281,7 +301,7 @@ def run_gpu(args):
         "e2e": e2e,
     }
     if not args.no_cpu_baseline and world == 1:
-        line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
+        line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds, docs)
     return line
 
 
@@ -407,12 +427,17 @@ def _oracle_sample(w, rows_per_head, seed=1234):
     return q.float(), k.float(), v.float(), heads, rng
 
 
-def _row_flops(w, i):
-    keys = (i + 1) if w.causal else w.S
+def _row_flops(w, i, docs=None):
+    if docs is None:
+        keys = (i + 1) if w.causal else w.S
+    else:
+        import bisect
+        d = bisect.bisect_right(docs, i) - 1
+        keys = (i + 1 - docs[d]) if w.causal else (docs[d + 1] - docs[d])
     return 4.0 * keys * w.D
 
 
-def cpu_baseline(w, seconds):
+def cpu_baseline(w, seconds, docs=None):
     """The fp64 oracle, as it stands, on a bounded sample of the workload's
     rows, timed on this machine's host cores."""
     import numpy as np
@@ -423,8 +448,8 @@ def cpu_baseline(w, seconds):
     t0 = time.perf_counter()
     while el < seconds:
         rows = [(0, int(h), int(rng.integers(0, w.S))) for h in heads]
-        oracle.attention_rows(q, k, v, pos, pos, w.causal, w.scale, rows)
-        done_flops += sum(_row_flops(w, i) for _, _, i in rows)
+        oracle.attention_rows(q, k, v, pos, pos, w.causal, w.scale, rows, docs=docs)
+        done_flops += sum(_row_flops(w, i, docs) for _, _, i in rows)
         rows_done += len(rows)
         el = time.perf_counter() - t0
     return {"value": round(done_flops / el / 1e12, 6), "unit": "TFLOP/s",
@@ -443,13 +468,14 @@ def run_reference(args):
     if rank != 0:
         return None
     w = workloads.WORKLOADS[args.workload]
+    docs, _ = _docs(w, args.docs)
     q, k, v, heads, rng = _oracle_sample(w, 0)
     pos = np.arange(w.S)
 
     def one():
         rows = [(0, int(h), int(rng.integers(0, w.S))) for h in heads]
-        oracle.attention_rows(q, k, v, pos, pos, w.causal, w.scale, rows)
-        return sum(_row_flops(w, i) for _, _, i in rows)
+        oracle.attention_rows(q, k, v, pos, pos, w.causal, w.scale, rows, docs=docs)
+        return sum(_row_flops(w, i, docs) for _, _, i in rows)
 
     for _ in range(args.warmup):
         one()
@@ -466,7 +492,8 @@ def run_reference(args):
             "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic: seeded N(0,1) Q/K/V (bf16 values upcast to f64)",
             "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "S": w.S,
-                       "D": w.D, "causal": w.causal, "chunks": w.n_chunks},
+                       "D": w.D, "causal": w.causal, "chunks": w.n_chunks,
+                       "docs": {"mean_len": args.docs, "n_docs": len(docs) - 1} if docs else None},
             "cpu_baseline": {"value": round(val, 6), "unit": "TFLOP/s", "cores": os.cpu_count(),
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": round(val, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
@@ -484,6 +511,9 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--docs", type=int, default=0,
+                    help="pack the sequence into seeded documents of this mean length "
+                         "(forward only; 0 = one document)")
     ap.add_argument("--pass", dest="which", default="fwd", choices=["fwd", "bwd"],
                     help="time the forward (default) or the backward pass")
     args = ap.parse_args()

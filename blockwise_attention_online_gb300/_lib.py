@@ -55,7 +55,8 @@ class Problem(ctypes.Structure):
     _fields_ = [("B", c_int64), ("Hq", c_int64), ("Hkv", c_int64), ("D", c_int64),
                 ("Sq", c_int64), ("dtype", c_int32), ("causal", c_int32),
                 ("scale", c_float), ("o_fp32", c_int32),
-                ("q_strides", Strides), ("o_strides", Strides)]
+                ("q_strides", Strides), ("o_strides", Strides),
+                ("doc_bounds", c_void_p), ("n_docs", c_int32), ("reserved_docs", c_int32)]
 
 
 class RaError(RuntimeError):

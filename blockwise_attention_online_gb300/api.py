@@ -78,7 +78,20 @@ def _chunks(k_chunks, v_chunks, chunk_spans, host=False):
     return arr, len(k_chunks)
 
 
-def _problem(q, Hkv, causal, scale, out_strides):
+def _set_docs(pb, docs):
+    """Document boundaries b_0 < ... < b_n (host int64 array kept alive on pb)."""
+    if docs is None:
+        pb.n_docs = 0
+        pb.doc_bounds = None
+        return
+    b = [int(x) for x in docs]
+    arr = (ctypes.c_int64 * len(b))(*b)
+    pb._docs_keepalive = arr
+    pb.doc_bounds = ctypes.cast(arr, ctypes.c_void_p)
+    pb.n_docs = len(b) - 1
+
+
+def _problem(q, Hkv, causal, scale, out_strides, docs=None):
     B, Hq, Sq, D = q.shape
     pb = Problem()
     pb.B, pb.Hq, pb.Hkv, pb.D, pb.Sq = B, Hq, Hkv, D, Sq
@@ -88,12 +101,13 @@ def _problem(q, Hkv, causal, scale, out_strides):
     pb.o_fp32 = 0
     pb.q_strides = _strides(q)
     pb.o_strides = out_strides
+    _set_docs(pb, docs)
     return pb
 
 
 def ring_attention(q, k_chunks, v_chunks, *, chunk_spans=None, q_segments=None,
                    causal=False, scale=None, out=None, m=None, l=None, out_dtype=None,
-                   stream=None):
+                   docs=None, stream=None):
     """Chunked forward pass over key/value chunks (one persistent kernel).
 
     q: [B, Hq, Sq, D] (bf16 or fp32, CUDA). k_chunks / v_chunks: lists of
@@ -104,6 +118,8 @@ def ring_attention(q, k_chunks, v_chunks, *, chunk_spans=None, q_segments=None,
     the chunks in ring order starting at chunk r.
     out_dtype: torch.float32 to receive O in fp32 from bf16 inputs (default:
     the dtype of q, or of ``out`` when given).
+    docs: packed documents, boundaries b_0 < ... < b_n of global positions
+    (a query sees only keys of its own document [b_d, b_{d+1})).
     Returns (O [B, Hq, Sq, D], m [B, Hq, Sq] fp32, l [B, Hq, Sq] fp32).
     """
     lib = load()
@@ -118,7 +134,7 @@ def ring_attention(q, k_chunks, v_chunks, *, chunk_spans=None, q_segments=None,
         m = torch.empty(B, Hq, Sq, device=q.device, dtype=torch.float32)
     if l is None:
         l = torch.empty(B, Hq, Sq, device=q.device, dtype=torch.float32)
-    pb = _problem(q, Hkv, causal, scale, _strides(out))
+    pb = _problem(q, Hkv, causal, scale, _strides(out), docs)
     pb.o_fp32 = 1 if (out.dtype == torch.float32 and q.dtype != torch.float32) else 0
     segs, nsegs = _segments(q, q_segments)
     chs, nch = _chunks(k_chunks, v_chunks, chunk_spans)
@@ -129,7 +145,7 @@ def ring_attention(q, k_chunks, v_chunks, *, chunk_spans=None, q_segments=None,
 
 def ring_attention_host(q, k_chunks, v_chunks, *, chunk_spans=None, q_segments=None,
                         causal=False, scale=None, out=None, m=None, l=None, out_dtype=None,
-                        stream=None):
+                        docs=None, stream=None):
     """ring_attention with every tensor in host memory (pinned for full speed).
 
     The library copies the inputs to the device, runs the ring kernel and
@@ -157,7 +173,7 @@ def ring_attention_host(q, k_chunks, v_chunks, *, chunk_spans=None, q_segments=N
     for t in (out, m, l):
         if t.is_cuda or not t.is_contiguous():
             raise ValueError("outputs must be contiguous CPU tensors")
-    pb = _problem(q, Hkv, causal, scale, _strides(out))
+    pb = _problem(q, Hkv, causal, scale, _strides(out), docs)
     pb.o_fp32 = 1 if (out.dtype == torch.float32 and q.dtype != torch.float32) else 0
     segs, nsegs = _segments(q, q_segments)
     chs, nch = _chunks(k_chunks, v_chunks, chunk_spans, host=True)
@@ -168,11 +184,11 @@ def ring_attention_host(q, k_chunks, v_chunks, *, chunk_spans=None, q_segments=N
 
 def ring_attention_bwd(q, k_chunks, v_chunks, o, dout, m, l, *, chunk_spans=None,
                        q_segments=None, causal=False, scale=None, dq=None, dk=None, dv=None,
-                       stream=None):
+                       docs=None, stream=None):
     """Gradients of ``ring_attention``'s O: (dq, [dk per chunk], [dv per chunk]).
 
-    q, k_chunks, v_chunks, chunk_spans, q_segments, causal, scale: exactly as
-    given to the forward call; o, m, l: its outputs; dout: bf16 gradient of O
+    q, k_chunks, v_chunks, chunk_spans, q_segments, causal, scale, docs:
+    exactly as given to the forward call; o, m, l: its outputs; dout: bf16 gradient of O
     with o's strides. Gradients are fp32: dq like q, dk/dv like each chunk
     (dense). bf16 inputs only.
     """
@@ -194,7 +210,7 @@ def ring_attention_bwd(q, k_chunks, v_chunks, o, dout, m, l, *, chunk_spans=None
     for t in [dq, *dk, *dv]:
         if t.dtype != torch.float32 or not t.is_contiguous():
             raise ValueError("gradients are dense fp32 tensors")
-    pb = _problem(q, Hkv, causal, scale, _strides(o))
+    pb = _problem(q, Hkv, causal, scale, _strides(o), docs)
     pb.o_fp32 = 1 if (o.dtype == torch.float32 and q.dtype != torch.float32) else 0
     segs, nsegs = _segments(q, q_segments)
     chs, nch = _chunks(k_chunks, v_chunks, chunk_spans)
@@ -209,7 +225,7 @@ def ring_attention_bwd(q, k_chunks, v_chunks, o, dout, m, l, *, chunk_spans=None
 
 
 def chunk_stats(q, k, v, *, spans=None, q_segments=None, causal=False, scale=None,
-                u=None, l=None, m=None, stream=None):
+                u=None, l=None, m=None, docs=None, stream=None):
     """(u, l, m) of one key/value chunk, as if it were the only one.
 
     u: [B, Hq, Sq, D] fp32 un-normalised numerator; l, m: [B, Hq, Sq] fp32.
@@ -224,7 +240,7 @@ def chunk_stats(q, k, v, *, spans=None, q_segments=None, causal=False, scale=Non
         l = torch.empty(B, Hq, Sq, device=q.device, dtype=torch.float32)
     if m is None:
         m = torch.empty(B, Hq, Sq, device=q.device, dtype=torch.float32)
-    pb = _problem(q, k.shape[1], causal, scale, _strides(u))
+    pb = _problem(q, k.shape[1], causal, scale, _strides(u), docs)
     segs, nsegs = _segments(q, q_segments)
     chs, _ = _chunks([k], [v], None if spans is None else [spans])
     check(lib.ra_chunk_stats(ctypes.byref(pb), q.data_ptr(), segs, nsegs, chs,
@@ -279,7 +295,8 @@ def stats_to_lse(m, l, lse=None, stream=None):
     return lse
 
 
-def segment_work(B, Hq, Hkv, D, q_segments, chunk_lens, chunk_spans, causal, dtype=_lib.RA_BF16):
+def segment_work(B, Hq, Hkv, D, q_segments, chunk_lens, chunk_spans, causal, dtype=_lib.RA_BF16,
+                 docs=None):
     """Per query segment: visible (query, key) pairs per head and scheduled
     128x128 tile products (host-side bookkeeping, no GPU needed)."""
     lib = load()
@@ -289,6 +306,7 @@ def segment_work(B, Hq, Hkv, D, q_segments, chunk_lens, chunk_spans, causal, dty
     pb.dtype, pb.causal, pb.scale, pb.o_fp32 = dtype, 1 if causal else 0, 0.0, 0
     pb.q_strides = Strides(Hq * Sq * D, Sq * D, D)
     pb.o_strides = pb.q_strides
+    _set_docs(pb, docs)
     segs = (QSegment * len(q_segments))()
     for i, (ln, spans) in enumerate(q_segments):
         segs[i].len = int(ln)

@@ -62,7 +62,7 @@ struct BwdCfg {
   static constexpr int kStage0 = 2 * kTileBytes;
   static constexpr int kStageBytes = 2 * kTileBytes;
   static constexpr int kAux0 = kStage0 + 2 * kStageBytes;
-  static constexpr int kAuxBytes = 3 * 128 * 4;
+  static constexpr int kAuxBytes = 4 * 128 * 4;
   static constexpr int kBar = kAux0 + 2 * kAuxBytes;
   static constexpr int kBarBytes = 256;
   static constexpr int kSmemBytes = kBar + kBarBytes + 1024;  // + alignment slack
@@ -79,12 +79,17 @@ __device__ __forceinline__ int bwd_row_position(const BwdPlan& p, int row) {
   return q.pos0 + q.step * (row - q.row0);
 }
 
-// Key tiles of span k not entirely in the future of position qmax.
-__device__ __forceinline__ int bwd_live_tiles(const BwdPlan& p, int k, int qmax) {
+// Key tiles [tb, te) of span k holding a position inside the key window
+// [lo, hi] of some row of a query tile.
+__device__ __forceinline__ void bwd_live_tiles(const BwdPlan& p, int k, int lo, int hi, int& tb,
+                                               int& te) {
   const KvSeg& s = p.ks[k];
-  if (!p.causal) return s.ntiles;
-  if (qmax < s.pos0) return 0;
-  return min(s.ntiles, ((qmax - s.pos0) / s.step) / 128 + 1);
+  if (!p.causal && p.n_docs == 0) {
+    tb = 0;
+    te = s.ntiles;
+    return;
+  }
+  live_range(s.pos0, s.step, s.len, lo, hi, tb, te);
 }
 
 // ------------------------------------------------------------ preparation
@@ -132,18 +137,23 @@ __global__ void bwd_prep_kernel(const void* o, int o_fp32, int64_t o_sb, int64_t
   lse2[row] = lr > 0.f ? fmaf(m[row], kLog2e, log2f(lr)) : kInf;
 }
 
-// One thread per 128-row query tile: its lowest and highest position.
-__global__ void bwd_qtile_kernel(const __grid_constant__ BwdPlan p, int2* out) {
+// One thread per 128-row query tile: bounds of its rows' key windows
+// (x: lowest lo, y: highest hi, z: highest lo, w: lowest hi). A key tile
+// inside [z, w] is visible to every row; one outside [x, y] to none.
+__global__ void bwd_qtile_kernel(const __grid_constant__ BwdPlan p, int4* out) {
   const int t = blockIdx.x * blockDim.x + threadIdx.x;
   if (t >= p.n_qtiles) return;
-  int lo = 0x7fffffff, hi = -1;
+  int4 w = make_int4(0x7fffffff, -1, -1, 0x7fffffff);
   const int r1 = min(p.Sq, 128 * t + 128);
   for (int r = 128 * t; r < r1; ++r) {
-    const int pos = bwd_row_position(p, r);
-    lo = min(lo, pos);
-    hi = max(hi, pos);
+    int lo, hi;
+    key_window(p, bwd_row_position(p, r), lo, hi);
+    w.x = min(w.x, lo);
+    w.y = max(w.y, hi);
+    w.z = max(w.z, lo);
+    w.w = min(w.w, hi);
   }
-  out[t] = make_int2(lo, hi);
+  out[t] = w;
 }
 
 // ------------------------------------------------------------ shared pieces
@@ -231,15 +241,18 @@ __device__ __forceinline__ void issue_tmem_a(uint32_t d_tmem, uint32_t a_tmem, u
 
 // ------------------------------------------------------------ dK, dV
 // The query tiles a key tile sees: heads hkv*g .. hkv*g + g - 1, every tile
-// whose highest position reaches the key tile's lowest (all when not causal).
+// whose rows' key windows meet the key tile's positions [kmin, kmax] (all
+// when neither causal nor packed).
 struct QWalk {
   int idx, n, nqt, h0;
-  __device__ __forceinline__ bool next(const BwdPlan& p, int kmin, int& h, int& qt) {
+  __device__ __forceinline__ bool next(const BwdPlan& p, int kmin, int kmax, int& h, int& qt) {
     while (idx < n) {
       const int i = idx++;
       qt = i % nqt;
       h = h0 + i / nqt;
-      if (!p.causal || p.qtile_pos[qt].y >= kmin) return true;
+      if (!p.causal && p.n_docs == 0) return true;
+      const int4 w = p.qtile_pos[qt];
+      if (w.y >= kmin && w.x <= kmax) return true;
     }
     return false;
   }
@@ -287,7 +300,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkv_kernel(const __grid_co
     QWalk w{0, g * p.n_qtiles, p.n_qtiles, hkv * g};
     int h, qt, j = 0;
     bool ok = true;
-    while (ok && w.next(p, kmin, h, qt)) {
+    while (ok && w.next(p, kmin, kmax, h, qt)) {
       const int st = j & 1;
       ok = warp_wait(bb.st_empty0 + 8 * st, ((j >> 1) & 1) ^ 1, bb.abort_flag, budget, kSiteBwdEmpty);
       if (!ok) break;
@@ -300,15 +313,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkv_kernel(const __grid_co
           tma_load_4d(sDO + bx * C::kBoxBytes, &p.domap, bb.st_full0 + 8 * st, bx * 64, 128 * qt, h, b);
         }
       }
-      // per-column data of this query tile: -lse2, -delta, position
+      // per-column data of this query tile: -lse2, -delta, key window [lo, hi]
       float* aux = reinterpret_cast<float*>(gbase + C::kAux0 + st * C::kAuxBytes);
       const int64_t rowbase = (int64_t(b) * p.Hq + h) * p.Sq;
       for (int i = lane; i < 128; i += 32) {
         const int row = 128 * qt + i;
         const bool valid = row < p.Sq;
+        int lo = 0x7fffffff, hi = int(0x80000000);  // an empty window
+        if (valid) key_window(p, bwd_row_position(p, row), lo, hi);
         aux[i] = valid ? -p.lse2[rowbase + row] : -kInf;
         aux[128 + i] = valid ? -p.delta[rowbase + row] : 0.f;
-        reinterpret_cast<int*>(aux)[256 + i] = valid ? bwd_row_position(p, row) : int(0x80000000);
+        reinterpret_cast<int*>(aux)[256 + i] = hi;
+        reinterpret_cast<int*>(aux)[384 + i] = lo;
       }
       mbar_arrive(bb.st_full0 + 8 * st);
       ++j;
@@ -328,7 +344,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkv_kernel(const __grid_co
     bool ok = warp_wait(bb.res_full, 0, bb.abort_flag, budget, kSiteBwdKv);
     QWalk w{0, g * p.n_qtiles, p.n_qtiles, hkv * g};
     int h, qt, j = 0;
-    while (ok && w.next(p, kmin, h, qt)) {
+    while (ok && w.next(p, kmin, kmax, h, qt)) {
       const int st = j & 1;
       const uint32_t sQ = base + C::kStage0 + st * C::kStageBytes, sDO = sQ + C::kTileBytes;
       ok = warp_wait(bb.st_full0 + 8 * st, (j >> 1) & 1, bb.abort_flag, budget, kSiteBwdStage);
@@ -372,17 +388,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkv_kernel(const __grid_co
     QWalk w{0, g * p.n_qtiles, p.n_qtiles, hkv * g};
     int h, qt, j = 0;
     bool ok = true;
-    while (ok && w.next(p, kmin, h, qt)) {
+    while (ok && w.next(p, kmin, kmax, h, qt)) {
       const int st = j & 1;
       ok = warp_wait(bb.st_full0 + 8 * st, (j >> 1) & 1, bb.abort_flag, budget, kSiteBwdStage) &&
            warp_wait(bb.sdp_full, j & 1, bb.abort_flag, budget, kSiteBwdSdp);
       if (!ok) break;
       tc_fence_after();
       const float* aux = reinterpret_cast<const float*>(gbase + C::kAux0 + st * C::kAuxBytes);
-      const int* apos = reinterpret_cast<const int*>(aux) + 256;
-      // a mask is needed only where some key of the tile lies after some
-      // query of the query tile, or where the key tile is ragged
-      const bool masked = (p.causal && kmax > p.qtile_pos[qt].x) || kvalid < 128;
+      const int* ahi = reinterpret_cast<const int*>(aux) + 256;
+      const int* alo = reinterpret_cast<const int*>(aux) + 384;
+      // a mask is needed only where some key of the tile lies outside some
+      // row's window, or where the key tile is ragged
+      bool masked = kvalid < 128;
+      if (p.causal || p.n_docs) {
+        const int4 qw = p.qtile_pos[qt];
+        masked = masked || kmax > qw.w || kmin < qw.z;
+      }
 #pragma unroll 1
       for (int i = 2 * hw; i < 2 * hw + 2; ++i) {
         // the chunk's column data first (shared-memory broadcasts), so that
@@ -412,11 +433,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkv_kernel(const __grid_co
           f2_split(x23, x2, x3);
           float p0 = ex2(x0), p1 = ex2(x1), p2 = ex2(x2), p3 = ex2(x3);
           if (masked) {
-            const int4 qp4 = *reinterpret_cast<const int4*>(apos + 32 * i + c);
-            if (!krow_ok || (p.causal && kpos > qp4.x)) p0 = 0.f;
-            if (!krow_ok || (p.causal && kpos > qp4.y)) p1 = 0.f;
-            if (!krow_ok || (p.causal && kpos > qp4.z)) p2 = 0.f;
-            if (!krow_ok || (p.causal && kpos > qp4.w)) p3 = 0.f;
+            const int4 h4 = *reinterpret_cast<const int4*>(ahi + 32 * i + c);
+            const int4 l4 = *reinterpret_cast<const int4*>(alo + 32 * i + c);
+            if (!krow_ok || kpos > h4.x || kpos < l4.x) p0 = 0.f;
+            if (!krow_ok || kpos > h4.y || kpos < l4.y) p1 = 0.f;
+            if (!krow_ok || kpos > h4.z || kpos < l4.z) p2 = 0.f;
+            if (!krow_ok || kpos > h4.w || kpos < l4.w) p3 = 0.f;
           }
           const uint64_t t01 = add2(f2(__uint_as_float(dp[c]), __uint_as_float(dp[c + 1])), f2(del.x, del.y));
           const uint64_t t23 = add2(f2(__uint_as_float(dp[c + 2]), __uint_as_float(dp[c + 3])), f2(del.z, del.w));
@@ -500,7 +522,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
   u /= p.n_qtiles;
   const int hq = u % p.Hq, b = u / p.Hq;
   const int hkv = hq / (p.Hq / p.Hkv);
-  const int qmax = p.qtile_pos[qt].y;
+  // key positions some row of the tile may see: [wlo, whi]
+  int wlo = 0, whi = 0x7fffffff;
+  if (p.causal || p.n_docs) {
+    const int4 qw = p.qtile_pos[qt];
+    wlo = qw.x;
+    whi = qw.y;
+  }
   const uint32_t sQ = base + C::kRes0, sDO = base + C::kRes1;
 
   if (warp == 0) {
@@ -518,8 +546,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
     bool ok = true;
     for (int k = 0; ok && k < p.n_kvsegs; ++k) {
       const KvSeg& sg = p.ks[k];
-      const int nl = bwd_live_tiles(p, k, qmax);
-      for (int t = 0; t < nl; ++t) {
+      int tb, te;
+      bwd_live_tiles(p, k, wlo, whi, tb, te);
+      for (int t = tb; t < te; ++t) {
         const int st = j & 1;
         ok = warp_wait(bb.st_empty0 + 8 * st, ((j >> 1) & 1) ^ 1, bb.abort_flag, budget, kSiteBwdEmpty);
         if (!ok) break;
@@ -552,8 +581,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
     bool ok = warp_wait(bb.res_full, 0, bb.abort_flag, budget, kSiteBwdKv);
     int j = 0;
     for (int k = 0; ok && k < p.n_kvsegs; ++k) {
-      const int nl = bwd_live_tiles(p, k, qmax);
-      for (int t = 0; t < nl; ++t) {
+      int tb, te;
+      bwd_live_tiles(p, k, wlo, whi, tb, te);
+      for (int t = tb; t < te; ++t) {
         const int st = j & 1;
         const uint32_t sK = base + C::kStage0 + st * C::kStageBytes, sV = sK + C::kTileBytes;
         ok = warp_wait(bb.st_full0 + 8 * st, (j >> 1) & 1, bb.abort_flag, budget, kSiteBwdStage);
@@ -592,7 +622,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
     const int64_t srow = (int64_t(b) * p.Hq + hq) * p.Sq + grow;
     const float lse = rvalid ? p.lse2[srow] : kInf;
     const float del = rvalid ? p.delta[srow] : 0.f;
-    const int qpos = rvalid ? bwd_row_position(p, grow) : 0x7ffffffe;
+    int rlo = 0, rhi = 0x7ffffffe;  // keys this row may see: positions [rlo, rhi]
+    if (rvalid) key_window(p, bwd_row_position(p, grow), rlo, rhi);
     const uint32_t lane_off = uint32_t(sub * 32) << 16;
     const uint32_t tS = tmem + lane_off, tP = tmem + 128 + lane_off, tdQ = tmem + 256 + lane_off;
     const uint64_t c2x2 = f2(p.scale_log2, p.scale_log2), nlse = f2(-lse, -lse), ndel = f2(-del, -del);
@@ -600,13 +631,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
     bool ok = true;
     for (int k = 0; ok && k < p.n_kvsegs; ++k) {
       const KvSeg& sg = p.ks[k];
-      const int nl = bwd_live_tiles(p, k, qmax);
-      for (int t = 0; t < nl; ++t) {
-        // visible keys of this row: a prefix [0, L) of the key tile
-        int L = min(128, sg.len - 128 * t);
-        if (p.causal) {
+      int tb, te;
+      bwd_live_tiles(p, k, wlo, whi, tb, te);
+      for (int t = tb; t < te; ++t) {
+        // visible keys of this row: the range [C0, L) of the key tile
+        int L = min(128, sg.len - 128 * t), C0 = 0;
+        if (p.causal || p.n_docs) {
           const int first = sg.pos0 + sg.step * (128 * t);
-          L = qpos < first ? 0 : min(L, (qpos - first) / sg.step + 1);
+          L = rhi < first ? 0 : min(L, (rhi - first) / sg.step + 1);
+          if (rlo > first) C0 = min(L, (rlo - first - 1) / sg.step + 1);
         }
         ok = warp_wait(bb.sdp_full, j & 1, bb.abort_flag, budget, kSiteBwdSdp);
         if (!ok) break;
@@ -627,10 +660,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
 #pragma unroll
           for (int q = 0; q < 2; ++q) {
             const int i = 2 * hh + q;
-            if (L < 128) {
+            if (L < 128 || C0 > 0) {
 #pragma unroll
               for (int c = 0; c < 32; ++c)
-                if (32 * i + c >= L) s[q][c] = 0xff800000u;  // -inf: p = 0
+                if (32 * i + c >= L || 32 * i + c < C0) s[q][c] = 0xff800000u;  // -inf: p = 0
             }
             uint32_t pd[16];
 #pragma unroll
@@ -692,7 +725,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
 template <int D>
 int launch_bwd_d(const BwdPlan& plan, const void* o, int o_fp32, int64_t o_sb, int64_t o_sh,
                  int64_t o_sr, const void* dout, const float* m, const float* l, float* lse2,
-                 float* delta, int2* qtile_pos, void* stream) {
+                 float* delta, int4* qtile_pos, void* stream) {
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   const int64_t rows = int64_t(plan.B) * plan.Hq * plan.Sq;
   bwd_prep_kernel<<<unsigned((rows + 127) / 128), 128, 0, cs>>>(
@@ -726,7 +759,7 @@ int launch_bwd_d(const BwdPlan& plan, const void* o, int o_fp32, int64_t o_sb, i
 
 int launch_bwd_bf16(const BwdPlan& plan, int D, const void* o, int o_fp32, int64_t o_sb,
                     int64_t o_sh, int64_t o_sr, const void* dout, const float* m,
-                    const float* l, float* lse2, float* delta, int2* qtile_pos, void* stream) {
+                    const float* l, float* lse2, float* delta, int4* qtile_pos, void* stream) {
   return D == 128 ? launch_bwd_d<128>(plan, o, o_fp32, o_sb, o_sh, o_sr, dout, m, l, lse2, delta,
                                       qtile_pos, stream)
                   : launch_bwd_d<64>(plan, o, o_fp32, o_sb, o_sh, o_sr, dout, m, l, lse2, delta,

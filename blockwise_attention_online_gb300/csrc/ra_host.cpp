@@ -82,6 +82,8 @@ struct Common {
   int64_t B, Hq, Hkv, D, Sq;
   int dtype, causal;
   float scale;
+  int n_docs;                        // 0: no document mask
+  std::vector<int32_t> doc_bounds;   // n_docs + 1 boundaries
   std::vector<Span> qspans;   // query pieces, owner = segment
   std::vector<Span> kvspans;  // key/value pieces, owner = chunk (row0 within chunk)
   std::vector<int> chunk_begin;  // kvspans of chunk c: [begin[c], begin[c+1])
@@ -92,6 +94,34 @@ struct Common {
 ra_status check_strides(const ra_strides& s, const char* what) {
   if (s.batch < 0 || s.head < 0 || s.row < 0)
     return fail(RA_ERR_INVALID, "%s: negative stride", what);
+  return RA_OK;
+}
+
+// Document boundaries: strictly increasing, inside [0, 2^31 - 1], and every
+// query and key position inside [b_0, b_n).
+ra_status check_docs(const ra_problem& p, Common* c) {
+  c->n_docs = 0;
+  c->doc_bounds.clear();
+  if (p.reserved_docs != 0) return fail(RA_ERR_INVALID, "reserved_docs must be 0");
+  if (p.n_docs == 0) return RA_OK;
+  if (p.n_docs < 0 || p.n_docs > RA_MAX_DOCS)
+    return fail(RA_ERR_INVALID, "n_docs=%d not in [0,%d]", p.n_docs, RA_MAX_DOCS);
+  if (!p.doc_bounds) return fail(RA_ERR_INVALID, "doc_bounds is NULL");
+  for (int32_t d = 0; d <= p.n_docs; ++d) {
+    const int64_t b = p.doc_bounds[d];
+    if (b < 0 || b > kPosLimit)
+      return fail(RA_ERR_INVALID, "doc_bounds[%d]=%lld outside [0, 2^31-1]", d, (long long)b);
+    if (d > 0 && b <= p.doc_bounds[d - 1])
+      return fail(RA_ERR_INVALID, "doc_bounds must increase strictly (index %d)", d);
+    c->doc_bounds.push_back(int32_t(b));
+  }
+  const int64_t b0 = p.doc_bounds[0], bn = p.doc_bounds[p.n_docs];
+  for (const std::vector<Span>* v : {&c->qspans, &c->kvspans})
+    for (const Span& sp : *v)
+      if (sp.pos0 < b0 || sp.pos0 + sp.step * (sp.len - 1) >= bn)
+        return fail(RA_ERR_INVALID, "a position lies outside the documents [%lld, %lld)",
+                    (long long)b0, (long long)bn);
+  c->n_docs = p.n_docs;
   return RA_OK;
 }
 
@@ -140,7 +170,7 @@ ra_status validate(const ra_problem* pb, const void* q, const ra_q_segment* segs
     int64_t r = row;
     for (int k = 0; k < segs[s].pos.nspan; ++k) {
       const ra_span& sp = segs[s].pos.span[k];
-      if (sp.len > 0) c->qspans.push_back({r, sp.len, sp.pos0, sp.step, s});
+      if (sp.len > 0) c->qspans.push_back({r, sp.len, sp.pos0, sp.len > 1 ? sp.step : 1, s});
       r += sp.len;
     }
     row += segs[s].len;
@@ -161,7 +191,7 @@ ra_status validate(const ra_problem* pb, const void* q, const ra_q_segment* segs
       int64_t r = 0;
       for (int s = 0; s < ch.pos.nspan; ++s) {
         const ra_span& sp = ch.pos.span[s];
-        if (sp.len > 0) c->kvspans.push_back({r, sp.len, sp.pos0, sp.step, k});
+        if (sp.len > 0) c->kvspans.push_back({r, sp.len, sp.pos0, sp.len > 1 ? sp.step : 1, k});
         r += sp.len;
       }
     }
@@ -170,29 +200,37 @@ ra_status validate(const ra_problem* pb, const void* q, const ra_q_segment* segs
   if ((int64_t)c->qspans.size() > ra::kMaxQPieces)
     return fail(RA_ERR_UNSUPPORTED, "%zu query spans exceed the limit of %d",
                 c->qspans.size(), ra::kMaxQPieces);
-  return RA_OK;
+  return check_docs(p, c);
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// Highest position over query rows [r0, r1) (spans are sorted by row).
-int64_t qmax_of_rows(const std::vector<Span>& qs, int64_t r0, int64_t r1) {
-  int64_t best = -1;
+// Lowest and highest position over query rows [r0, r1) (spans are sorted by
+// row).
+void qrange_of_rows(const std::vector<Span>& qs, int64_t r0, int64_t r1, int64_t* qmin,
+                    int64_t* qmax) {
+  *qmin = kPosLimit;
+  *qmax = -1;
   for (const Span& s : qs) {
     int64_t a = std::max(r0, s.row0), b = std::min(r1, s.row0 + s.len);
-    if (a < b) best = std::max(best, s.pos0 + s.step * (b - 1 - s.row0));
+    if (a < b) {
+      *qmin = std::min(*qmin, s.pos0 + s.step * (a - s.row0));
+      *qmax = std::max(*qmax, s.pos0 + s.step * (b - 1 - s.row0));
+    }
   }
-  return best;
 }
 
-// Key tiles of a span (128 rows each) that are not entirely in the future of
-// a query whose highest position is qmax.
-int64_t live_tiles(const Span& kv, int64_t qmax, bool causal) {
-  int64_t nt = (kv.len + 127) / 128;
-  if (!causal) return nt;
-  if (qmax < kv.pos0) return 0;
-  int64_t last = (qmax - kv.pos0) / kv.step;  // last visible row index in span
-  return std::min(nt, last / 128 + 1);
+// Key tiles of a span (128 rows each) holding a position that some query in
+// the position range [qmin, qmax] may see: the same count as the kernels'
+// tile walk (both use ra::key_window and ra::live_range).
+int64_t live_tiles(const Common& c, const Span& kv, int64_t qmin, int64_t qmax) {
+  if (!c.causal && c.n_docs == 0) return (kv.len + 127) / 128;
+  int lo, hi, unused;
+  ra::key_window(c, int(qmin), lo, unused);
+  ra::key_window(c, int(qmax), unused, hi);
+  int tb, te;
+  ra::live_range(int(kv.pos0), int(kv.step), int(kv.len), lo, hi, tb, te);
+  return te - tb;
 }
 
 // ----------------------------------------------------------- tensor maps
@@ -303,6 +341,11 @@ ra_status lib_pool(cudaMemPool_t* out) {
 // inputs here). Empty for the device-pointer entry points.
 using BeforeLaunch = std::function<ra_status()>;
 
+void fill_docs(const Common& c, int32_t* bounds, int32_t* n) {
+  *n = c.n_docs;
+  for (size_t i = 0; i < c.doc_bounds.size(); ++i) bounds[i] = c.doc_bounds[i];
+}
+
 void fill_q_pieces(const Common& c, ra::QPiece* qp, int32_t* n) {
   *n = (int32_t)c.qspans.size();
   for (size_t i = 0; i < c.qspans.size(); ++i) {
@@ -376,6 +419,7 @@ ra_status run_tc(const Common& c, const ra_problem& p, const void* q,
   plan.scale_log2 = float(double(c.scale) * 1.4426950408889634);
   plan.o_fp32 = out_f32 ? 1 : 0;
   fill_q_pieces(c, plan.qp, &plan.n_qpieces);
+  fill_docs(c, plan.doc_bounds, &plan.n_docs);
   plan.n_kvsegs = int32_t(c.kvspans.size());
   for (size_t i = 0; i < c.kvspans.size(); ++i) {
     const Span& s = c.kvspans[i];
@@ -396,14 +440,16 @@ ra_status run_tc(const Common& c, const ra_problem& p, const void* q,
   std::vector<int64_t> work(npairs, 0);
   for (int64_t qp = 0; qp < npairs; ++qp) {
     int64_t r0 = qp * ra::kTcRowsPerUnit, r1 = std::min(c.Sq, r0 + ra::kTcRowsPerUnit);
-    int64_t qmax = qmax_of_rows(c.qspans, r0, r1);
-    for (const Span& kv : c.kvspans) work[qp] += live_tiles(kv, qmax, c.causal != 0);
+    int64_t qmin, qmax;
+    qrange_of_rows(c.qspans, r0, r1, &qmin, &qmax);
+    for (const Span& kv : c.kvspans) work[qp] += live_tiles(c, kv, qmin, qmax);
   }
-  // visit order of the pairs: longest first when the work differs (causal)
+  // visit order of the pairs: longest first when the work differs (causal,
+  // documents)
   std::vector<int32_t> order(npairs);
   std::iota(order.begin(), order.end(), 0);
   plan.has_order = 0;
-  if (npairs <= ra::kTcMaxOrder && c.causal) {
+  if (npairs <= ra::kTcMaxOrder && (c.causal || c.n_docs > 0)) {
     std::stable_sort(order.begin(), order.end(),
                      [&](int32_t a, int32_t b) { return work[a] > work[b]; });
     for (int64_t i = 0; i < npairs; ++i) plan.order[i] = uint16_t(order[i]);
@@ -511,6 +557,7 @@ ra_status run_simt(const Common& c, const ra_problem& p, const void* q,
   plan.ring = c.ring ? 1 : 0; plan.n_chunks = c.nchunks;
   plan.scale = c.scale;
   fill_q_pieces(c, plan.qp, &plan.n_qpieces);
+  fill_docs(c, plan.doc_bounds, &plan.n_docs);
   plan.n_kvsegs = int32_t(c.kvspans.size());
   for (size_t i = 0; i < c.kvspans.size(); ++i) {
     const Span& s = c.kvspans[i];
@@ -627,6 +674,7 @@ ra_status run_bwd(const ra_problem* pb, const void* q, const ra_q_segment* segs,
   plan.scale = c.scale;
   plan.scale_log2 = float(double(c.scale) * 1.4426950408889634);
   fill_q_pieces(c, plan.qp, &plan.n_qpieces);
+  fill_docs(c, plan.doc_bounds, &plan.n_docs);
   plan.n_kvsegs = int32_t(c.kvspans.size());
   int32_t tiles = 0;
   for (size_t i = 0; i < c.kvspans.size(); ++i) {
@@ -643,10 +691,10 @@ ra_status run_bwd(const ra_problem* pb, const void* q, const ra_q_segment* segs,
       int64_t(plan.n_qtiles) * c.Hq * c.B > (int64_t(1) << 31) - 1)
     return fail(RA_ERR_UNSUPPORTED, "too many tiles for one launch");
 
-  // per query row: lse2, delta; per query tile: position range
+  // per query row: lse2, delta; per query tile: key window bounds
   const size_t rows = size_t(c.B * c.Hq * c.Sq);
   auto up = [](size_t n) { return (n + 255) & ~size_t(255); };
-  const size_t bytes = 2 * up(rows * 4) + up(size_t(plan.n_qtiles) * 8);
+  const size_t bytes = 2 * up(rows * 4) + up(size_t(plan.n_qtiles) * 16);
   cudaMemPool_t pool = nullptr;
   if ((st = lib_pool(&pool)) != RA_OK) return st;
   char* scratch = nullptr;
@@ -654,7 +702,7 @@ ra_status run_bwd(const ra_problem* pb, const void* q, const ra_q_segment* segs,
   if (e != cudaSuccess) return cuda_status(e, "allocating backward scratch");
   float* lse2 = reinterpret_cast<float*>(scratch);
   float* delta = reinterpret_cast<float*>(scratch + up(rows * 4));
-  int2* qtile_pos = reinterpret_cast<int2*>(scratch + 2 * up(rows * 4));
+  int4* qtile_pos = reinterpret_cast<int4*>(scratch + 2 * up(rows * 4));
   plan.lse2 = lse2;
   plan.delta = delta;
   plan.qtile_pos = qtile_pos;
@@ -849,7 +897,7 @@ ra_status ra_segment_work(const ra_problem* problem, const ra_q_segment* segs, i
     int64_t r = 0;
     for (int s = 0; s < chunks[k].pos.nspan; ++s) {
       const ra_span& sp = chunks[k].pos.span[s];
-      if (sp.len > 0) kv.push_back({r, sp.len, sp.pos0, sp.step, k});
+      if (sp.len > 0) kv.push_back({r, sp.len, sp.pos0, sp.len > 1 ? sp.step : 1, k});
       r += sp.len;
     }
   }
@@ -862,10 +910,18 @@ ra_status ra_segment_work(const ra_problem* problem, const ra_q_segment* segs, i
       int64_t acc = 0;
       for (int64_t i = 0; i < qs.len; ++i) {
         int64_t pq = qs.pos0 + qs.step * i;
+        if (!c.causal && c.n_docs == 0) {
+          for (const Span& ks : kv) acc += ks.len;
+          continue;
+        }
+        int lo, hi;
+        ra::key_window(c, int(pq), lo, hi);
         for (const Span& ks : kv) {
-          if (!c.causal) { acc += ks.len; continue; }
-          if (pq < ks.pos0) continue;
-          acc += std::min(ks.len, (pq - ks.pos0) / ks.step + 1);
+          // rows with lo <= pos0 + step * r <= hi
+          if (hi < ks.pos0) continue;
+          const int64_t r_hi = std::min(ks.len - 1, (hi - ks.pos0) / ks.step);
+          const int64_t r_lo = lo <= ks.pos0 ? 0 : (lo - ks.pos0 - 1) / ks.step + 1;
+          if (r_hi >= r_lo) acc += r_hi - r_lo + 1;
         }
       }
       pairs[qs.owner] += acc;
@@ -875,12 +931,13 @@ ra_status ra_segment_work(const ra_problem* problem, const ra_q_segment* segs, i
     const int64_t npairs = (c.Sq + ra::kTcRowsPerUnit - 1) / ra::kTcRowsPerUnit;
     for (int64_t qp = 0; qp < npairs; ++qp) {
       int64_t r0 = qp * ra::kTcRowsPerUnit, r1 = std::min(c.Sq, r0 + ra::kTcRowsPerUnit);
-      int64_t qmax = qmax_of_rows(c.qspans, r0, r1);
+      int64_t qmin, qmax;
+      qrange_of_rows(c.qspans, r0, r1, &qmin, &qmax);
       int owner = 0;
       for (const Span& qs : c.qspans)
         if (r0 >= qs.row0 && r0 < qs.row0 + qs.len) owner = qs.owner;
       int64_t n = 0;
-      for (const Span& ks : kv) n += live_tiles(ks, qmax, c.causal != 0);
+      for (const Span& ks : kv) n += live_tiles(c, ks, qmin, qmax);
       tiles[owner] += 2 * n;
     }
   }

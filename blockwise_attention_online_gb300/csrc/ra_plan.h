@@ -24,6 +24,51 @@ struct KvSeg {
 };
 
 constexpr int kMaxQPieces = 64;
+constexpr int kMaxDocs = 512;
+
+#if defined(__CUDACC__)
+#define RA_HD __host__ __device__ __forceinline__
+#else
+#define RA_HD inline
+#endif
+
+// Packed documents: a plan with n_docs > 0 holds boundaries b_0 < ... < b_n
+// (doc_bounds[0 .. n_docs]); document d is the position range [b_d, b_{d+1})
+// and a query sees only keys of its own document. The window of a query at
+// position pos is the key positions [lo, hi] it may see: its document (all
+// positions when there are no documents), cut at pos itself when causal.
+// Every plan type below carries the same three members used here.
+template <class Plan>
+RA_HD void key_window(const Plan& p, int pos, int& lo, int& hi) {
+  lo = 0;
+  hi = p.causal ? pos : 0x7fffffff;
+  if (p.n_docs > 0) {
+    int a = 0, z = p.n_docs - 1;  // last d with b_d <= pos
+    while (a < z) {
+      const int mid = (a + z + 1) >> 1;
+      if (p.doc_bounds[mid] <= pos) a = mid; else z = mid - 1;
+    }
+    lo = p.doc_bounds[a];
+    if (!p.causal) hi = p.doc_bounds[a + 1] - 1;
+  }
+}
+
+// Tiles [tb, te) of a monotone key span (positions pos0 + step * i, len rows,
+// 128-row tiles) that hold at least one position inside [lo, hi]. The host
+// (work estimates) and the kernels (tile walks) share this arithmetic, so
+// both count the same tiles.
+RA_HD void live_range(int pos0, int step, int len, int lo, int hi, int& tb, int& te) {
+  const int nt = (len + 127) / 128;
+  if (hi < pos0 || len <= 0) { tb = te = 0; return; }
+  const long long last = (static_cast<long long>(hi) - pos0) / step;  // last row with pos <= hi
+  te = last / 128 + 1 < nt ? static_cast<int>(last / 128 + 1) : nt;
+  tb = 0;
+  if (lo > pos0) {
+    const long long first = (static_cast<long long>(lo) - pos0 + step - 1) / step;  // first row with pos >= lo
+    tb = first >= len ? nt : static_cast<int>(first / 128);
+  }
+  if (tb > te) tb = te;
+}
 
 // ---------------------------------------------------------------- bf16 path
 constexpr int kTcMaxChunks = 32;
@@ -67,6 +112,8 @@ struct alignas(128) TcPlan {
   int32_t chunk_seg_begin[kTcMaxChunks + 1];
   QPiece qp[kMaxQPieces];
   KvSeg ks[kTcMaxKvSegs];
+  int32_t n_docs;                    // 0: no document mask
+  int32_t doc_bounds[kMaxDocs + 1];
   uint16_t order[kTcMaxOrder];       // q-pair visit order (longest first)
 };
 static_assert(sizeof(TcPlan) <= 32000, "bf16 plan must fit the parameter space");
@@ -85,7 +132,8 @@ struct alignas(128) BwdPlan {
   CUtensorMap vmap[kTcMaxChunks];    // V chunk c
   const float* lse2;                 // [B, Hq, Sq]; +inf where the row sees no key
   const float* delta;                // [B, Hq, Sq]
-  const int2* qtile_pos;             // [n_qtiles]: lowest, highest position of its rows
+  const int4* qtile_pos;             // [n_qtiles]: key windows of its rows: lowest lo,
+                                     // highest hi, highest lo, lowest hi
   float* dq;                         // [B, Hq, Sq, D] fp32, dense
   float* dk[kTcMaxChunks];           // [B, Hkv, len_c, D] fp32, dense
   float* dv[kTcMaxChunks];
@@ -98,6 +146,8 @@ struct alignas(128) BwdPlan {
   int32_t kseg_tile_begin[kTcMaxKvSegs + 1];  // first global key tile of span i
   QPiece qp[kMaxQPieces];
   KvSeg ks[kTcMaxKvSegs];
+  int32_t n_docs;                             // 0: no document mask
+  int32_t doc_bounds[kMaxDocs + 1];
 };
 static_assert(sizeof(BwdPlan) <= 32000, "backward plan must fit the parameter space");
 
@@ -125,6 +175,8 @@ struct SimtPlan {
   QPiece qp[kMaxQPieces];
   KvSeg ks[kSimtMaxKvSegs];
   SimtChunk ch[kSimtMaxChunks];
+  int32_t n_docs;                    // 0: no document mask
+  int32_t doc_bounds[kMaxDocs + 1];
 };
 static_assert(sizeof(SimtPlan) <= 32000, "fp32 plan must fit the parameter space");
 
@@ -148,7 +200,7 @@ int read_and_clear_device_error(int* code);
 // then the dK/dV and dQ kernels; all on `stream`.
 int launch_bwd_bf16(const BwdPlan& plan, int D, const void* o, int o_fp32, int64_t o_sb,
                     int64_t o_sh, int64_t o_sr, const void* dout, const float* m,
-                    const float* l, float* lse2, float* delta, int2* qtile_pos, void* stream);
+                    const float* l, float* lse2, float* delta, int4* qtile_pos, void* stream);
 int read_and_clear_bwd_error(int* code);
 
 }  // namespace ra

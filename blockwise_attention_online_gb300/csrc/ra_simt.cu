@@ -46,13 +46,14 @@ __global__ void __launch_bounds__(kRows * kParts) simt_ring_kernel(const __grid_
   const bool rvalid = grow < p.Sq;
   const int D = p.D;
 
-  int qpos = 0x7ffffffe, qseg = 0;
+  // keys this row may see: positions [rlo, rhi]
+  int rlo = 0, rhi = 0x7ffffffe, qseg = 0;
   {
     const int first = find_piece(p, row0);
     qseg = p.qp[first].seg;
     if (rvalid) {
       const QPiece& pc = p.qp[find_piece(p, grow)];
-      qpos = pc.pos0 + pc.step * (grow - pc.row0);
+      key_window(p, pc.pos0 + pc.step * (grow - pc.row0), rlo, rhi);
     }
   }
 
@@ -95,7 +96,7 @@ __global__ void __launch_bounds__(kRows * kParts) simt_ring_kernel(const __grid_
           acc += __shfl_xor_sync(0xffffffffu, acc, 1);
           acc += __shfl_xor_sync(0xffffffffu, acc, 2);
           const int kpos = sg.pos0 + sg.step * (t0 + j);
-          const bool vis = j < nk && (!p.causal || kpos <= qpos);
+          const bool vis = j < nk && kpos >= rlo && kpos <= rhi;
           sc[j] = vis ? acc * p.scale : kNegInf;
           tmax = fmaxf(tmax, sc[j]);
         }

@@ -90,7 +90,8 @@ enum : int {
 };
 
 struct Unit {
-  int b, hq, hkv, qrow0, qseg, qmax, n;
+  int b, hq, hkv, qrow0, qseg, n;
+  int lo, hi;  // key positions any row of the unit may see: [lo, hi]
 };
 
 __device__ __forceinline__ int find_piece(const TcPlan& p, int row) {
@@ -107,12 +108,16 @@ __device__ __forceinline__ int row_position(const TcPlan& p, int row) {
   return q.pos0 + q.step * (row - q.row0);
 }
 
-// Key tiles of span k that are not entirely in the future of position qmax.
-__device__ __forceinline__ int live_tiles(const TcPlan& p, int k, int qmax) {
+// Key tiles [tb, te) of span k that hold a position some row of the unit
+// may see (not entirely in its future, nor outside its documents).
+__device__ __forceinline__ void live_tiles(const TcPlan& p, int k, const Unit& U, int& tb, int& te) {
   const KvSeg& s = p.ks[k];
-  if (!p.causal) return s.ntiles;
-  if (qmax < s.pos0) return 0;
-  return min(s.ntiles, ((qmax - s.pos0) / s.step) / 128 + 1);
+  if (!p.causal && p.n_docs == 0) {
+    tb = 0;
+    te = s.ntiles;
+    return;
+  }
+  live_range(s.pos0, s.step, s.len, U.lo, U.hi, tb, te);
 }
 
 __device__ __forceinline__ void decode_unit(const TcPlan& p, int u, Unit& U) {
@@ -126,20 +131,29 @@ __device__ __forceinline__ void decode_unit(const TcPlan& p, int u, Unit& U) {
   const int r1 = min(U.qrow0 + kTcRowsPerUnit, p.Sq);
   int i = find_piece(p, U.qrow0);
   U.qseg = p.qp[i].seg;
-  int qmax = -1;
+  int qmin = 0x7fffffff, qmax = -1;
   for (; i < p.n_qpieces && p.qp[i].row0 < r1; ++i) {
     const QPiece& q = p.qp[i];
-    const int e = min(r1, q.row0 + q.len);
+    const int a = max(U.qrow0, q.row0), e = min(r1, q.row0 + q.len);
+    qmin = min(qmin, q.pos0 + q.step * (a - q.row0));
     qmax = max(qmax, q.pos0 + q.step * (e - 1 - q.row0));
   }
-  U.qmax = qmax;
+  // the windows grow with the position: the lowest row bounds lo, the highest hi
+  int unused;
+  key_window(p, qmin, U.lo, unused);
+  key_window(p, qmax, unused, U.hi);
   int n = 0;
-  for (int k = 0; k < p.n_kvsegs; ++k) n += live_tiles(p, k, qmax);
+  for (int k = 0; k < p.n_kvsegs; ++k) {
+    int tb, te;
+    live_tiles(p, k, U, tb, te);
+    n += te - tb;
+  }
   U.n = n;
 }
 
 // Walks the live key tiles of a unit: chunks in ring order, spans in order,
-// tiles in order. Every warp role runs the same walk.
+// tiles in order. Every warp role runs the same walk. `t` is the tile index
+// within the span, `nlive` one past the span's last live tile.
 struct TileIter {
   int s, ks, ks_end, t, nlive;
   __device__ __forceinline__ TileIter() : s(-1), ks(0), ks_end(0), t(0), nlive(0) {}
@@ -155,8 +169,7 @@ struct TileIter {
       }
       ++ks;
       if (ks < ks_end) {
-        t = 0;
-        nlive = live_tiles(p, ks, U.qmax);
+        live_tiles(p, ks, U, t, nlive);
         continue;
       }
       if (++s >= p.n_chunks) return;
@@ -176,8 +189,7 @@ struct TileIter {
       }
       ++ks;
       if (ks < ks_end) {
-        t = 0;
-        nlive = live_tiles(p, ks, U.qmax);
+        live_tiles(p, ks, U, t, nlive);
         continue;
       }
       if (++s >= p.n_chunks) return false;
@@ -548,22 +560,25 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ring_kernel(const __grid_const
       const int n = (I.t1 < 0 ? U.n : I.t1) - I.t0;
       const int grow = U.qrow0 + wg * 128 + r;
       const bool rvalid = grow < p.Sq;
-      const int qpos = rvalid ? row_position(p, grow) : 0x7ffffffe;
+      // keys this row may see: positions [rlo, rhi]
+      int rlo = 0, rhi = 0x7ffffffe;
+      if (rvalid) key_window(p, row_position(p, grow), rlo, rhi);
       float m_ref = kNegInf, mx = kNegInf, l = 0.f, lr = 0.f;
       if (n > 0) {
         TileIter iter;
         iter.seek(p, U, I.t0);
         int ks, t;
         for (int j = 0; j < n && iter.next(p, U, ks, t); ++j) {
-          // visible columns of this row: a prefix [0, L) of the tile (known
-          // before S arrives)
-          int L;
+          // visible columns of this row: the range [C0, L) of the tile (known
+          // before S arrives; C0 > 0 only where a document starts inside it)
+          int L, C0 = 0;
           {
             const KvSeg& sg = p.ks[ks];
             L = min(128, sg.len - 128 * t);
-            if (p.causal) {
+            if (p.causal || p.n_docs) {
               const int first = sg.pos0 + sg.step * (128 * t);
-              L = qpos < first ? 0 : min(L, (qpos - first) / sg.step + 1);
+              L = rhi < first ? 0 : min(L, (rhi - first) / sg.step + 1);
+              if (rlo > first) C0 = min(L, (rlo - first - 1) / sg.step + 1);
             }
           }
           ok = warp_wait(b_sfull, sc & 1, abort_flag, budget, kSiteSoftS);
@@ -583,12 +598,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ring_kernel(const __grid_const
             tmem_ld_wait();
 #pragma unroll
             for (int i = 0; i < 4; ++i) reg_fence(s[i]);
-            if (L < 128) {
+            if (L < 128 || C0 > 0) {
 #pragma unroll
               for (int i = 0; i < 4; ++i)
 #pragma unroll
                 for (int c = 0; c < 32; ++c)
-                  if (32 * i + c >= L) s[i][c] = 0xff800000u;  // -inf
+                  if (32 * i + c >= L || 32 * i + c < C0) s[i][c] = 0xff800000u;  // -inf
             }
 #pragma unroll
             for (int i = 0; i < 4; ++i)
@@ -637,10 +652,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ring_kernel(const __grid_const
             tmem_ld32(tS + 32 * i, s);
             tmem_ld_wait();
             reg_fence(s);
-            if (L < 128) {
+            if (L < 128 || C0 > 0) {
 #pragma unroll
               for (int c = 0; c < 32; ++c)
-                if (32 * i + c >= L) s[c] = 0xff800000u;  // -inf
+                if (32 * i + c >= L || 32 * i + c < C0) s[c] = 0xff800000u;  // -inf
             }
             uint32_t pk[16];
 #pragma unroll

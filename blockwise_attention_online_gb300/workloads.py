@@ -15,6 +15,7 @@ from __future__ import annotations
 import math
 from dataclasses import dataclass
 
+import numpy as np
 import torch
 
 
@@ -95,6 +96,19 @@ def make_qkv(w: Workload, device="cpu", S: int | None = None, seed: int | None =
         out.append(t.to(w.torch_dtype))
         del t
     return tuple(out)
+
+
+def packed_documents(S: int, seed: int, mean_len: int, min_len: int = 1) -> list[int]:
+    """Boundaries b_0 = 0 < b_1 < ... < b_n = S of packed documents whose
+    lengths are drawn log-uniformly in [min_len, 4 * mean_len) with ``seed``
+    (many short documents, a few long ones; the last is cut at S)."""
+    rng = np.random.default_rng(seed)
+    hi = max(min_len + 1, 4 * mean_len)
+    b = [0]
+    while b[-1] < S:
+        n = int(np.exp(rng.uniform(np.log(min_len), np.log(hi))))
+        b.append(min(S, b[-1] + max(min_len, n)))
+    return b
 
 
 def scalar_two_shards():

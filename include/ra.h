@@ -33,6 +33,10 @@
  * - Causal masking uses GLOBAL positions ([BLOG] "Causal masks depend on
  *   global positions"): key j is visible to query i iff pos(j) <= pos(i).
  *   Positions are described per chunk / query segment by spans.
+ * - Packed documents (optional, ra_problem.doc_bounds): several variable-
+ *   length sequences share one position range; a query sees only the keys of
+ *   its own document, causal or not. The pages do not discuss packing: this
+ *   is the plainest extension of the global-position mask.
  * - A row that sees no key gets O = 0 (or u = 0), l = 0, m = -inf.
  * - dtype RA_BF16: Q, K, V and O are bfloat16; products are accumulated in
  *   fp32 on the tensor cores; head_dim must be 64, 96 or 128.
@@ -59,6 +63,7 @@ typedef enum {
 typedef enum { RA_F32 = 0, RA_BF16 = 1 } ra_dtype;
 
 #define RA_MAX_SPANS 4
+#define RA_MAX_DOCS 512
 
 /* Rows [r, r + len) of a chunk / segment have global positions
  * pos0, pos0 + step, ..., pos0 + (len - 1) * step.  step >= 1. */
@@ -115,6 +120,17 @@ typedef struct {
                                rounding of up to 2^-9 relative.) */
   ra_strides q_strides;     /* Q: [B, Hq, Sq, D] */
   ra_strides o_strides;     /* O (ring) or u (chunk stats): [B, Hq, Sq, D] */
+  /* Packed documents. n_docs = 0: one document holds every position and
+     doc_bounds is ignored. n_docs in 1..RA_MAX_DOCS: doc_bounds is a HOST
+     array of n_docs + 1 strictly increasing positions b_0 < ... < b_n (read
+     during the call only); document d holds positions [b_d, b_{d+1}) and key
+     j is visible to query i only if both lie in the same document (and, when
+     causal, pos(j) <= pos(i)). Every query and key position must lie in
+     [b_0, b_n) (else RA_ERR_INVALID). The same documents apply to every batch
+     element and head. */
+  const int64_t* doc_bounds;
+  int32_t n_docs;
+  int32_t reserved_docs;    /* must be 0 */
 } ra_problem;
 
 /*
@@ -335,7 +351,7 @@ const char* ra_last_error(void);
 /* ABI version of this header: 10000 * major + 100 * minor + patch. */
 int32_t ra_version(void);
 
-#define RA_VERSION 100
+#define RA_VERSION 101
 
 #ifdef __cplusplus
 }

@@ -73,7 +73,7 @@ def assert_bf16(O, m, l, Oref, mref, lref, what=""):
     return err
 
 
-def layout_run(q, k, v, P, kind, causal, scale=None, out_dtype=None):
+def layout_run(q, k, v, P, kind, causal, scale=None, out_dtype=None, docs=None):
     """Shard global-order q, k, v per ``kind`` over P virtual ranks, run the
     library's ring kernel, return O, m, l back in global order."""
     S = k.shape[2]
@@ -83,7 +83,7 @@ def layout_run(q, k, v, P, kind, causal, scale=None, out_dtype=None):
     qs = torch.cat(layouts.shard(q, kind, P), dim=2).contiguous()
     segs = [(S // P, s) for s in rs]       # as many segments as chunks: ring order
     O, m, l = ring_attention(qs, kc, vc, chunk_spans=rs, q_segments=segs, causal=causal,
-                             scale=scale, out_dtype=out_dtype)
+                             scale=scale, out_dtype=out_dtype, docs=docs)
     O = layouts.to_global(O, kind, P)
     m = layouts.to_global(m.unsqueeze(-1), kind, P).squeeze(-1)
     l = layouts.to_global(l.unsqueeze(-1), kind, P).squeeze(-1)
@@ -123,12 +123,13 @@ class LazyHeads:
         return self.t[idx].float().cpu().numpy()
 
 
-def oracle_rows(q, k, v, causal, scale, heads, rows):
+def oracle_rows(q, k, v, causal, scale, heads, rows, docs=None):
     """fp64 oracle on sampled (head, row) pairs of global-order q, k, v."""
     q, k, v = LazyHeads(q), LazyHeads(k), LazyHeads(v)
     S = k.shape[2]
     pos = np.arange(S)
     trip = [(0, h, i) for h in heads for i in rows]
-    O, M, L = oracle.attention_rows(q, k, v, np.arange(q.shape[2]), pos, causal, scale, trip)
+    O, M, L = oracle.attention_rows(q, k, v, np.arange(q.shape[2]), pos, causal, scale, trip,
+                                    docs=docs)
     n = len(rows)
     return (O.reshape(len(heads), n, -1), M.reshape(len(heads), n), L.reshape(len(heads), n))

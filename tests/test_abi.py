@@ -29,7 +29,7 @@ def test_library_exports_every_header_symbol():
     assert set(declared) == set(_lib.EXPORTED)
     for name in declared:
         assert hasattr(lib, name), name
-    assert lib.ra_version() == 100
+    assert lib.ra_version() == 101
 
 
 def _problem(**kw):
@@ -150,6 +150,53 @@ def test_segment_work_is_exact(kind, causal):
     assert all(t * 128 * 128 >= pr for t, pr in zip(tiles, pairs))
     if causal and kind == "zigzag":
         assert max(pairs) == min(pairs)
+
+
+@pytest.mark.parametrize("kind", ["contiguous", "zigzag", "striped"])
+@pytest.mark.parametrize("causal", [False, True])
+def test_segment_work_with_documents_is_exact(kind, causal):
+    """Packed documents: visible pairs per virtual rank bit-exact against the
+    oracle's count; the scheduled tiles cover them and never exceed the
+    unpacked schedule."""
+    n, P = 4096, 8
+    docs = [0, 1, 700, 701, 2048, 2100, 4000, 4096]
+    rs = layouts.rank_spans(kind, n, P)
+    segs = [(n // P, s) for s in rs]
+    pairs, tiles = segment_work(1, 4, 4, 128, segs, [n // P] * P, rs, causal, docs=docs)
+    _, tiles_plain = segment_work(1, 4, 4, 128, segs, [n // P] * P, rs, causal)
+    allk = np.arange(n)
+    want = [oracle.unmasked_pairs(p, allk, causal, docs) for p in olay.positions(kind, n, P)]
+    assert pairs == want
+    assert all(t * 128 * 128 >= pr for t, pr in zip(tiles, pairs))
+    assert all(a <= b for a, b in zip(tiles, tiles_plain))
+    if kind == "contiguous":
+        assert sum(tiles) < sum(tiles_plain)
+
+
+def test_documents_rejected():
+    lib = _lib.load()
+
+    def call(bounds, n_docs=None, reserved=0, segs=GOOD_SEGS, chunks=GOOD_CHUNKS):
+        p = _problem()
+        arr = (ctypes.c_int64 * max(1, len(bounds)))(*bounds)
+        p.doc_bounds = ctypes.cast(arr, ctypes.c_void_p) if bounds else None
+        p.n_docs = len(bounds) - 1 if n_docs is None else n_docs
+        p.reserved_docs = reserved
+        return _call(p, _segs(segs), len(segs), _chunks(chunks), len(chunks))
+
+    assert call([0, 100, 100, 256]) == _lib.RA_ERR_INVALID      # not strictly increasing
+    assert call([0, 200, 100, 256]) == _lib.RA_ERR_INVALID
+    assert call([0, 255]) == _lib.RA_ERR_INVALID                 # position 255 outside
+    assert call([1, 256]) == _lib.RA_ERR_INVALID                 # position 0 outside
+    assert call([-1, 256]) == _lib.RA_ERR_INVALID
+    assert call([0, 2**31]) == _lib.RA_ERR_INVALID
+    assert call([], n_docs=1) == _lib.RA_ERR_INVALID             # NULL bounds
+    assert call([0, 256], n_docs=-1) == _lib.RA_ERR_INVALID
+    assert call(list(range(0, 514)), n_docs=513) == _lib.RA_ERR_INVALID   # > RA_MAX_DOCS
+    assert call([0, 256], reserved=1) == _lib.RA_ERR_INVALID
+    assert "document" in lib.ra_last_error().decode() or "reserved" in lib.ra_last_error().decode()
+    # keys outside the documents are rejected too
+    assert call([0, 256], chunks=[(128, [(128, 0, 1)]), (128, [(128, 200, 1)])]) == _lib.RA_ERR_INVALID
 
 
 def _call_host(p, segs, nsegs, chunks, nchunks, q=4096, o=4096, m=4096, l=4096):
