@@ -56,16 +56,23 @@ RA_HD void key_window(const Plan& p, int pos, int& lo, int& hi) {
 // Tiles [tb, te) of a monotone key span (positions pos0 + step * i, len rows,
 // 128-row tiles) that hold at least one position inside [lo, hi]. The host
 // (work estimates) and the kernels (tile walks) share this arithmetic, so
-// both count the same tiles.
+// both count the same tiles. Positions lie in [0, 2^31 - 1), so every
+// difference below fits in 31 bits; unit steps (contiguous and zigzag spans)
+// need no division.
 RA_HD void live_range(int pos0, int step, int len, int lo, int hi, int& tb, int& te) {
-  const int nt = (len + 127) / 128;
-  if (hi < pos0 || len <= 0) { tb = te = 0; return; }
-  const long long last = (static_cast<long long>(hi) - pos0) / step;  // last row with pos <= hi
-  te = last / 128 + 1 < nt ? static_cast<int>(last / 128 + 1) : nt;
+  const int nt = (len + 127) >> 7;
+  if (hi < pos0 || len <= 0) {
+    tb = te = 0;
+    return;
+  }
+  const unsigned dh = static_cast<unsigned>(hi - pos0);
+  const unsigned last = step == 1 ? dh : dh / static_cast<unsigned>(step);  // last row with pos <= hi
+  te = (last >> 7) + 1u < static_cast<unsigned>(nt) ? static_cast<int>((last >> 7) + 1u) : nt;
   tb = 0;
   if (lo > pos0) {
-    const long long first = (static_cast<long long>(lo) - pos0 + step - 1) / step;  // first row with pos >= lo
-    tb = first >= len ? nt : static_cast<int>(first / 128);
+    const unsigned dl = static_cast<unsigned>(lo - pos0) - 1u;
+    const unsigned first = (step == 1 ? dl : dl / static_cast<unsigned>(step)) + 1u;  // first row with pos >= lo
+    tb = first >= static_cast<unsigned>(len) ? nt : static_cast<int>(first >> 7);
   }
   if (tb > te) tb = te;
 }

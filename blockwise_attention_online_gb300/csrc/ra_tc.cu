@@ -577,8 +577,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ring_kernel(const __grid_const
             L = min(128, sg.len - 128 * t);
             if (p.causal || p.n_docs) {
               const int first = sg.pos0 + sg.step * (128 * t);
-              L = rhi < first ? 0 : min(L, (rhi - first) / sg.step + 1);
-              if (rlo > first) C0 = min(L, (rlo - first - 1) / sg.step + 1);
+              if (sg.step == 1) {
+                L = rhi < first ? 0 : min(L, rhi - first + 1);
+                if (rlo > first) C0 = min(L, rlo - first);
+              } else {
+                L = rhi < first ? 0 : min(L, (rhi - first) / sg.step + 1);
+                if (rlo > first) C0 = min(L, (rlo - first - 1) / sg.step + 1);
+              }
             }
           }
           ok = warp_wait(b_sfull, sc & 1, abort_flag, budget, kSiteSoftS);
