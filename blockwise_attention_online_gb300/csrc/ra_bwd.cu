@@ -53,9 +53,9 @@ enum : int {
 
 template <int D>
 struct BwdCfg {
-  static constexpr int kTileBytes = 128 * D * 2;  // one 128-row bf16 tile
   static constexpr int kBoxBytes = 128 * 128;     // 128 rows x 64 bf16 (one swizzle atom wide)
-  static constexpr int kBoxes = D / 64;
+  static constexpr int kBoxes = (D + 63) / 64;    // D = 96: the second box is half zero fill
+  static constexpr int kTileBytes = kBoxes * kBoxBytes;  // one 128-row bf16 tile
   // shared memory: two resident tiles, two stages of two tiles, per-stage
   // column data (three arrays of 128 words), barriers
   static constexpr int kRes0 = 0, kRes1 = kTileBytes;
@@ -470,8 +470,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkv_kernel(const __grid_co
         const int64_t row = (int64_t(b) * p.Hkv + hkv) * p.chunk_len[sg.chunk] + krow0 + r;
         float* dkr = p.dk[sg.chunk] + row * D;
         float* dvr = p.dv[sg.chunk] + row * D;
+        // D / 32 column chunks, the first half of them (rounded up) to half 0
+        constexpr int kNc = D / 32, kPer = (kNc + 1) / 2;
 #pragma unroll 1
-        for (int cc = hw * (D / 64); cc < (hw + 1) * (D / 64); ++cc) {
+        for (int cc = hw * kPer; cc < min(kNc, (hw + 1) * kPer); ++cc) {
           uint32_t a[32], v[32];
           if (any) {
             tmem_ld32(tdK + 32 * cc, a);
@@ -702,8 +704,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
         // the TMEM loads are warp-collective: every lane takes part, rows
         // past Sq just do not store
         float* dqr = p.dq + srow * D;
+        constexpr int kNc = D / 32, kPer = (kNc + 1) / 2;
 #pragma unroll 1
-        for (int cc = hw * (D / 64); cc < (hw + 1) * (D / 64); ++cc) {
+        for (int cc = hw * kPer; cc < min(kNc, (hw + 1) * kPer); ++cc) {
           uint32_t a[32];
           if (any) {
             tmem_ld32(tdQ + 32 * cc, a);
@@ -765,10 +768,17 @@ int launch_bwd_d(const BwdPlan& plan, const void* o, int o_fp32, int64_t o_sb, i
 int launch_bwd_bf16(const BwdPlan& plan, int D, const void* o, int o_fp32, int64_t o_sb,
                     int64_t o_sh, int64_t o_sr, const void* dout, const float* m,
                     const float* l, float* lse2, float* delta, int4* qtile_pos, void* stream) {
-  return D == 128 ? launch_bwd_d<128>(plan, o, o_fp32, o_sb, o_sh, o_sr, dout, m, l, lse2, delta,
-                                      qtile_pos, stream)
-                  : launch_bwd_d<64>(plan, o, o_fp32, o_sb, o_sh, o_sr, dout, m, l, lse2, delta,
-                                     qtile_pos, stream);
+  switch (D) {
+    case 128:
+      return launch_bwd_d<128>(plan, o, o_fp32, o_sb, o_sh, o_sr, dout, m, l, lse2, delta,
+                               qtile_pos, stream);
+    case 96:
+      return launch_bwd_d<96>(plan, o, o_fp32, o_sb, o_sh, o_sr, dout, m, l, lse2, delta,
+                              qtile_pos, stream);
+    default:
+      return launch_bwd_d<64>(plan, o, o_fp32, o_sb, o_sh, o_sr, dout, m, l, lse2, delta,
+                              qtile_pos, stream);
+  }
 }
 
 int read_and_clear_bwd_error(int* code) {

@@ -605,8 +605,8 @@ ra_status run_bwd(const ra_problem* pb, const void* q, const ra_q_segment* segs,
   const ra_problem& p = *pb;
   if (c.dtype != RA_BF16)
     return fail(RA_ERR_UNSUPPORTED, "the backward pass is implemented for bf16 inputs only");
-  if (c.D != 64 && c.D != 128)
-    return fail(RA_ERR_UNSUPPORTED, "the backward pass supports head_dim 64 or 128, got %lld",
+  if (c.D != 64 && c.D != 96 && c.D != 128)
+    return fail(RA_ERR_UNSUPPORTED, "the backward pass supports head_dim 64, 96 or 128, got %lld",
                 (long long)c.D);
   if (nchunks > 0 && !grads) return fail(RA_ERR_INVALID, "grads is NULL");
   for (int32_t k = 0; k < nchunks; ++k)

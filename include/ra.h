@@ -247,9 +247,9 @@ typedef struct {
  * problem->o_strides (multiples of 8 elements). Outputs, fp32 and dense: dq
  * [B, Hq, Sq, D]; grads[k].dk, grads[k].dv [B, Hkv, len_k, D] for every chunk
  * with len_k > 0 (all zero when no query sees the chunk). The call takes a
- * small scratch (two floats per query row, 8 bytes per 128-row query tile)
+ * small scratch (two floats per query row, 16 bytes per 128-row query tile)
  * from the library's memory pool on `stream` and frees it again.
- * bf16 inputs only (RA_ERR_UNSUPPORTED for RA_F32); head_dim 64 or 128; the
+ * bf16 inputs only (RA_ERR_UNSUPPORTED for RA_F32); head_dim 64, 96 or 128; the
  * chunk and span limits of ra_ring_attention's bf16 path.
  */
 ra_status ra_ring_attention_bwd(const ra_problem* problem, const void* q,

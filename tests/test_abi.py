@@ -247,8 +247,8 @@ def _grads(n, ptr=4096):
 def test_backward_entry_rejects_before_launch():
     p = _problem()
     segs, ch = _segs(GOOD_SEGS), _chunks(GOOD_CHUNKS)
-    # head_dim 96: forward only
-    assert _call_bwd(_problem(D=96), segs, 1, _chunks(GOOD_CHUNKS, D=96), 2,
+    # head_dim outside {64, 96, 128}
+    assert _call_bwd(_problem(D=80), segs, 1, _chunks(GOOD_CHUNKS, D=80), 2,
                      _grads(2)) == _lib.RA_ERR_UNSUPPORTED
     # fp32 inputs: the backward is bf16 only
     assert _call_bwd(_problem(dtype=_lib.RA_F32, D=64), segs, 1, _chunks(GOOD_CHUNKS, D=64), 2,

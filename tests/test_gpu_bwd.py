@@ -71,6 +71,8 @@ def _layout_bwd(q, k, v, do, kind, P, causal, out_dtype=None):
     (1, 4, 2, 768, 128, "zigzag", 2, True),
     (2, 2, 1, 640, 64, "striped", 4, True),
     (1, 8, 2, 1024, 128, "contiguous", 8, True),
+    (1, 4, 2, 640, 96, "zigzag", 2, True),
+    (2, 2, 2, 384, 96, "contiguous", 3, False),
 ])
 def test_backward_matches_oracle(B, Hq, Hkv, S, D, kind, P, causal):
     q, k, v, do = _inputs(11, B, Hq, Hkv, S, D)
