@@ -307,10 +307,10 @@ def run_gpu(args):
 
 def run_gpu_bwd(args):
     """The backward pass of the same workload: one step = ra_ring_attention_bwd
-    (preparation, dK/dV and dQ kernels) on the forward's O, m, l and a seeded
-    dO. FLOPs count the standard five products of the backward (2.5 x the
-    forward's), causal-adjusted like the forward; the two-kernel design
-    executes seven (S and dP are recomputed once per kernel)."""
+    (two preparation kernels, then one grid of dK/dV and dQ CTAs) on the
+    forward's O, m, l and a seeded dO. FLOPs count the standard five products
+    of the backward (2.5 x the forward's), causal-adjusted like the forward;
+    the design executes seven (S and dP are recomputed by both kinds of CTA)."""
     import torch
     from blockwise_attention_online_gb300 import device_status, ring_attention, ring_attention_bwd
 
@@ -379,10 +379,10 @@ def run_gpu_bwd(args):
         "pct_of_peak": round(100 * value / world / peak_b, 2),
         "roofline": {"bound": "tensor", "achieved": round(achieved, 3), "peak": peak_b,
                      "unit": "TFLOP/s", "frac": round(achieved / peak_b, 4), "traffic": None,
-                     "kernel": "bwd_dkv_kernel<128> + bwd_dq_kernel<128> (one step)",
+                     "kernel": "bwd_kernel<128> (dK/dV and dQ CTAs, one step)",
                      "peak_source": f"{src} bf16 burst (MEASURED_PEAKS.json)"},
         "clocks": clk.summary(),
-        "gpu_launches": 4 * args.steps,
+        "gpu_launches": 3 * args.steps,
         "e2e": None,
     }
     if not args.no_cpu_baseline and world == 1:

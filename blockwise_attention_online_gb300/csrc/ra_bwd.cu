@@ -14,16 +14,16 @@
 //   dK_c = scale dS_c^T Q        dQ   = scale sum_c dS_c K_c
 //
 // Three launches on the caller's stream:
-//   bwd_prep_kernel / bwd_qtile_kernel  lse2 and delta per query row; lowest
-//                                       and highest position of each
-//                                       128-row query tile
-//   bwd_dkv_kernel<D>  one CTA per (batch, key/value head, 128-row key tile):
+//   bwd_prep_kernel    lse2 and delta per query row
+//   bwd_qtile_kernel   bounds of the key windows of each 128-row query tile
+//   bwd_kernel<D>      two kinds of CTA in one grid:
+//     bwd_dkv_tile     one per (batch, key/value head, 128-row key tile):
 //                      walks every live query tile of the heads that read it
 //                      and accumulates dK, dV in TMEM (the per-shard sum)
-//   bwd_dq_kernel<D>   one CTA per (batch, query head, 128-row query tile):
+//     bwd_dq_tile      one per (batch, query head, 128-row query tile):
 //                      walks every live key tile and accumulates dQ in TMEM
 //
-// Warp roles of both tcgen05 kernels (384 threads): warp 0 TMA producer,
+// Warp roles of both kinds of CTA (384 threads): warp 0 TMA producer,
 // warp 1 MMA warp (waits warp-uniformly, one elected lane issues), warps 2-3
 // idle, warps 4-11 the elementwise work: one TMEM lane (= tile row) per
 // thread, warpgroup h on columns [64h, 64h + 64) of every 128-column tile (no
@@ -51,18 +51,21 @@ enum : int {
   kSiteBwdAcc = 36
 };
 
-template <int D>
+// kDocs: the dK/dV CTAs of a launch with packed documents stage a (lo, hi)
+// key window per query column instead of its position (one more array).
+template <int D, bool kDocs = true>
 struct BwdCfg {
   static constexpr int kBoxBytes = 128 * 128;     // 128 rows x 64 bf16 (one swizzle atom wide)
   static constexpr int kBoxes = (D + 63) / 64;    // D = 96: the second box is half zero fill
   static constexpr int kTileBytes = kBoxes * kBoxBytes;  // one 128-row bf16 tile
   // shared memory: two resident tiles, two stages of two tiles, per-stage
-  // column data (three arrays of 128 words), barriers
+  // column data (-lse2, -delta, then the (lo, hi) key windows or, without
+  // documents, the positions), barriers
   static constexpr int kRes0 = 0, kRes1 = kTileBytes;
   static constexpr int kStage0 = 2 * kTileBytes;
   static constexpr int kStageBytes = 2 * kTileBytes;
   static constexpr int kAux0 = kStage0 + 2 * kStageBytes;
-  static constexpr int kAuxBytes = 4 * 128 * 4;
+  static constexpr int kAuxBytes = (kDocs ? 4 : 3) * 128 * 4;
   static constexpr int kBar = kAux0 + 2 * kAuxBytes;
   static constexpr int kBarBytes = 256;
   static constexpr int kSmemBytes = kBar + kBarBytes + 1024;  // + alignment slack
@@ -163,10 +166,10 @@ struct BwdBars {
   volatile int* abort_flag;
 };
 
-template <int D>
+template <int D, bool kDocs = true>
 __device__ __forceinline__ void bwd_setup(uint8_t* smem_raw, uint32_t& base, uint8_t*& gbase,
                                           BwdBars& bb) {
-  using C = BwdCfg<D>;
+  using C = BwdCfg<D, kDocs>;
   const uint32_t raw = smem_addr(smem_raw);
   base = (raw + 1023u) & ~1023u;
   gbase = smem_raw + (base - raw);
@@ -243,6 +246,7 @@ __device__ __forceinline__ void issue_tmem_a(uint32_t d_tmem, uint32_t a_tmem, u
 // The query tiles a key tile sees: heads hkv*g .. hkv*g + g - 1, every tile
 // whose rows' key windows meet the key tile's positions [kmin, kmax] (all
 // when neither causal nor packed).
+template <bool kDocs>
 struct QWalk {
   int idx, n, nqt, h0;
   __device__ __forceinline__ bool next(const BwdPlan& p, int kmin, int kmax, int& h, int& qt) {
@@ -250,28 +254,31 @@ struct QWalk {
       const int i = idx++;
       qt = i % nqt;
       h = h0 + i / nqt;
-      if (!p.causal && p.n_docs == 0) return true;
-      const int4 w = p.qtile_pos[qt];
-      if (w.y >= kmin && w.x <= kmax) return true;
+      if constexpr (kDocs) {
+        const int4 w = p.qtile_pos[qt];
+        if (w.y >= kmin && w.x <= kmax) return true;
+      } else {
+        if (!p.causal || p.qtile_pos[qt].y >= kmin) return true;
+      }
     }
     return false;
   }
 };
 
-template <int D>
-__global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkv_kernel(const __grid_constant__ BwdPlan p) {
-  using C = BwdCfg<D>;
+template <int D, bool kDocs>
+__device__ __forceinline__ void bwd_dkv_tile(const BwdPlan& p, int cta) {
+  using C = BwdCfg<D, kDocs>;
   extern __shared__ uint8_t smem_raw[];
   uint32_t base;
   uint8_t* gbase;
   BwdBars bb;
-  bwd_setup<D>(smem_raw, base, gbase, bb);
+  bwd_setup<D, kDocs>(smem_raw, base, gbase, bb);
   const uint32_t tmem = *bb.tmem_slot;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const unsigned long long budget = p.timeout_ns;
 
   // this CTA's key tile
-  int u = blockIdx.x;
+  int u = cta;
   const int gt = u % p.n_ktiles;
   u /= p.n_ktiles;
   const int hkv = u % p.Hkv, b = u / p.Hkv;
@@ -297,7 +304,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkv_kernel(const __grid_co
         tma_load_4d(sV + bx * C::kBoxBytes, &p.vmap[sg.chunk], bb.res_full, bx * 64, krow0, hkv, b);
       }
     }
-    QWalk w{0, g * p.n_qtiles, p.n_qtiles, hkv * g};
+    QWalk<kDocs> w{0, g * p.n_qtiles, p.n_qtiles, hkv * g};
     int h, qt, j = 0;
     bool ok = true;
     while (ok && w.next(p, kmin, kmax, h, qt)) {
@@ -313,18 +320,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkv_kernel(const __grid_co
           tma_load_4d(sDO + bx * C::kBoxBytes, &p.domap, bb.st_full0 + 8 * st, bx * 64, 128 * qt, h, b);
         }
       }
-      // per-column data of this query tile: -lse2, -delta, key window [lo, hi]
+      // per-column data of this query tile: -lse2, -delta, then its key
+      // window (lo, hi) with documents, else its position
       float* aux = reinterpret_cast<float*>(gbase + C::kAux0 + st * C::kAuxBytes);
       const int64_t rowbase = (int64_t(b) * p.Hq + h) * p.Sq;
       for (int i = lane; i < 128; i += 32) {
         const int row = 128 * qt + i;
         const bool valid = row < p.Sq;
-        int lo = 0x7fffffff, hi = int(0x80000000);  // an empty window
-        if (valid) key_window(p, bwd_row_position(p, row), lo, hi);
         aux[i] = valid ? -p.lse2[rowbase + row] : -kInf;
         aux[128 + i] = valid ? -p.delta[rowbase + row] : 0.f;
-        reinterpret_cast<int*>(aux)[256 + i] = hi;
-        reinterpret_cast<int*>(aux)[384 + i] = lo;
+        if constexpr (kDocs) {
+          int lo = 0x7fffffff, hi = int(0x80000000);  // an empty window
+          if (valid) key_window(p, bwd_row_position(p, row), lo, hi);
+          reinterpret_cast<int2*>(aux + 256)[i] = make_int2(lo, hi);
+        } else {
+          reinterpret_cast<int*>(aux)[256 + i] = valid ? bwd_row_position(p, row) : int(0x80000000);
+        }
       }
       mbar_arrive(bb.st_full0 + 8 * st);
       ++j;
@@ -342,7 +353,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkv_kernel(const __grid_co
     const bool leader = elect_one();
     const uint32_t tS = tmem, tP = tmem + 128, tdV = tmem + 256, tdK = tmem + 384;
     bool ok = warp_wait(bb.res_full, 0, bb.abort_flag, budget, kSiteBwdKv);
-    QWalk w{0, g * p.n_qtiles, p.n_qtiles, hkv * g};
+    QWalk<kDocs> w{0, g * p.n_qtiles, p.n_qtiles, hkv * g};
     int h, qt, j = 0;
     while (ok && w.next(p, kmin, kmax, h, qt)) {
       const int st = j & 1;
@@ -385,7 +396,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkv_kernel(const __grid_co
     const uint32_t tdV = tmem + 256 + lane_off, tdK = tmem + 384 + lane_off;
     const float c2 = p.scale_log2;
     const uint64_t c2x2 = f2(c2, c2);
-    QWalk w{0, g * p.n_qtiles, p.n_qtiles, hkv * g};
+    QWalk<kDocs> w{0, g * p.n_qtiles, p.n_qtiles, hkv * g};
     int h, qt, j = 0;
     bool ok = true;
     while (ok && w.next(p, kmin, kmax, h, qt)) {
@@ -395,14 +406,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkv_kernel(const __grid_co
       if (!ok) break;
       tc_fence_after();
       const float* aux = reinterpret_cast<const float*>(gbase + C::kAux0 + st * C::kAuxBytes);
-      const int* ahi = reinterpret_cast<const int*>(aux) + 256;
-      const int* alo = reinterpret_cast<const int*>(aux) + 384;
+      const int4* awin = reinterpret_cast<const int4*>(aux + 256);  // two columns' windows
+      const int* apos = reinterpret_cast<const int*>(aux) + 256;     // positions
       // a mask is needed only where some key of the tile lies outside some
-      // row's window, or where the key tile is ragged
+      // row's window (after some row's position, without documents), or
+      // where the key tile is ragged
       bool masked = kvalid < 128;
-      if (p.causal || p.n_docs) {
+      if constexpr (kDocs) {
         const int4 qw = p.qtile_pos[qt];
         masked = masked || kmax > qw.w || kmin < qw.z;
+      } else {
+        masked = masked || (p.causal && kmax > p.qtile_pos[qt].w);
       }
 #pragma unroll 1
       for (int i = 2 * hw; i < 2 * hw + 2; ++i) {
@@ -420,6 +434,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkv_kernel(const __grid_co
         tmem_ld_wait();
         reg_fence(s);
         reg_fence(dp);
+        if (kDocs && masked) {
+          // a score outside its column's window (or of a missing key row)
+          // becomes -inf: p = 0 and dS = 0
+#pragma unroll
+          for (int c = 0; c < 32; c += 2) {
+            const int4 w = awin[(32 * i + c) / 2];
+            if (!krow_ok || kpos < w.x || kpos > w.y) s[c] = 0xff800000u;
+            if (!krow_ok || kpos < w.z || kpos > w.w) s[c + 1] = 0xff800000u;
+          }
+        }
         uint32_t pp[16], pd[16];
 #pragma unroll
         for (int c = 0; c < 32; c += 4) {
@@ -432,13 +456,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkv_kernel(const __grid_co
           f2_split(x01, x0, x1);
           f2_split(x23, x2, x3);
           float p0 = ex2(x0), p1 = ex2(x1), p2 = ex2(x2), p3 = ex2(x3);
-          if (masked) {
-            const int4 h4 = *reinterpret_cast<const int4*>(ahi + 32 * i + c);
-            const int4 l4 = *reinterpret_cast<const int4*>(alo + 32 * i + c);
-            if (!krow_ok || kpos > h4.x || kpos < l4.x) p0 = 0.f;
-            if (!krow_ok || kpos > h4.y || kpos < l4.y) p1 = 0.f;
-            if (!krow_ok || kpos > h4.z || kpos < l4.z) p2 = 0.f;
-            if (!krow_ok || kpos > h4.w || kpos < l4.w) p3 = 0.f;
+          if (!kDocs && masked) {
+            const int4 qp4 = *reinterpret_cast<const int4*>(apos + 32 * i + c);
+            if (!krow_ok || (p.causal && kpos > qp4.x)) p0 = 0.f;
+            if (!krow_ok || (p.causal && kpos > qp4.y)) p1 = 0.f;
+            if (!krow_ok || (p.causal && kpos > qp4.z)) p2 = 0.f;
+            if (!krow_ok || (p.causal && kpos > qp4.w)) p3 = 0.f;
           }
           const uint64_t t01 = add2(f2(__uint_as_float(dp[c]), __uint_as_float(dp[c + 1])), f2(del.x, del.y));
           const uint64_t t23 = add2(f2(__uint_as_float(dp[c + 2]), __uint_as_float(dp[c + 3])), f2(del.z, del.w));
@@ -505,7 +528,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkv_kernel(const __grid_co
 
 // ------------------------------------------------------------ dQ
 template <int D>
-__global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_constant__ BwdPlan p) {
+__device__ __forceinline__ void bwd_dq_tile(const BwdPlan& p, int cta) {
   using C = BwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint32_t base;
@@ -518,7 +541,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
 
   // this CTA's query tile; with a causal mask the later tiles (more keys)
   // are started first
-  int u = blockIdx.x;
+  int u = cta;
   int qt = u % p.n_qtiles;
   if (p.causal) qt = p.n_qtiles - 1 - qt;
   u /= p.n_qtiles;
@@ -730,6 +753,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
   bwd_teardown(tmem);
 }
 
+// One launch for both: CTAs [0, n_kv_ctas) take key tiles, the rest query
+// tiles. The block scheduler hands out the query-tile CTAs as the key-tile
+// CTAs of the last wave retire, so neither grid leaves a partial last wave
+// idle on its own.
+template <int D, bool kDocs>
+__global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_constant__ BwdPlan p,
+                                                             int n_kv_ctas) {
+  if (int(blockIdx.x) < n_kv_ctas)
+    bwd_dkv_tile<D, kDocs>(p, int(blockIdx.x));
+  else
+    bwd_dq_tile<D>(p, int(blockIdx.x) - n_kv_ctas);
+}
+
 template <int D>
 int launch_bwd_d(const BwdPlan& plan, const void* o, int o_fp32, int64_t o_sb, int64_t o_sh,
                  int64_t o_sr, const void* dout, const float* m, const float* l, float* lse2,
@@ -744,20 +780,15 @@ int launch_bwd_d(const BwdPlan& plan, const void* o, int o_fp32, int64_t o_sb, i
   bwd_qtile_kernel<<<unsigned((plan.n_qtiles + 127) / 128), 128, 0, cs>>>(plan, qtile_pos);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   constexpr int kSmem = BwdCfg<D>::kSmemBytes;
-  if ((e = cudaFuncSetAttribute(bwd_dkv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                kSmem)) != cudaSuccess)
-    return e;
-  if ((e = cudaFuncSetAttribute(bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                kSmem)) != cudaSuccess)
+  const bool docs = plan.n_docs > 0;
+  auto kern = docs ? bwd_kernel<D, true> : bwd_kernel<D, false>;
+  if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem)) !=
+      cudaSuccess)
     return e;
   const int64_t kv_ctas = int64_t(plan.n_ktiles) * plan.Hkv * plan.B;
   const int64_t q_ctas = int64_t(plan.n_qtiles) * plan.Hq * plan.B;
-  if (kv_ctas > 0) {
-    bwd_dkv_kernel<D><<<unsigned(kv_ctas), kBwdThreads, kSmem, cs>>>(plan);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  }
-  if (q_ctas > 0) {
-    bwd_dq_kernel<D><<<unsigned(q_ctas), kBwdThreads, kSmem, cs>>>(plan);
+  if (kv_ctas + q_ctas > 0) {
+    kern<<<unsigned(kv_ctas + q_ctas), kBwdThreads, kSmem, cs>>>(plan, int(kv_ctas));
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   return cudaSuccess;
