@@ -96,38 +96,37 @@ __device__ __forceinline__ void bwd_live_tiles(const BwdPlan& p, int k, int lo, 
 }
 
 // ------------------------------------------------------------ preparation
-// One thread per query row: delta = sum_d dO * O (O as the forward wrote it)
-// and lse2 = m log2(e) + log2(l), +inf for a row that sees no key.
+// Two query rows per warp, 16 lanes per row, 8 head_dim elements per lane
+// (head_dim <= 128), so that every load is coalesced: delta = sum_d dO * O
+// (O as the forward wrote it) and lse2 = m log2(e) + log2(l), +inf for a row
+// that sees no key.
 __global__ void bwd_prep_kernel(const void* o, int o_fp32, int64_t o_sb, int64_t o_sh,
                                 int64_t o_sr, const uint16_t* dout, const float* m,
                                 const float* l, int B, int Hq, int Sq, int D, float* lse2,
                                 float* delta) {
-  const int64_t row = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int lane = threadIdx.x & 31, sl = lane & 15;
+  const int64_t row = ((int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5) * 2 + (lane >> 4);
   const int64_t rows = int64_t(B) * Hq * Sq;
-  if (row >= rows) return;
-  const int64_t bh = row / Sq, i = row - bh * Sq;
-  const int64_t b = bh / Hq, h = bh - b * Hq;
-  const int64_t off = b * o_sb + h * o_sh + i * o_sr;
-  const uint4* d4 = reinterpret_cast<const uint4*>(dout + off);
+  const bool active = row < rows;
   float acc = 0.f;
-  if (o_fp32) {
-    const float4* o4 = reinterpret_cast<const float4*>(static_cast<const float*>(o) + off);
-    for (int c = 0; c < D / 8; ++c) {
-      const uint4 g = d4[c];
-      const float4 a = o4[2 * c], bq = o4[2 * c + 1];
-      const uint32_t w[4] = {g.x, g.y, g.z, g.w};
+  if (active && sl < D / 8) {
+    const int64_t bh = row / Sq, i = row - bh * Sq;
+    const int64_t b = bh / Hq, h = bh - b * Hq;
+    const int64_t off = b * o_sb + h * o_sh + i * o_sr + 8 * sl;
+    const uint4 g = *reinterpret_cast<const uint4*>(dout + off);
+    const uint32_t w[4] = {g.x, g.y, g.z, g.w};
+    if (o_fp32) {
+      const float4* o4 = reinterpret_cast<const float4*>(static_cast<const float*>(o) + off);
+      const float4 a = o4[0], bq = o4[1];
       const float ov[8] = {a.x, a.y, a.z, a.w, bq.x, bq.y, bq.z, bq.w};
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         acc = fmaf(__uint_as_float(w[k] << 16), ov[2 * k], acc);
         acc = fmaf(__uint_as_float(w[k] & 0xffff0000u), ov[2 * k + 1], acc);
       }
-    }
-  } else {
-    const uint4* o4 = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(o) + off);
-    for (int c = 0; c < D / 8; ++c) {
-      const uint4 g = d4[c], a = o4[c];
-      const uint32_t w[4] = {g.x, g.y, g.z, g.w}, v[4] = {a.x, a.y, a.z, a.w};
+    } else {
+      const uint4 a = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(o) + off);
+      const uint32_t v[4] = {a.x, a.y, a.z, a.w};
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         acc = fmaf(__uint_as_float(w[k] << 16), __uint_as_float(v[k] << 16), acc);
@@ -135,20 +134,26 @@ __global__ void bwd_prep_kernel(const void* o, int o_fp32, int64_t o_sb, int64_t
       }
     }
   }
-  delta[row] = acc;
-  const float lr = l[row];
-  lse2[row] = lr > 0.f ? fmaf(m[row], kLog2e, log2f(lr)) : kInf;
+  // sum over the 16 lanes of each row (the xor offsets stay inside a half)
+#pragma unroll
+  for (int d = 8; d > 0; d >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, d);
+  if (active && sl == 0) {
+    delta[row] = acc;
+    const float lr = l[row];
+    lse2[row] = lr > 0.f ? fmaf(m[row], kLog2e, log2f(lr)) : kInf;
+  }
 }
 
-// One thread per 128-row query tile: bounds of its rows' key windows
+// One warp per 128-row query tile: bounds of its rows' key windows
 // (x: lowest lo, y: highest hi, z: highest lo, w: lowest hi). A key tile
 // inside [z, w] is visible to every row; one outside [x, y] to none.
 __global__ void bwd_qtile_kernel(const __grid_constant__ BwdPlan p, int4* out) {
-  const int t = blockIdx.x * blockDim.x + threadIdx.x;
-  if (t >= p.n_qtiles) return;
+  const int t = int((int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5);
+  const int lane = threadIdx.x & 31;
+  if (t >= p.n_qtiles) return;  // whole warps
   int4 w = make_int4(0x7fffffff, -1, -1, 0x7fffffff);
   const int r1 = min(p.Sq, 128 * t + 128);
-  for (int r = 128 * t; r < r1; ++r) {
+  for (int r = 128 * t + lane; r < r1; r += 32) {
     int lo, hi;
     key_window(p, bwd_row_position(p, r), lo, hi);
     w.x = min(w.x, lo);
@@ -156,7 +161,11 @@ __global__ void bwd_qtile_kernel(const __grid_constant__ BwdPlan p, int4* out) {
     w.z = max(w.z, lo);
     w.w = min(w.w, hi);
   }
-  out[t] = w;
+  w.x = __reduce_min_sync(0xffffffffu, w.x);
+  w.y = __reduce_max_sync(0xffffffffu, w.y);
+  w.z = __reduce_max_sync(0xffffffffu, w.z);
+  w.w = __reduce_min_sync(0xffffffffu, w.w);
+  if (lane == 0) out[t] = w;
 }
 
 // ------------------------------------------------------------ shared pieces
@@ -772,12 +781,12 @@ int launch_bwd_d(const BwdPlan& plan, const void* o, int o_fp32, int64_t o_sb, i
                  float* delta, int4* qtile_pos, void* stream) {
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   const int64_t rows = int64_t(plan.B) * plan.Hq * plan.Sq;
-  bwd_prep_kernel<<<unsigned((rows + 127) / 128), 128, 0, cs>>>(
+  bwd_prep_kernel<<<unsigned((rows * 16 + 255) / 256), 256, 0, cs>>>(
       o, o_fp32, o_sb, o_sh, o_sr, static_cast<const uint16_t*>(dout), m, l, plan.B, plan.Hq,
       plan.Sq, D, lse2, delta);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  bwd_qtile_kernel<<<unsigned((plan.n_qtiles + 127) / 128), 128, 0, cs>>>(plan, qtile_pos);
+  bwd_qtile_kernel<<<unsigned((plan.n_qtiles + 3) / 4), 128, 0, cs>>>(plan, qtile_pos);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   constexpr int kSmem = BwdCfg<D>::kSmemBytes;
   const bool docs = plan.n_docs > 0;
