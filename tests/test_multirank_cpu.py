@@ -49,3 +49,20 @@ def test_single_process_is_identity():
     import bench
     assert bench.max_over_ranks(3.5) == 3.5
     assert bench.whole_job_tflops(1e12, 1, 1, 1000.0) == pytest.approx(1.0)
+
+
+@pytest.mark.parametrize("workload,mean_len", [("bf16_8k", 1024), ("bf16_32k_causal", 4096)])
+def test_bench_flops_with_documents_match_the_oracle_pair_count(workload, mean_len):
+    """bench.py --docs counts 4 * B * Hq * D flops per visible (query, key)
+    pair; the pair count is the oracle's for the same seeded documents."""
+    import numpy as np
+    import bench
+    import oracle
+    from blockwise_attention_online_gb300 import workloads
+    w = workloads.WORKLOADS[workload]
+    docs, flops = bench._docs(w, mean_len)
+    assert docs[0] == 0 and docs[-1] == w.S and len(docs) >= 2
+    pos = np.arange(w.S)
+    pairs = oracle.unmasked_pairs(pos, pos, w.causal, docs)
+    assert flops == 4.0 * w.B * w.Hq * w.D * pairs
+    assert bench._docs(w, 0) == (None, w.flops())
