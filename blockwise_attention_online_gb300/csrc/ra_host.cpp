@@ -43,6 +43,9 @@ ra_status ok() {
 }
 
 constexpr int64_t kPosLimit = (int64_t(1) << 31) - 1;
+// Fixed cost of a stream-K unit in key-tile steps (measured: a unit switch
+// costs about two tile steps of a long unit).
+constexpr int64_t kUnitCost = 2;
 constexpr int64_t kRowLimit = (int64_t(1) << 31) - 256;
 
 // A flattened monotone span of rows with global positions.
@@ -482,10 +485,33 @@ ra_status run_tc(const Common& c, const ra_problem& p, const void* q,
   }
   if (T > (int64_t(1) << 30)) return fail(RA_ERR_UNSUPPORTED, "stream-K range too large");
   plan.sk_total = int32_t(T);
+  // CTA boundaries on the tile line: the tail units are weighed as their
+  // tiles plus kUnitCost for the unit's fixed costs (its Q load, the switch
+  // of the softmax warps, its epilogue), and the weighted line is cut in G
+  // equal shares; a cut inside a unit's fixed cost moves to its first tile.
+  // With equal units this is the plain cut of the tiles in G shares; with
+  // many short units (causal starts, packed documents) the CTAs that get
+  // them take fewer tiles.
+  {
+    const int64_t W = T + kUnitCost * sk_units;
+    int64_t i = 0, q = 0;  // unit i starts at weight q
+    plan.sk_bound[0] = 0;
+    for (int64_t c = 1; c <= G; ++c) {
+      const int64_t x = c * W / G;
+      while (i < sk_units && q + kUnitCost + (plan.sk_prefix[i + 1] - plan.sk_prefix[i]) <= x) {
+        q += kUnitCost + (plan.sk_prefix[i + 1] - plan.sk_prefix[i]);
+        ++i;
+      }
+      const int64_t n = i < sk_units ? plan.sk_prefix[i + 1] - plan.sk_prefix[i] : 0;
+      const int64_t in = std::min(n, std::max<int64_t>(0, x - q - kUnitCost));
+      plan.sk_bound[c] = int32_t(i < sk_units ? plan.sk_prefix[i] + in : T);
+    }
+    plan.sk_bound[G] = int32_t(T);
+  }
   // does any CTA boundary fall strictly inside a unit?
   bool split = false;
   for (int64_t cta = 1; cta < G && !split; ++cta) {
-    const int64_t a = cta * T / G;
+    const int64_t a = plan.sk_bound[cta];
     for (int64_t i = 0; i < sk_units; ++i)
       if (plan.sk_prefix[i] < a && a < plan.sk_prefix[i + 1]) { split = true; break; }
   }

@@ -111,11 +111,13 @@ struct alignas(128) TcPlan {
   int32_t n_qpieces, n_kvsegs, n_qpairs, has_order;
   int32_t n_units;
   // work split: every CTA first takes dp_rounds whole units round-robin, then
-  // its share [c*T/G, (c+1)*T/G) of the T key tiles of units dp_rounds*G ..
+  // its share [sk_bound[c], sk_bound[c+1]) of the T key tiles of units
+  // dp_rounds*G .. (laid end to end, sk_prefix[i] = first tile of unit i)
   int32_t grid, dp_rounds, sk_units, sk_total;
   unsigned epoch;                    // value a published partial carries
   TcScratch scratch;                 // null pointers when no unit is split
   int32_t sk_prefix[kTcMaxSkUnits + 1];
+  int32_t sk_bound[kTcMaxGrid + 1];
   int32_t chunk_seg_begin[kTcMaxChunks + 1];
   QPiece qp[kMaxQPieces];
   KvSeg ks[kTcMaxKvSegs];

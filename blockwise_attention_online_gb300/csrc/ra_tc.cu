@@ -218,9 +218,8 @@ struct Walker {
   long long a, b;
   __device__ __forceinline__ void init(const TcPlan& p) {
     k = 0;
-    const long long T = p.sk_total, G = p.grid, c = blockIdx.x;
-    a = c * T / G;
-    b = (c + 1) * T / G;
+    a = p.sk_bound[blockIdx.x];
+    b = p.sk_bound[blockIdx.x + 1];
     // last unit starting at or before a; step back over empty units at a
     int lo = 0, hi = p.sk_units - 1;
     while (lo < hi) {
@@ -737,16 +736,14 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ring_kernel(const __grid_const
       float a_self = 1.f;
       int c_first = 0, c_end = 0;  // CTAs [c_first, c_end) hold later parts
       if (I.kind == kHead) {
-        const long long T = p.sk_total, G = p.grid;
-        const long long hi = p.sk_prefix[I.u - p.dp_rounds * p.grid + 1];
+        const int hi = p.sk_prefix[I.u - p.dp_rounds * p.grid + 1];
         c_first = blockIdx.x + 1;
         c_end = c_first;
-        while (c_end < p.grid && (long long)c_end * T / G < hi) ++c_end;
+        while (c_end < p.grid && p.sk_bound[c_end] < hi) ++c_end;
         // wait for every later part's flag (one thread polls, the warpgroup follows)
         if (r == 0) {
           for (int c = c_first; c < c_end; ++c) {
-            const long long ca = (long long)c * T / G, cb = (long long)(c + 1) * T / G;
-            if (ca >= cb) continue;  // that CTA holds no tiles at all
+            if (p.sk_bound[c] >= p.sk_bound[c + 1]) continue;  // that CTA holds no tiles at all
             const unsigned* f = p.scratch.flags + c * 2 + wg;
             unsigned long long t0 = 0;
             for (uint32_t k = 1; ld_acquire(f) != p.epoch; ++k) {
@@ -775,8 +772,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ring_kernel(const __grid_const
         }
         float M = m_ref;
         for (int c = c_first; c < c_end; ++c) {
-          const long long ca = (long long)c * T / G, cb = (long long)(c + 1) * T / G;
-          if (ca >= cb) continue;
+          if (p.sk_bound[c] >= p.sk_bound[c + 1]) continue;
           const float4 st = __ldcg(p.scratch.stats + (size_t(c) * 2 + wg) * 128 + r);
           M = fmaxf(M, st.x);
         }
@@ -784,8 +780,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ring_kernel(const __grid_const
         l *= a_self;
         lr *= a_self;
         for (int c = c_first; c < c_end; ++c) {
-          const long long ca = (long long)c * T / G, cb = (long long)(c + 1) * T / G;
-          if (ca >= cb) continue;
+          if (p.sk_bound[c] >= p.sk_bound[c + 1]) continue;
           const float4 st = __ldcg(p.scratch.stats + (size_t(c) * 2 + wg) * 128 + r);
           const float bp = (st.x == kNegInf) ? 0.f : ex2(st.x - M);
           mx = fmaxf(mx, st.y);
@@ -829,9 +824,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ring_kernel(const __grid_const
 #pragma unroll
             for (int c = 0; c < 32; ++c) o[cc][c] = __float_as_uint(__uint_as_float(o[cc][c]) * a_self);
           for (int c = c_first; c < c_end; ++c) {
-            const long long ca = (long long)c * p.sk_total / p.grid;
-            const long long cb = (long long)(c + 1) * p.sk_total / p.grid;
-            if (ca >= cb) continue;
+            if (p.sk_bound[c] >= p.sk_bound[c + 1]) continue;
             const size_t prow = (size_t(c) * 2 + wg) * 128 + r;
             const float4 st = __ldcg(p.scratch.stats + prow);
             const float bp = (st.x == kNegInf) ? 0.f : ex2(st.x - m_ref);
