@@ -203,8 +203,10 @@ struct TileIter {
 };
 
 // A CTA's work, in order: whole units c, c+G, ... for dp_rounds rounds, then
-// its share [c*T/G, (c+1)*T/G) of the key tiles of the remaining units (a
-// stream-K split). A share may begin inside a unit (a TAIL part: it publishes
+// its share [sk_bound[c], sk_bound[c+1]) of the key tiles of the remaining
+// units laid end to end (a stream-K split; the host places the cuts so that
+// shares of tiles plus per-unit fixed costs are equal). A share may begin
+// inside a unit (a TAIL part: it publishes
 // partial results to its scratch slot) and may end inside one (a HEAD part: it
 // merges the partials of the CTAs that hold the rest before the epilogue).
 enum : int { kFull = 0, kHead = 1, kTail = 2 };
