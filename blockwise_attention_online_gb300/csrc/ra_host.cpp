@@ -927,6 +927,14 @@ ra_status ra_segment_work(const ra_problem* problem, const ra_q_segment* segs, i
       r += sp.len;
     }
   }
+  if (c.n_docs > 0) {
+    // the same rule as the launches: every key position inside [b_0, b_n)
+    const int64_t b0 = c.doc_bounds.front(), bn = c.doc_bounds.back();
+    for (const Span& sp : kv)
+      if (sp.pos0 < b0 || sp.pos0 + sp.step * (sp.len - 1) >= bn)
+        return fail(RA_ERR_INVALID, "a position lies outside the documents [%lld, %lld)",
+                    (long long)b0, (long long)bn);
+  }
   for (int32_t s = 0; s < nsegs; ++s) {
     if (pairs) pairs[s] = 0;
     if (tiles) tiles[s] = 0;
