@@ -85,6 +85,8 @@ def _set_docs(pb, docs):
         pb.doc_bounds = None
         return
     b = [int(x) for x in docs]
+    if len(b) < 2:
+        raise ValueError("docs needs at least two boundaries (one document)")
     arr = (ctypes.c_int64 * len(b))(*b)
     pb._docs_keepalive = arr
     pb.doc_bounds = ctypes.cast(arr, ctypes.c_void_p)

@@ -171,6 +171,8 @@ def test_segment_work_with_documents_is_exact(kind, causal):
     assert all(a <= b for a, b in zip(tiles, tiles_plain))
     if kind == "contiguous":
         assert sum(tiles) < sum(tiles_plain)
+    with pytest.raises(ValueError):
+        segment_work(1, 4, 4, 128, segs, [n // P] * P, rs, causal, docs=[0])
     # keys outside the documents are rejected, as by the launches
     with pytest.raises(_lib.RaError):
         segment_work(1, 4, 4, 128, segs, [n // P] * P, rs, causal, docs=docs[:-1] + [4095])
