@@ -283,3 +283,34 @@ def test_lse_entries_reject_bad_arguments():
     assert lib.ra_merge_lse(0, 8, None, None, None, None, None) == _lib.RA_OK
     assert lib.ra_stats_to_lse(4, None, 16, 16, None) == _lib.RA_ERR_INVALID
     assert lib.ra_stats_to_lse(0, None, None, None, None) == _lib.RA_OK
+
+
+def test_binding_structs_match_the_header_layout(tmp_path):
+    """Every ctypes struct of the binding has the size and field offsets the
+    C compiler gives the header's struct (a drift would pass garbage through
+    the ABI without any error)."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    pairs = {"ra_span": _lib.Span, "ra_positions": _lib.Positions, "ra_strides": _lib.Strides,
+             "ra_kv_chunk": _lib.KvChunk, "ra_kv_grad": _lib.KvGrad, "ra_q_segment": _lib.QSegment,
+             "ra_problem": _lib.Problem}
+    lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "ra.h"', "int main(void) {"]
+    for cname, cls in pairs.items():
+        lines.append(f'  printf("{cname} size %zu\\n", sizeof({cname}));')
+        for fname, _ in cls._fields_:
+            lines.append(f'  printf("{cname} {fname} %zu\\n", offsetof({cname}, {fname}));')
+    lines += ["  return 0;", "}"]
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines) + "\n")
+    exe = tmp_path / "layout"
+    subprocess.check_call([cc, "-std=c11", "-I", os.path.join(ROOT, "include"), str(src), "-o",
+                           str(exe)])
+    out = subprocess.check_output([str(exe)], text=True).split("\n")
+    got = {tuple(x.split()[:2]): int(x.split()[2]) for x in out if x}
+    for cname, cls in pairs.items():
+        assert got[(cname, "size")] == ctypes.sizeof(cls), cname
+        for fname, _ in cls._fields_:
+            assert got[(cname, fname)] == getattr(cls, fname).offset, (cname, fname)
