@@ -173,6 +173,11 @@ def test_segment_work_with_documents_is_exact(kind, causal):
         assert sum(tiles) < sum(tiles_plain)
     with pytest.raises(ValueError):
         segment_work(1, 4, 4, 128, segs, [n // P] * P, rs, causal, docs=[0])
+    # the most documents a call takes: 512 of 8 positions each
+    many = list(range(0, n + 1, 8))
+    assert len(many) - 1 == 512
+    pairs512, _ = segment_work(1, 4, 4, 128, segs, [n // P] * P, rs, causal, docs=many)
+    assert sum(pairs512) == (512 * (8 * 9 // 2) if causal else 512 * 64)
     # keys outside the documents are rejected, as by the launches
     with pytest.raises(_lib.RaError):
         segment_work(1, 4, 4, 128, segs, [n // P] * P, rs, causal, docs=docs[:-1] + [4095])
