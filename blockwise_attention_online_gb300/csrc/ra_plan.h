@@ -189,9 +189,15 @@ struct SimtPlan {
 };
 static_assert(sizeof(SimtPlan) <= 32000, "fp32 plan must fit the parameter space");
 
+// Bytes of stream-K scratch for a grid of `grid` CTAs: the raw O slots
+// ([grid][2][128][D] fp32), the row statistics ([grid][2][128] float4) and the
+// flags ([grid][2] u32), plus alignment slack.
+constexpr size_t tc_scratch_bytes(int grid, int D) {
+  return size_t(grid) * 2 * 128 * (size_t(D) * 4 + 16) + size_t(grid) * 2 * 4 + 256;
+}
+
 // Kernel launchers (defined in the .cu files; return a cudaError_t as int).
 int launch_tc_bf16(const TcPlan& plan, int D, void* stream);
-size_t tc_scratch_bytes(int grid, int D);
 void tc_scratch_carve(void* base, int grid, int D, TcScratch* s);
 // Device address of the fixed scratch array used by ra_ring_attention_noalloc
 // on the current device (looked up once per device); returns a cudaError_t.

@@ -38,6 +38,7 @@
 // a code in a device status word, tells its other warps to stop, waits for its
 // own copies and MMAs in flight, frees TMEM and returns.
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 #include <stdint.h>
 
 #include <mutex>
@@ -54,6 +55,9 @@ namespace ra {
 // Host code must not use its name as a pointer: the device address comes from
 // cudaGetSymbolAddress below.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[RA_NOALLOC_SCRATCH_BYTES];
+// the largest split (one CTA per SM of the widest grid, head_dim 128) fits
+static_assert(tc_scratch_bytes(kTcMaxGrid, 128) <= RA_NOALLOC_SCRATCH_BYTES,
+              "the fixed scratch array must hold the largest stream-K split");
 
 namespace {
 
@@ -890,10 +894,6 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ring_kernel(const __grid_const
 
 }  // namespace
 
-size_t tc_scratch_bytes(int grid, int D) {
-  return size_t(grid) * 2 * 128 * (size_t(D) * 4 + 16) + size_t(grid) * 2 * 4 + 256;
-}
-
 void tc_scratch_carve(void* base, int grid, int D, TcScratch* s) {
   char* b = static_cast<char*>(base);
   s->o = reinterpret_cast<float*>(b);
@@ -933,20 +933,51 @@ int launch_tc_bf16(const TcPlan& plan, int D, void* stream) {
   }
 }
 
+// Unique id of the calling thread's current CUDA context (0 if none is
+// current or the driver cannot say). Context ids are never reused within a
+// process, so a device reset, which replaces the primary context, changes it.
+static unsigned long long current_context_id() {
+  static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+  static PFN_cuCtxGetId_v12000 get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 4000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(fn);
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(fn);
+  });
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return 0;
+  if (get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
+// The array's device address in the current context. The lookup runs once
+// per device and context (with that device current); a cached address is
+// reused only while the same context is current, so a device reset leads to
+// a fresh lookup instead of a stale pointer.
 int tc_static_scratch(void** ptr, size_t* bytes) {
   constexpr int kMaxDevices = 64;
   static std::mutex mu;
   static void* addr[kMaxDevices] = {};
+  static unsigned long long ctx_of[kMaxDevices] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lock(mu);
-  if (addr[dev] == nullptr) {  // once per device, with that device current
+  const unsigned long long ctx = current_context_id();
+  if (addr[dev] == nullptr || ctx == 0 || ctx != ctx_of[dev]) {
     void* a = nullptr;
-    e = cudaGetSymbolAddress(&a, g_noalloc_scratch);
+    e = cudaGetSymbolAddress(&a, g_noalloc_scratch);  // makes the context current if needed
     if (e != cudaSuccess) return e;
     addr[dev] = a;
+    ctx_of[dev] = current_context_id();
   }
   *ptr = addr[dev];
   *bytes = sizeof(g_noalloc_scratch);

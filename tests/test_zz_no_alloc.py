@@ -64,3 +64,64 @@ def test_noalloc_matches_allocating_entry_point_twice(seed, Hq, Hkv, S, causal, 
         # same kernel, same schedule: the results are identical
         for a, b in zip(got, ref):
             assert torch.equal(a, b)
+
+
+_CHILD = r"""
+import ctypes, json, sys
+import torch
+sys.path.insert(0, sys.argv[1])
+sys.path.insert(0, sys.argv[2])
+from blockwise_attention_online_gb300 import _lib
+from blockwise_attention_online_gb300.api import _chunks, _problem, _segments, _stream, _strides
+lib = _lib.load()
+g = torch.Generator(device="cpu").manual_seed(33)
+Hq, S, D = 4, 2304, 128
+q = torch.randn(1, Hq, S, D, generator=g).to(torch.bfloat16).cuda()
+k = torch.randn(1, Hq, S, D, generator=g).to(torch.bfloat16).cuda()
+v = torch.randn(1, Hq, S, D, generator=g).to(torch.bfloat16).cuda()
+kc = [t.contiguous() for t in torch.split(k, [1024, 1280], dim=2)]
+vc = [t.contiguous() for t in torch.split(v, [1024, 1280], dim=2)]
+outs = [(torch.empty_like(q), torch.empty(1, Hq, S, device="cuda"), torch.empty(1, Hq, S, device="cuda"))
+        for _ in range(3)]
+def call(entry, o):
+    pb = _problem(q, Hq, False, None, _strides(o[0]))
+    segs, nsegs = _segments(q, None)
+    chs, nch = _chunks(kc, vc, None)
+    _lib.check(getattr(lib, entry)(ctypes.byref(pb), q.data_ptr(), segs, nsegs, chs, nch,
+                                   o[0].data_ptr(), o[1].data_ptr(), o[2].data_ptr(), _stream(None)))
+    _lib.check(lib.ra_device_status(_stream(None)))
+call("ra_ring_attention_noalloc", outs[0])   # first call: the one-time address lookup
+torch.cuda.synchronize()
+free0 = torch.cuda.mem_get_info()[0]
+call("ra_ring_attention_noalloc", outs[1])
+call("ra_ring_attention_noalloc", outs[2])
+torch.cuda.synchronize()
+free1 = torch.cuda.mem_get_info()[0]
+call("ra_ring_attention", outs[2])           # allocating entry point: its pool keeps the scratch
+torch.cuda.synchronize()
+free2 = torch.cuda.mem_get_info()[0]
+print(json.dumps({"free0": free0, "free1": free1, "free2": free2,
+                  "same": all(torch.equal(a, b) for a, b in zip(outs[0], outs[1]))}))
+"""
+
+
+def test_noalloc_allocates_nothing_in_a_fresh_process():
+    """The point of the entry point: after its first call on a device, calls
+    leave the device's free memory unchanged (no allocation, not even a
+    stream-ordered one), while the allocating entry point's split launch on
+    the same problem does take memory from its pool. Run in a fresh process so
+    that nothing else has created the library's pool before."""
+    import json
+    import os
+    import subprocess
+    import sys
+    here = os.path.dirname(os.path.abspath(__file__))
+    root = os.path.dirname(here)
+    r = subprocess.run([sys.executable, "-c", _CHILD, root, here], capture_output=True,
+                       text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    res = json.loads(r.stdout.strip().splitlines()[-1])
+    assert res["same"]
+    assert res["free1"] == res["free0"], res
+    # the same problem through ra_ring_attention does allocate (so the check can see one)
+    assert res["free2"] < res["free1"], res
