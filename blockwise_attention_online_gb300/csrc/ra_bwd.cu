@@ -72,13 +72,36 @@ struct BwdCfg {
   static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 };
 
+// Chunk tables: the plan's own arrays, or their device-resident copies.
+__device__ __forceinline__ const KvSeg& bspan(const BwdPlan& p, int k) {
+  return p.ext_ks ? p.ext_ks[k] : p.ks[k];
+}
+__device__ __forceinline__ int btile_begin(const BwdPlan& p, int k) {
+  return p.ext_ktb ? p.ext_ktb[k] : p.kseg_tile_begin[k];
+}
+__device__ __forceinline__ const CUtensorMap* bkmap(const BwdPlan& p, int c) {
+  return p.ext_kmap ? p.ext_kmap + c : &p.kmap[c];
+}
+__device__ __forceinline__ const CUtensorMap* bvmap(const BwdPlan& p, int c) {
+  return p.ext_vmap ? p.ext_vmap + c : &p.vmap[c];
+}
+// Before the first TMA copy through a chunk's maps: device-resident maps
+// were written by a copy from the host (generic proxy).
+__device__ __forceinline__ void bwd_fence_maps(const BwdPlan& p, int c) {
+  if (p.ext_kmap != nullptr) {
+    fence_tmap_acquire(p.ext_kmap + c);
+    fence_tmap_acquire(p.ext_vmap + c);
+  }
+}
+
 __device__ __forceinline__ int bwd_row_position(const BwdPlan& p, int row) {
+  const QPiece* qp = p.ext_qp ? p.ext_qp : p.qp;
   int lo = 0, hi = p.n_qpieces - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if (p.qp[mid].row0 <= row) lo = mid; else hi = mid - 1;
+    if (qp[mid].row0 <= row) lo = mid; else hi = mid - 1;
   }
-  const QPiece& q = p.qp[lo];
+  const QPiece& q = qp[lo];
   return q.pos0 + q.step * (row - q.row0);
 }
 
@@ -86,7 +109,7 @@ __device__ __forceinline__ int bwd_row_position(const BwdPlan& p, int row) {
 // [lo, hi] of some row of a query tile.
 __device__ __forceinline__ void bwd_live_tiles(const BwdPlan& p, int k, int lo, int hi, int& tb,
                                                int& te) {
-  const KvSeg& s = p.ks[k];
+  const KvSeg& s = bspan(p, k);
   if (!p.causal && p.n_docs == 0) {
     tb = 0;
     te = s.ntiles;
@@ -291,10 +314,16 @@ __device__ __forceinline__ void bwd_dkv_tile(const BwdPlan& p, int cta) {
   const int gt = u % p.n_ktiles;
   u /= p.n_ktiles;
   const int hkv = u % p.Hkv, b = u / p.Hkv;
-  int ks = 0;
-  while (ks + 1 < p.n_kvsegs && p.kseg_tile_begin[ks + 1] <= gt) ++ks;
-  const KvSeg& sg = p.ks[ks];
-  const int kt = gt - p.kseg_tile_begin[ks];
+  int ks = 0;  // last span whose first tile is at or before gt
+  {
+    int hi = p.n_kvsegs - 1;
+    while (ks < hi) {
+      const int mid = (ks + hi + 1) >> 1;
+      if (btile_begin(p, mid) <= gt) ks = mid; else hi = mid - 1;
+    }
+  }
+  const KvSeg& sg = bspan(p, ks);
+  const int kt = gt - btile_begin(p, ks);
   const int krow0 = sg.row0 + 128 * kt;                 // first row within the chunk
   const int kvalid = min(128, sg.len - 128 * kt);       // rows of the tile that exist
   const int kmin = sg.pos0 + sg.step * (128 * kt);
@@ -306,11 +335,12 @@ __device__ __forceinline__ void bwd_dkv_tile(const BwdPlan& p, int cta) {
     // ---------------------------------------------------------- producer
     const bool leader = elect_one();
     if (leader) {
+      bwd_fence_maps(p, sg.chunk);
       mbar_arrive_expect_tx(bb.res_full, 2 * C::kTileBytes);
 #pragma unroll
       for (int bx = 0; bx < C::kBoxes; ++bx) {
-        tma_load_4d(sK + bx * C::kBoxBytes, &p.kmap[sg.chunk], bb.res_full, bx * 64, krow0, hkv, b);
-        tma_load_4d(sV + bx * C::kBoxBytes, &p.vmap[sg.chunk], bb.res_full, bx * 64, krow0, hkv, b);
+        tma_load_4d(sK + bx * C::kBoxBytes, bkmap(p, sg.chunk), bb.res_full, bx * 64, krow0, hkv, b);
+        tma_load_4d(sV + bx * C::kBoxBytes, bvmap(p, sg.chunk), bb.res_full, bx * 64, krow0, hkv, b);
       }
     }
     QWalk<kDocs> w{0, g * p.n_qtiles, p.n_qtiles, hkv * g};
@@ -499,9 +529,10 @@ __device__ __forceinline__ void bwd_dkv_tile(const BwdPlan& p, int cta) {
         tc_fence_after();
       }
       if (ok) {
-        const int64_t row = (int64_t(b) * p.Hkv + hkv) * p.chunk_len[sg.chunk] + krow0 + r;
-        float* dkr = p.dk[sg.chunk] + row * D;
-        float* dvr = p.dv[sg.chunk] + row * D;
+        const int clen = p.ext_chunk_len ? p.ext_chunk_len[sg.chunk] : p.chunk_len[sg.chunk];
+        const int64_t row = (int64_t(b) * p.Hkv + hkv) * clen + krow0 + r;
+        float* dkr = (p.ext_dk ? p.ext_dk[sg.chunk] : p.dk[sg.chunk]) + row * D;
+        float* dvr = (p.ext_dv ? p.ext_dv[sg.chunk] : p.dv[sg.chunk]) + row * D;
         // D / 32 column chunks, the first half of them (rounded up) to half 0
         constexpr int kNc = D / 32, kPer = (kNc + 1) / 2;
 #pragma unroll 1
@@ -578,8 +609,9 @@ __device__ __forceinline__ void bwd_dq_tile(const BwdPlan& p, int cta) {
     }
     int j = 0;
     bool ok = true;
+    int fenced = -1;
     for (int k = 0; ok && k < p.n_kvsegs; ++k) {
-      const KvSeg& sg = p.ks[k];
+      const KvSeg& sg = bspan(p, k);
       int tb, te;
       bwd_live_tiles(p, k, wlo, whi, tb, te);
       for (int t = tb; t < te; ++t) {
@@ -588,12 +620,16 @@ __device__ __forceinline__ void bwd_dq_tile(const BwdPlan& p, int cta) {
         if (!ok) break;
         const uint32_t sK = base + C::kStage0 + st * C::kStageBytes, sV = sK + C::kTileBytes;
         if (leader) {
+          if (sg.chunk != fenced) {
+            bwd_fence_maps(p, sg.chunk);
+            fenced = sg.chunk;
+          }
           mbar_arrive_expect_tx(bb.st_full0 + 8 * st, 2 * C::kTileBytes);
 #pragma unroll
           for (int bx = 0; bx < C::kBoxes; ++bx) {
-            tma_load_4d(sK + bx * C::kBoxBytes, &p.kmap[sg.chunk], bb.st_full0 + 8 * st, bx * 64,
+            tma_load_4d(sK + bx * C::kBoxBytes, bkmap(p, sg.chunk), bb.st_full0 + 8 * st, bx * 64,
                         sg.row0 + 128 * t, hkv, b);
-            tma_load_4d(sV + bx * C::kBoxBytes, &p.vmap[sg.chunk], bb.st_full0 + 8 * st, bx * 64,
+            tma_load_4d(sV + bx * C::kBoxBytes, bvmap(p, sg.chunk), bb.st_full0 + 8 * st, bx * 64,
                         sg.row0 + 128 * t, hkv, b);
           }
         }
@@ -664,7 +700,7 @@ __device__ __forceinline__ void bwd_dq_tile(const BwdPlan& p, int cta) {
     int j = 0;
     bool ok = true;
     for (int k = 0; ok && k < p.n_kvsegs; ++k) {
-      const KvSeg& sg = p.ks[k];
+      const KvSeg& sg = bspan(p, k);
       int tb, te;
       bwd_live_tiles(p, k, wlo, whi, tb, te);
       for (int t = tb; t < te; ++t) {

@@ -200,9 +200,9 @@ ra_status validate(const ra_problem* pb, const void* q, const ra_q_segment* segs
     }
     c->chunk_begin.push_back(int(c->kvspans.size()));
   }
-  if ((int64_t)c->qspans.size() > ra::kMaxQPieces)
+  if ((int64_t)c->qspans.size() > ra::kTcMaxQPiecesAll)
     return fail(RA_ERR_UNSUPPORTED, "%zu query spans exceed the limit of %d",
-                c->qspans.size(), ra::kMaxQPieces);
+                c->qspans.size(), ra::kTcMaxQPiecesAll);
   return check_docs(p, c);
 }
 
@@ -349,11 +349,18 @@ void fill_docs(const Common& c, int32_t* bounds, int32_t* n) {
   for (size_t i = 0; i < c.doc_bounds.size(); ++i) bounds[i] = c.doc_bounds[i];
 }
 
-void fill_q_pieces(const Common& c, ra::QPiece* qp, int32_t* n) {
+// Query spans into `qp` (the plan's array when they fit, else `ext`, a
+// byte buffer bound for device memory).
+void fill_q_pieces(const Common& c, ra::QPiece* qp, int32_t* n, unsigned char* ext = nullptr) {
   *n = (int32_t)c.qspans.size();
   for (size_t i = 0; i < c.qspans.size(); ++i) {
     const Span& s = c.qspans[i];
-    qp[i] = {int32_t(s.row0), int32_t(s.len), int32_t(s.pos0), int32_t(s.step), s.owner};
+    const ra::QPiece piece = {int32_t(s.row0), int32_t(s.len), int32_t(s.pos0), int32_t(s.step),
+                              s.owner};
+    if (ext)
+      std::memcpy(ext + i * sizeof(ra::QPiece), &piece, sizeof(piece));
+    else
+      qp[i] = piece;
   }
 }
 
@@ -366,12 +373,16 @@ ra_status run_tc(const Common& c, const ra_problem& p, const void* q,
                  const ra_kv_chunk* chunks, void* out, float* m, float* l,
                  bool stats_mode, void* stream, ScratchSource source,
                  const BeforeLaunch& before_launch) {
-  if (c.nchunks > ra::kTcMaxChunks)
+  if (c.nchunks > ra::kTcMaxChunksAll)
     return fail(RA_ERR_UNSUPPORTED, "bf16 path handles at most %d chunks, got %d",
-                ra::kTcMaxChunks, c.nchunks);
-  if ((int)c.kvspans.size() > ra::kTcMaxKvSegs)
+                ra::kTcMaxChunksAll, c.nchunks);
+  if ((int)c.kvspans.size() > ra::kTcMaxKvSegsAll)
     return fail(RA_ERR_UNSUPPORTED, "bf16 path handles at most %d chunk spans, got %zu",
-                ra::kTcMaxKvSegs, c.kvspans.size());
+                ra::kTcMaxKvSegsAll, c.kvspans.size());
+  // chunk tables that do not fit the plan go to device memory
+  const bool ext_tables = c.nchunks > ra::kTcMaxChunks ||
+                          (int)c.kvspans.size() > ra::kTcMaxKvSegs ||
+                          (int)c.qspans.size() > ra::kMaxQPieces;
   ra_status st;
   if (!aligned16(q)) return fail(RA_ERR_INVALID, "q must be 16-byte aligned");
   if (!aligned16(out)) return fail(RA_ERR_INVALID, "output must be 16-byte aligned");
@@ -397,11 +408,25 @@ ra_status run_tc(const Common& c, const ra_problem& p, const void* q,
   if ((st = make_map(&plan.qmap, q, c.D, std::max<int64_t>(c.Sq, 1), c.Hq, c.B,
                      p.q_strides, "q")) != RA_OK)
     return st;
+  // device-resident tables are assembled here and copied in right before the
+  // launch (the copy from pageable memory is staged, so this buffer may be
+  // reused as soon as the copy call returns)
+  static thread_local std::vector<unsigned char> tables;
+  static thread_local std::vector<CUtensorMap> ext_maps;
+  const ra::TcTablesLayout lay =
+      ra::TcTablesLayout::of(ext_tables ? c.nchunks : 0, ext_tables ? int(c.kvspans.size()) : 0,
+                             ext_tables ? int(c.qspans.size()) : 0);
+  if (ext_tables) {
+    ext_maps.assign(size_t(2) * c.nchunks, CUtensorMap{});
+    tables.assign(lay.bytes, 0);
+  }
   for (int k = 0; k < c.nchunks; ++k) {
     const ra_kv_chunk& ch = chunks[k];
     if (ch.len == 0) continue;
-    if ((st = make_map(&plan.kmap[k], ch.k, c.D, ch.len, c.Hkv, c.B, ch.k_strides, "k")) != RA_OK) return st;
-    if ((st = make_map(&plan.vmap[k], ch.v, c.D, ch.len, c.Hkv, c.B, ch.v_strides, "v")) != RA_OK) return st;
+    CUtensorMap* km = ext_tables ? &ext_maps[k] : &plan.kmap[k];
+    CUtensorMap* vm = ext_tables ? &ext_maps[c.nchunks + k] : &plan.vmap[k];
+    if ((st = make_map(km, ch.k, c.D, ch.len, c.Hkv, c.B, ch.k_strides, "k")) != RA_OK) return st;
+    if ((st = make_map(vm, ch.v, c.D, ch.len, c.Hkv, c.B, ch.v_strides, "v")) != RA_OK) return st;
   }
   plan.out = out; plan.m = m; plan.l = l;
   plan.o_sb = p.o_strides.batch; plan.o_sh = p.o_strides.head; plan.o_sr = p.o_strides.row;
@@ -421,15 +446,26 @@ ra_status run_tc(const Common& c, const ra_problem& p, const void* q,
   plan.scale = c.scale;
   plan.scale_log2 = float(double(c.scale) * 1.4426950408889634);
   plan.o_fp32 = out_f32 ? 1 : 0;
-  fill_q_pieces(c, plan.qp, &plan.n_qpieces);
+  fill_q_pieces(c, plan.qp, &plan.n_qpieces, ext_tables ? tables.data() + lay.qp : nullptr);
   fill_docs(c, plan.doc_bounds, &plan.n_docs);
   plan.n_kvsegs = int32_t(c.kvspans.size());
-  for (size_t i = 0; i < c.kvspans.size(); ++i) {
-    const Span& s = c.kvspans[i];
-    plan.ks[i] = {s.owner, int32_t(s.row0), int32_t(s.len), int32_t(s.pos0), int32_t(s.step),
-                  int32_t((s.len + 127) / 128)};
+  if (ext_tables) {
+    std::memcpy(tables.data() + lay.kmap, ext_maps.data(), size_t(2) * c.nchunks * sizeof(CUtensorMap));
+    for (size_t i = 0; i < c.kvspans.size(); ++i) {
+      const Span& s = c.kvspans[i];
+      const ra::KvSeg kv = {s.owner, int32_t(s.row0), int32_t(s.len), int32_t(s.pos0),
+                            int32_t(s.step), int32_t((s.len + 127) / 128)};
+      std::memcpy(tables.data() + lay.ks + i * sizeof(ra::KvSeg), &kv, sizeof(kv));
+    }
+    std::memcpy(tables.data() + lay.csb, c.chunk_begin.data(), size_t(c.nchunks + 1) * sizeof(int32_t));
+  } else {
+    for (size_t i = 0; i < c.kvspans.size(); ++i) {
+      const Span& s = c.kvspans[i];
+      plan.ks[i] = {s.owner, int32_t(s.row0), int32_t(s.len), int32_t(s.pos0), int32_t(s.step),
+                    int32_t((s.len + 127) / 128)};
+    }
+    for (int k = 0; k <= c.nchunks; ++k) plan.chunk_seg_begin[k] = c.chunk_begin[k];
   }
-  for (int k = 0; k <= c.nchunks; ++k) plan.chunk_seg_begin[k] = c.chunk_begin[k];
 
   const int64_t npairs = (c.Sq + ra::kTcRowsPerUnit - 1) / ra::kTcRowsPerUnit;
   plan.n_qpairs = int32_t(npairs);
@@ -519,45 +555,66 @@ ra_status run_tc(const Common& c, const ra_problem& p, const void* q,
   unsigned ep = ++epoch_counter;
   if (ep == 0) ep = ++epoch_counter;
   plan.epoch = ep;
-  void* scratch = nullptr;
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
-  if (split && source == ScratchSource::kStatic) {
-    const size_t bytes = ra::tc_scratch_bytes(int(G), int(c.D));
-    void* base = nullptr;
-    size_t cap = 0;
-    cudaError_t e = static_cast<cudaError_t>(ra::tc_static_scratch(&base, &cap));
-    if (e != cudaSuccess) return cuda_status(e, "looking up the fixed scratch array");
-    if (bytes > cap)
-      return fail(RA_ERR_UNSUPPORTED, "split needs %zu bytes of scratch, the fixed array holds %zu",
-                  bytes, cap);
-    ra::tc_scratch_carve(base, int(G), int(c.D), &plan.scratch);
-    if (before_launch && (st = before_launch()) != RA_OK) return st;
-    // the array keeps the previous call's contents: clear the flags
-    e = cudaMemsetAsync(plan.scratch.flags, 0, size_t(G) * 2 * sizeof(unsigned), cs);
-    if (e != cudaSuccess) return cuda_status(e, "clearing stream-K flags");
-    return cuda_status(ra::launch_tc_bf16(plan, int(c.D), stream), "bf16 ring kernel launch");
+  const size_t scratch_bytes = split ? ra::tc_scratch_bytes(int(G), int(c.D)) : 0;
+  const size_t tables_bytes = ext_tables ? lay.bytes : 0;
+  // Device memory of this launch: the stream-K scratch at the start, the
+  // chunk tables at the end; from the library pool (freed again after the
+  // launch, stream-ordered) or from the fixed array (no allocation).
+  char* mem = nullptr;
+  size_t tables_off = 0;
+  bool pooled = false;
+  if (scratch_bytes + tables_bytes > 0) {
+    if (source == ScratchSource::kStatic) {
+      void* base = nullptr;
+      size_t cap = 0;
+      cudaError_t e = static_cast<cudaError_t>(ra::tc_static_scratch(&base, &cap));
+      if (e != cudaSuccess) return cuda_status(e, "looking up the fixed scratch array");
+      mem = static_cast<char*>(base);
+      tables_off = (scratch_bytes + 255) & ~size_t(255);
+      if (tables_off + tables_bytes > cap)
+        return fail(RA_ERR_UNSUPPORTED,
+                    "the launch needs %zu bytes of scratch and chunk tables, the fixed array holds %zu",
+                    tables_off + tables_bytes, cap);
+    } else {
+      cudaMemPool_t pool = nullptr;
+      if ((st = lib_pool(&pool)) != RA_OK) return st;
+      tables_off = (scratch_bytes + 255) & ~size_t(255);
+      cudaError_t e = cudaMallocFromPoolAsync(reinterpret_cast<void**>(&mem),
+                                              tables_off + tables_bytes, pool, cs);
+      if (e != cudaSuccess) return cuda_status(e, "allocating stream-K scratch and chunk tables");
+      pooled = true;
+    }
   }
-  if (split) {
-    const size_t bytes = ra::tc_scratch_bytes(int(G), int(c.D));
-    cudaMemPool_t pool = nullptr;
-    if ((st = lib_pool(&pool)) != RA_OK) return st;
-    cudaError_t e = cudaMallocFromPoolAsync(&scratch, bytes, pool, cs);
-    if (e != cudaSuccess) return cuda_status(e, "allocating stream-K scratch");
-    ra::tc_scratch_carve(scratch, int(G), int(c.D), &plan.scratch);
-    if (before_launch && (st = before_launch()) != RA_OK) {
-      cudaFreeAsync(scratch, cs);
-      return st;
-    }
-    e = cudaMemsetAsync(plan.scratch.flags, 0, size_t(G) * 2 * sizeof(unsigned), cs);
-    if (e != cudaSuccess) {
-      cudaFreeAsync(scratch, cs);
-      return cuda_status(e, "clearing stream-K flags");
-    }
-  } else if (before_launch && (st = before_launch()) != RA_OK) {
+  auto release = [&] {
+    if (pooled) cudaFreeAsync(mem, cs);
+  };
+  if (split) ra::tc_scratch_carve(mem, int(G), int(c.D), &plan.scratch);
+  if (ext_tables) {
+    char* t = mem + tables_off;
+    plan.ext_kmap = reinterpret_cast<const CUtensorMap*>(t + lay.kmap);
+    plan.ext_vmap = reinterpret_cast<const CUtensorMap*>(t + lay.vmap);
+    plan.ext_ks = reinterpret_cast<const ra::KvSeg*>(t + lay.ks);
+    plan.ext_csb = reinterpret_cast<const int32_t*>(t + lay.csb);
+    plan.ext_qp = reinterpret_cast<const ra::QPiece*>(t + lay.qp);
+  }
+  if (before_launch && (st = before_launch()) != RA_OK) {
+    release();
     return st;
   }
+  cudaError_t e = cudaSuccess;
+  if (ext_tables)
+    e = cudaMemcpyAsync(mem + tables_off, tables.data(), tables_bytes, cudaMemcpyHostToDevice, cs);
+  // the flags of split units must start cleared (the fixed array keeps the
+  // previous call's contents; a pool block may hold anything)
+  if (e == cudaSuccess && split)
+    e = cudaMemsetAsync(plan.scratch.flags, 0, size_t(G) * 2 * sizeof(unsigned), cs);
+  if (e != cudaSuccess) {
+    release();
+    return cuda_status(e, "preparing the launch");
+  }
   const int err = ra::launch_tc_bf16(plan, int(c.D), stream);
-  if (scratch) cudaFreeAsync(scratch, cs);
+  release();
   return cuda_status(err, "bf16 ring kernel launch");
 }
 
@@ -571,6 +628,9 @@ ra_status run_simt(const Common& c, const ra_problem& p, const void* q,
   if ((int)c.kvspans.size() > ra::kSimtMaxKvSegs)
     return fail(RA_ERR_UNSUPPORTED, "fp32 path handles at most %d chunk spans, got %zu",
                 ra::kSimtMaxKvSegs, c.kvspans.size());
+  if ((int)c.qspans.size() > ra::kMaxQPieces)
+    return fail(RA_ERR_UNSUPPORTED, "fp32 path handles at most %d query spans, got %zu",
+                ra::kMaxQPieces, c.qspans.size());
   static thread_local ra::SimtPlan plan;
   std::memset(&plan, 0, sizeof(plan));
   plan.q = static_cast<const float*>(q);
@@ -638,12 +698,15 @@ ra_status run_bwd(const ra_problem* pb, const void* q, const ra_q_segment* segs,
   for (int32_t k = 0; k < nchunks; ++k)
     if (chunks[k].len > 0 && (!grads[k].dk || !grads[k].dv))
       return fail(RA_ERR_INVALID, "chunk %d: NULL dk or dv", k);
-  if (c.nchunks > ra::kTcMaxChunks)
+  if (c.nchunks > ra::kTcMaxChunksAll)
     return fail(RA_ERR_UNSUPPORTED, "bf16 path handles at most %d chunks, got %d",
-                ra::kTcMaxChunks, c.nchunks);
-  if ((int)c.kvspans.size() > ra::kTcMaxKvSegs)
+                ra::kTcMaxChunksAll, c.nchunks);
+  if ((int)c.kvspans.size() > ra::kTcMaxKvSegsAll)
     return fail(RA_ERR_UNSUPPORTED, "bf16 path handles at most %d chunk spans, got %zu",
-                ra::kTcMaxKvSegs, c.kvspans.size());
+                ra::kTcMaxKvSegsAll, c.kvspans.size());
+  const bool ext_tables = c.nchunks > ra::kTcMaxChunks ||
+                          (int)c.kvspans.size() > ra::kTcMaxKvSegs ||
+                          (int)c.qspans.size() > ra::kMaxQPieces;
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   if (c.Sq > 0) {
     if (!o || !dout || !m || !l || !dq) return fail(RA_ERR_INVALID, "o, dout, m, l or dq is NULL");
@@ -680,14 +743,35 @@ ra_status run_bwd(const ra_problem* pb, const void* q, const ra_q_segment* segs,
   if ((st = make_map(&plan.qmap, q, c.D, c.Sq, c.Hq, c.B, p.q_strides, "q")) != RA_OK) return st;
   if ((st = make_map(&plan.domap, dout, c.D, c.Sq, c.Hq, c.B, p.o_strides, "dout")) != RA_OK)
     return st;
+  // chunk tables: in the plan, or assembled here for device memory
+  const ra::BwdTablesLayout lay = ra::BwdTablesLayout::of(
+      ext_tables ? c.nchunks : 0, ext_tables ? int(c.kvspans.size()) : 0,
+      ext_tables ? int(c.qspans.size()) : 0);
+  static thread_local std::vector<CUtensorMap> ext_maps;
+  static thread_local std::vector<unsigned char> tables;
+  if (ext_tables) {
+    ext_maps.assign(size_t(2) * c.nchunks, CUtensorMap{});
+    tables.assign(lay.bytes, 0);
+  }
   for (int k = 0; k < c.nchunks; ++k) {
     const ra_kv_chunk& ch = chunks[k];
-    plan.chunk_len[k] = int32_t(ch.len);
+    const int32_t len = int32_t(ch.len);
+    float* dkp = ch.len ? grads[k].dk : nullptr;
+    float* dvp = ch.len ? grads[k].dv : nullptr;
+    if (ext_tables) {
+      std::memcpy(tables.data() + lay.len + k * sizeof(int32_t), &len, sizeof(len));
+      std::memcpy(tables.data() + lay.dk + k * sizeof(float*), &dkp, sizeof(dkp));
+      std::memcpy(tables.data() + lay.dv + k * sizeof(float*), &dvp, sizeof(dvp));
+    } else {
+      plan.chunk_len[k] = len;
+      plan.dk[k] = dkp;
+      plan.dv[k] = dvp;
+    }
     if (ch.len == 0) continue;
-    if ((st = make_map(&plan.kmap[k], ch.k, c.D, ch.len, c.Hkv, c.B, ch.k_strides, "k")) != RA_OK) return st;
-    if ((st = make_map(&plan.vmap[k], ch.v, c.D, ch.len, c.Hkv, c.B, ch.v_strides, "v")) != RA_OK) return st;
-    plan.dk[k] = grads[k].dk;
-    plan.dv[k] = grads[k].dv;
+    CUtensorMap* km = ext_tables ? &ext_maps[k] : &plan.kmap[k];
+    CUtensorMap* vm = ext_tables ? &ext_maps[c.nchunks + k] : &plan.vmap[k];
+    if ((st = make_map(km, ch.k, c.D, ch.len, c.Hkv, c.B, ch.k_strides, "k")) != RA_OK) return st;
+    if ((st = make_map(vm, ch.v, c.D, ch.len, c.Hkv, c.B, ch.v_strides, "v")) != RA_OK) return st;
   }
   plan.dq = dq;
   plan.timeout_ns = 2000000000ull;
@@ -699,19 +783,35 @@ ra_status run_bwd(const ra_problem* pb, const void* q, const ra_q_segment* segs,
   plan.causal = c.causal; plan.n_chunks = c.nchunks;
   plan.scale = c.scale;
   plan.scale_log2 = float(double(c.scale) * 1.4426950408889634);
-  fill_q_pieces(c, plan.qp, &plan.n_qpieces);
+  fill_q_pieces(c, plan.qp, &plan.n_qpieces, ext_tables ? tables.data() + lay.qp : nullptr);
   fill_docs(c, plan.doc_bounds, &plan.n_docs);
   plan.n_kvsegs = int32_t(c.kvspans.size());
-  int32_t tiles = 0;
+  int64_t tiles = 0;
   for (size_t i = 0; i < c.kvspans.size(); ++i) {
     const Span& sp = c.kvspans[i];
-    plan.ks[i] = {sp.owner, int32_t(sp.row0), int32_t(sp.len), int32_t(sp.pos0), int32_t(sp.step),
-                  int32_t((sp.len + 127) / 128)};
-    plan.kseg_tile_begin[i] = tiles;
-    tiles += plan.ks[i].ntiles;
+    const ra::KvSeg kv = {sp.owner, int32_t(sp.row0), int32_t(sp.len), int32_t(sp.pos0),
+                          int32_t(sp.step), int32_t((sp.len + 127) / 128)};
+    const int32_t t0 = int32_t(tiles);
+    if (ext_tables) {
+      std::memcpy(tables.data() + lay.ks + i * sizeof(ra::KvSeg), &kv, sizeof(kv));
+      std::memcpy(tables.data() + lay.ktb + i * sizeof(int32_t), &t0, sizeof(t0));
+    } else {
+      plan.ks[i] = kv;
+      plan.kseg_tile_begin[i] = t0;
+    }
+    tiles += kv.ntiles;
   }
-  plan.kseg_tile_begin[c.kvspans.size()] = tiles;
-  plan.n_ktiles = tiles;
+  if (tiles > (int64_t(1) << 30)) return fail(RA_ERR_UNSUPPORTED, "too many key tiles");
+  {
+    const int32_t tn = int32_t(tiles);
+    if (ext_tables)
+      std::memcpy(tables.data() + lay.ktb + c.kvspans.size() * sizeof(int32_t), &tn, sizeof(tn));
+    else
+      plan.kseg_tile_begin[c.kvspans.size()] = tn;
+  }
+  if (ext_tables)
+    std::memcpy(tables.data() + lay.kmap, ext_maps.data(), size_t(2) * c.nchunks * sizeof(CUtensorMap));
+  plan.n_ktiles = int32_t(tiles);
   plan.n_qtiles = int32_t((c.Sq + 127) / 128);
   if (int64_t(plan.n_ktiles) * c.Hkv * c.B > (int64_t(1) << 31) - 1 ||
       int64_t(plan.n_qtiles) * c.Hq * c.B > (int64_t(1) << 31) - 1)
@@ -720,7 +820,8 @@ ra_status run_bwd(const ra_problem* pb, const void* q, const ra_q_segment* segs,
   // per query row: lse2, delta; per query tile: key window bounds
   const size_t rows = size_t(c.B * c.Hq * c.Sq);
   auto up = [](size_t n) { return (n + 255) & ~size_t(255); };
-  const size_t bytes = 2 * up(rows * 4) + up(size_t(plan.n_qtiles) * 16);
+  const size_t tables_off = 2 * up(rows * 4) + up(size_t(plan.n_qtiles) * 16);
+  const size_t bytes = tables_off + (ext_tables ? lay.bytes : 0);
   cudaMemPool_t pool = nullptr;
   if ((st = lib_pool(&pool)) != RA_OK) return st;
   char* scratch = nullptr;
@@ -732,6 +833,23 @@ ra_status run_bwd(const ra_problem* pb, const void* q, const ra_q_segment* segs,
   plan.lse2 = lse2;
   plan.delta = delta;
   plan.qtile_pos = qtile_pos;
+  if (ext_tables) {
+    char* t = scratch + tables_off;
+    plan.ext_kmap = reinterpret_cast<const CUtensorMap*>(t + lay.kmap);
+    plan.ext_vmap = reinterpret_cast<const CUtensorMap*>(t + lay.vmap);
+    plan.ext_dk = reinterpret_cast<float* const*>(t + lay.dk);
+    plan.ext_dv = reinterpret_cast<float* const*>(t + lay.dv);
+    plan.ext_chunk_len = reinterpret_cast<const int32_t*>(t + lay.len);
+    plan.ext_ks = reinterpret_cast<const ra::KvSeg*>(t + lay.ks);
+    plan.ext_ktb = reinterpret_cast<const int32_t*>(t + lay.ktb);
+    plan.ext_qp = reinterpret_cast<const ra::QPiece*>(t + lay.qp);
+    // staged copy from pageable memory: the buffer may be reused once it returns
+    e = cudaMemcpyAsync(t, tables.data(), lay.bytes, cudaMemcpyHostToDevice, cs);
+    if (e != cudaSuccess) {
+      cudaFreeAsync(scratch, cs);
+      return cuda_status(e, "copying the chunk tables");
+    }
+  }
   const bool o_f32 = p.o_fp32 == 1;
   const int err = ra::launch_bwd_bf16(plan, int(c.D), o, o_f32 ? 1 : 0, p.o_strides.batch,
                                       p.o_strides.head, p.o_strides.row, dout, m, l, lse2, delta,

@@ -78,8 +78,14 @@ RA_HD void live_range(int pos0, int step, int len, int lo, int hi, int& tb, int&
 }
 
 // ---------------------------------------------------------------- bf16 path
+// Chunk tables that fit the plan itself (the common case: no extra memory, no
+// copy). Larger problems, up to kTcMaxChunksAll chunks and kTcMaxKvSegsAll
+// spans, keep the same tables in device memory (TcTables).
 constexpr int kTcMaxChunks = 32;
 constexpr int kTcMaxKvSegs = 64;
+constexpr int kTcMaxChunksAll = 4096;
+constexpr int kTcMaxKvSegsAll = 8192;
+constexpr int kTcMaxQPiecesAll = 8192;  // query spans (the plan holds kMaxQPieces)
 constexpr int kTcMaxOrder = 8192;  // q-tile pairs that can be LPT-ordered
 constexpr int kTcRowsPerUnit = 256;  // two 128-row query tiles per work unit
 constexpr int kTcMaxSkUnits = 320;   // units in the stream-K tail (< 2 x grid)
@@ -123,9 +129,33 @@ struct alignas(128) TcPlan {
   KvSeg ks[kTcMaxKvSegs];
   int32_t n_docs;                    // 0: no document mask
   int32_t doc_bounds[kMaxDocs + 1];
+  // Device-resident chunk tables (null: the plan's own kmap, vmap, ks and
+  // chunk_seg_begin hold them): tensor maps [n_chunks] each, spans
+  // [n_kvsegs], first span of every chunk [n_chunks + 1].
+  const CUtensorMap* ext_kmap;
+  const CUtensorMap* ext_vmap;
+  const KvSeg* ext_ks;
+  const int32_t* ext_csb;
+  const QPiece* ext_qp;              // query spans [n_qpieces] (null: qp)
   uint16_t order[kTcMaxOrder];       // q-pair visit order (longest first)
 };
 static_assert(sizeof(TcPlan) <= 32000, "bf16 plan must fit the parameter space");
+
+// Byte layout of device-resident chunk tables (tensor maps first, 128-byte
+// aligned): K maps, V maps, spans, first span per chunk.
+struct TcTablesLayout {
+  size_t kmap, vmap, ks, csb, qp, bytes;
+  static TcTablesLayout of(int n_chunks, int n_segs, int n_qpieces) {
+    TcTablesLayout t;
+    t.kmap = 0;
+    t.vmap = t.kmap + size_t(n_chunks) * sizeof(CUtensorMap);
+    t.ks = t.vmap + size_t(n_chunks) * sizeof(CUtensorMap);
+    t.csb = t.ks + size_t(n_segs) * sizeof(KvSeg);
+    t.qp = (t.csb + size_t(n_chunks + 1) * sizeof(int32_t) + 15) & ~size_t(15);
+    t.bytes = (t.qp + size_t(n_qpieces) * sizeof(QPiece) + 255) & ~size_t(255);
+    return t;
+  }
+};
 
 // ------------------------------------------------------- bf16 backward pass
 // Gradients of the ring pass (dQ, and dK, dV of every chunk) in fp32. The
@@ -157,8 +187,36 @@ struct alignas(128) BwdPlan {
   KvSeg ks[kTcMaxKvSegs];
   int32_t n_docs;                             // 0: no document mask
   int32_t doc_bounds[kMaxDocs + 1];
+  // Device-resident chunk tables (null: the plan's own arrays above), for
+  // problems with more chunks or spans than the plan holds.
+  const CUtensorMap* ext_kmap;                // [n_chunks]
+  const CUtensorMap* ext_vmap;                // [n_chunks]
+  float* const* ext_dk;                       // [n_chunks]
+  float* const* ext_dv;                       // [n_chunks]
+  const int32_t* ext_chunk_len;               // [n_chunks]
+  const KvSeg* ext_ks;                        // [n_kvsegs]
+  const int32_t* ext_ktb;                     // kseg_tile_begin [n_kvsegs + 1]
+  const QPiece* ext_qp;                       // [n_qpieces]
 };
 static_assert(sizeof(BwdPlan) <= 32000, "backward plan must fit the parameter space");
+
+// Byte layout of the backward's device-resident chunk tables.
+struct BwdTablesLayout {
+  size_t kmap, vmap, dk, dv, len, ks, ktb, qp, bytes;
+  static BwdTablesLayout of(int n_chunks, int n_segs, int n_qpieces) {
+    BwdTablesLayout t;
+    t.kmap = 0;
+    t.vmap = t.kmap + size_t(n_chunks) * sizeof(CUtensorMap);
+    t.dk = t.vmap + size_t(n_chunks) * sizeof(CUtensorMap);
+    t.dv = t.dk + size_t(n_chunks) * sizeof(float*);
+    t.len = t.dv + size_t(n_chunks) * sizeof(float*);
+    t.ks = (t.len + size_t(n_chunks) * sizeof(int32_t) + 15) & ~size_t(15);
+    t.ktb = t.ks + size_t(n_segs) * sizeof(KvSeg);
+    t.qp = (t.ktb + size_t(n_segs + 1) * sizeof(int32_t) + 15) & ~size_t(15);
+    t.bytes = (t.qp + size_t(n_qpieces) * sizeof(QPiece) + 255) & ~size_t(255);
+    return t;
+  }
+};
 
 // ---------------------------------------------------------------- fp32 path
 constexpr int kSimtMaxChunks = 256;

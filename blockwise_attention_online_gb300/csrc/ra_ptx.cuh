@@ -74,6 +74,15 @@ __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// Orders earlier writes of a tensor map in global memory (made through the
+// generic proxy, e.g. a copy from the host) before the tensor-map proxy reads
+// it for TMA copies. Maps passed as __grid_constant__ parameters need none.
+__device__ __forceinline__ void fence_tmap_acquire(const CUtensorMap* map) {
+  asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(
+                   reinterpret_cast<uint64_t>(map))
+               : "memory");
+}
+
 // 4-D tiled tensor load into shared memory, completion counted in bytes on `bar`.
 __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
                                             int32_t c0, int32_t c1, int32_t c2, int32_t c3) {

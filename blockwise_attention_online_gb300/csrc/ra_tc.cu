@@ -98,24 +98,44 @@ struct Unit {
   int lo, hi;  // key positions any row of the unit may see: [lo, hi]
 };
 
+// Query spans: the plan's own array, or its device-resident copy.
+__device__ __forceinline__ const QPiece& qpiece(const TcPlan& p, int i) {
+  return p.ext_qp ? p.ext_qp[i] : p.qp[i];
+}
+
 __device__ __forceinline__ int find_piece(const TcPlan& p, int row) {
   int lo = 0, hi = p.n_qpieces - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if (p.qp[mid].row0 <= row) lo = mid; else hi = mid - 1;
+    if (qpiece(p, mid).row0 <= row) lo = mid; else hi = mid - 1;
   }
   return lo;
 }
 
 __device__ __forceinline__ int row_position(const TcPlan& p, int row) {
-  const QPiece& q = p.qp[find_piece(p, row)];
+  const QPiece& q = qpiece(p, find_piece(p, row));
   return q.pos0 + q.step * (row - q.row0);
+}
+
+// Chunk tables: the plan's own arrays, or their device-resident copies when
+// the problem has more chunks or spans than the plan holds.
+__device__ __forceinline__ const KvSeg& span_of(const TcPlan& p, int k) {
+  return p.ext_ks ? p.ext_ks[k] : p.ks[k];
+}
+__device__ __forceinline__ int seg_begin(const TcPlan& p, int c) {
+  return p.ext_csb ? p.ext_csb[c] : p.chunk_seg_begin[c];
+}
+__device__ __forceinline__ const CUtensorMap* kmap_of(const TcPlan& p, int c) {
+  return p.ext_kmap ? p.ext_kmap + c : &p.kmap[c];
+}
+__device__ __forceinline__ const CUtensorMap* vmap_of(const TcPlan& p, int c) {
+  return p.ext_vmap ? p.ext_vmap + c : &p.vmap[c];
 }
 
 // Key tiles [tb, te) of span k that hold a position some row of the unit
 // may see (not entirely in its future, nor outside its documents).
 __device__ __forceinline__ void live_tiles(const TcPlan& p, int k, const Unit& U, int& tb, int& te) {
-  const KvSeg& s = p.ks[k];
+  const KvSeg& s = span_of(p, k);
   if (!p.causal && p.n_docs == 0) {
     tb = 0;
     te = s.ntiles;
@@ -134,10 +154,10 @@ __device__ __forceinline__ void decode_unit(const TcPlan& p, int u, Unit& U) {
   U.qrow0 = qpair * kTcRowsPerUnit;
   const int r1 = min(U.qrow0 + kTcRowsPerUnit, p.Sq);
   int i = find_piece(p, U.qrow0);
-  U.qseg = p.qp[i].seg;
+  U.qseg = qpiece(p, i).seg;
   int qmin = 0x7fffffff, qmax = -1;
-  for (; i < p.n_qpieces && p.qp[i].row0 < r1; ++i) {
-    const QPiece& q = p.qp[i];
+  for (; i < p.n_qpieces && qpiece(p, i).row0 < r1; ++i) {
+    const QPiece& q = qpiece(p, i);
     const int a = max(U.qrow0, q.row0), e = min(r1, q.row0 + q.len);
     qmin = min(qmin, q.pos0 + q.step * (a - q.row0));
     qmax = max(qmax, q.pos0 + q.step * (e - 1 - q.row0));
@@ -178,8 +198,8 @@ struct TileIter {
       }
       if (++s >= p.n_chunks) return;
       const int c = p.ring ? (U.qseg - s + p.n_chunks) % p.n_chunks : s;
-      ks = p.chunk_seg_begin[c] - 1;
-      ks_end = p.chunk_seg_begin[c + 1];
+      ks = seg_begin(p, c) - 1;
+      ks_end = seg_begin(p, c + 1);
       t = 0;
       nlive = 0;
     }
@@ -198,8 +218,8 @@ struct TileIter {
       }
       if (++s >= p.n_chunks) return false;
       const int c = p.ring ? (U.qseg - s + p.n_chunks) % p.n_chunks : s;
-      ks = p.chunk_seg_begin[c] - 1;
-      ks_end = p.chunk_seg_begin[c + 1];
+      ks = seg_begin(p, c) - 1;
+      ks_end = seg_begin(p, c + 1);
       t = 0;
       nlive = 0;
     }
@@ -341,10 +361,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ring_kernel(const __grid_const
   }
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&p.qmap);
-    for (int c = 0; c < p.n_chunks; ++c) {
-      if (p.chunk_seg_begin[c] != p.chunk_seg_begin[c + 1]) {
-        prefetch_tmap(&p.kmap[c]);
-        prefetch_tmap(&p.vmap[c]);
+    if (p.ext_kmap == nullptr) {
+      for (int c = 0; c < p.n_chunks; ++c) {
+        if (p.chunk_seg_begin[c] != p.chunk_seg_begin[c + 1]) {
+          prefetch_tmap(&p.kmap[c]);
+          prefetch_tmap(&p.vmap[c]);
+        }
       }
     }
   }
@@ -362,7 +384,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ring_kernel(const __grid_const
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {  // one thread waits and issues the copies
-      int it = 0, qn = 0;
+      int it = 0, qn = 0, fenced = -1;
       bool ok = true;
       Walker wk;
       wk.init(p);
@@ -388,8 +410,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ring_kernel(const __grid_const
         iter.seek(p, U, I.t0);
         int ks, t;
         for (int j = 0; ok && j < n && iter.next(p, U, ks, t); ++j) {
-          const KvSeg& sg = p.ks[ks];
+          const KvSeg& sg = span_of(p, ks);
           const int row = sg.row0 + 128 * t;
+          if (p.ext_kmap != nullptr && sg.chunk != fenced) {  // maps copied in from the host
+            fence_tmap_acquire(kmap_of(p, sg.chunk));
+            fence_tmap_acquire(vmap_of(p, sg.chunk));
+            fenced = sg.chunk;
+          }
 #pragma unroll
           for (int kv = 0; kv < 2; ++kv) {
             const int st = it % C::kStages;
@@ -399,7 +426,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ring_kernel(const __grid_const
             {
               const uint32_t full = b_kvfull0 + 8 * st;
               mbar_arrive_expect_tx(full, C::kTileBytes);
-              const CUtensorMap* map = kv == 0 ? &p.kmap[sg.chunk] : &p.vmap[sg.chunk];
+              const CUtensorMap* map = kv == 0 ? kmap_of(p, sg.chunk) : vmap_of(p, sg.chunk);
 #pragma unroll
               for (int bx = 0; bx < C::kBoxes; ++bx)
                 tma_load_4d(sKV + st * C::kTileBytes + bx * C::kBoxBytes, map, full, bx * 64, row,
@@ -578,7 +605,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ring_kernel(const __grid_const
           // before S arrives; C0 > 0 only where a document starts inside it)
           int L, C0 = 0;
           {
-            const KvSeg& sg = p.ks[ks];
+            const KvSeg& sg = span_of(p, ks);
             L = min(128, sg.len - 128 * t);
             if (p.causal || p.n_docs) {
               const int first = sg.pos0 + sg.step * (128 * t);

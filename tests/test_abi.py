@@ -109,10 +109,11 @@ def test_invalid_descriptors_rejected():
     # misaligned pointer for the TMA path
     assert _call(p, _segs(GOOD_SEGS), 1, _chunks(GOOD_CHUNKS, ptr=4098), 2) == _lib.RA_ERR_INVALID
     assert _call(p, _segs(GOOD_SEGS), 1, _chunks(GOOD_CHUNKS), 2, q=4100) == _lib.RA_ERR_INVALID
-    # too many chunks for the bf16 path
-    many = [(1, [(1, i, 1)]) for i in range(33)]
-    p2 = _problem(Sq=33)
-    assert _call(p2, _segs([(33, [(33, 0, 1)])]), 1, _chunks(many), 33) == _lib.RA_ERR_UNSUPPORTED
+    # too many chunks for the bf16 path (its device-resident tables hold 4096)
+    many = [(1, [(1, i, 1)]) for i in range(4097)]
+    p2 = _problem(Sq=4097)
+    assert _call(p2, _segs([(4097, [(4097, 0, 1)])]), 1, _chunks(many), 4097) == \
+        _lib.RA_ERR_UNSUPPORTED
     # NULL outputs
     assert _call(p, _segs(GOOD_SEGS), 1, _chunks(GOOD_CHUNKS), 2, o=None) == _lib.RA_ERR_INVALID
     assert lib.ra_merge_stats(4, 0, 1, 1, 1, 1, 1, 1, None) == _lib.RA_ERR_INVALID
@@ -275,9 +276,9 @@ def test_backward_entry_rejects_before_launch():
     assert _call_bwd(p, segs, 1, ch, 2, _grads(2, ptr=4104)) == _lib.RA_ERR_INVALID
     # the forward's descriptor checks apply
     assert _call_bwd(p, _segs([(200, [(200, 0, 1)])]), 1, ch, 2, _grads(2)) == _lib.RA_ERR_INVALID
-    many = [(1, [(1, i, 1)]) for i in range(33)]
-    assert _call_bwd(_problem(Sq=33), _segs([(33, [(33, 0, 1)])]), 1, _chunks(many), 33,
-                     _grads(33)) == _lib.RA_ERR_UNSUPPORTED
+    many = [(1, [(1, i, 1)]) for i in range(4097)]
+    assert _call_bwd(_problem(Sq=4097), _segs([(4097, [(4097, 0, 1)])]), 1, _chunks(many), 4097,
+                     _grads(4097)) == _lib.RA_ERR_UNSUPPORTED
 
 
 def test_lse_entries_reject_bad_arguments():

@@ -51,6 +51,7 @@ def _call(entry, q, kc, vc, causal):
 @pytest.mark.parametrize("seed,Hq,Hkv,S,causal,lens", [
     (31, 4, 4, 2304, False, [1024, 1280]),    # 36 units over 81 CTAs: every unit split
     (32, 8, 2, 3072, True, [1000, 1000, 1072]),
+    (34, 4, 2, 2560, True, [64] * 40),        # chunk tables in the fixed array too
 ])
 def test_noalloc_matches_allocating_entry_point_twice(seed, Hq, Hkv, S, causal, lens):
     q, k, v = _inputs(seed, Hq, Hkv, S)
