@@ -17,6 +17,7 @@ sample of the same workload, on this machine's host cores.
 from __future__ import annotations
 
 import argparse
+import ctypes
 import json
 import math
 import os
@@ -62,55 +63,119 @@ def _traffic(kernel_key):
         return None
 
 
+_REASON_BITS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+                0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+
+class _Nvml:
+    """The few NVML reads the clock record needs (read-only; nothing is set)."""
+
+    def __init__(self, cuda_index):
+        import torch
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit failed")
+        self.lib = lib
+        self.h = ctypes.c_void_p()
+        ok = False
+        uuid = getattr(torch.cuda.get_device_properties(cuda_index), "uuid", None)
+        if uuid is not None:
+            for name in (f"GPU-{uuid}", str(uuid)):
+                if lib.nvmlDeviceGetHandleByUUID(name.encode(), ctypes.byref(self.h)) == 0:
+                    ok = True
+                    break
+        if not ok and lib.nvmlDeviceGetHandleByIndex_v2(cuda_index, ctypes.byref(self.h)) != 0:
+            raise RuntimeError("no NVML handle for the device")
+        self.reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(lib, "nvmlDeviceGetCurrentClocksThrottleReasons")
+        mx = ctypes.c_uint()
+        lib.nvmlDeviceGetMaxClockInfo(self.h, 1, ctypes.byref(mx))
+        self.max_mhz = float(mx.value)
+
+    def sample(self):
+        mhz, rs = ctypes.c_uint(), ctypes.c_ulonglong()
+        if self.lib.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(mhz)) != 0:
+            return None
+        if self.reasons_fn(self.h, ctypes.byref(rs)) != 0:
+            rs.value = 0
+        return float(mhz.value), int(rs.value)
+
+
 class ClockSampler:
-    """nvidia-smi clock / throttle samples while the timed region runs."""
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    """SM clock and clock-event reasons sampled while a timed region runs:
+    NVML read every millisecond from a helper thread (so that a region of a few
+    milliseconds still gets samples), else nvidia-smi every 10 ms."""
 
     def __init__(self, index):
         self.index = index
-        self.proc = None
+        self.samples = []
+        self.source = None
 
     def __enter__(self):
+        import threading
+        self.samples = []
+        self._stop = threading.Event()
+        self.proc = None
         try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
-                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.nv = _Nvml(self.index)
+            self.source = "nvml, 1 ms"
+
+            def loop():
+                while not self._stop.is_set():
+                    s = self.nv.sample()
+                    if s is not None:
+                        self.samples.append(s)
+                    time.sleep(0.001)
+
+            self.thread = threading.Thread(target=loop, daemon=True)
+            self.thread.start()
         except Exception:
-            self.proc = None
+            self.nv = None
+            self.source = "nvidia-smi, 10 ms"
+            try:
+                self.proc = subprocess.Popen(
+                    ["nvidia-smi", f"--id={self.index}",
+                     "--query-gpu=clocks.sm,clocks.max.sm,clocks_event_reasons.active",
+                     "--format=csv,noheader,nounits", "-lms", "10"],
+                    stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            except Exception:
+                self.proc = None
         return self
 
     def __exit__(self, *exc):
-        self.out = ""
+        if self.nv is not None:
+            self._stop.set()
+            self.thread.join(timeout=2)
+            self.max_mhz = self.nv.max_mhz
+            return
+        self.max_mhz = None
         if self.proc is not None:
             self.proc.terminate()
             try:
-                self.out, _ = self.proc.communicate(timeout=5)
+                out, _ = self.proc.communicate(timeout=5)
             except Exception:
                 self.proc.kill()
-                self.out = ""
+                out = ""
+            for line in (out or "").splitlines():
+                f = [x.strip() for x in line.split(",")]
+                try:
+                    self.samples.append((float(f[0]), int(f[2], 16)))
+                    self.max_mhz = float(f[1])
+                except (ValueError, IndexError):
+                    continue
 
     def summary(self):
-        sms, mx, reasons = [], None, set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in (self.out or "").splitlines():
-            f = [x.strip() for x in line.split(",")]
-            if len(f) < 9:
-                continue
-            try:
-                sms.append(float(f[1]))
-                mx = float(f[2])
-            except ValueError:
-                continue
-            for n, val in zip(names, f[5:9]):
-                if val.lower().startswith("active"):
-                    reasons.add(n)
-        if not sms:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        return {"sm_mhz": statistics.median(sms), "sm_max_mhz": mx,
-                "reasons": sorted(reasons), "samples": len(sms)}
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "source": self.source}
+        reasons = set()
+        for _, bits in self.samples:
+            for b, name in _REASON_BITS.items():
+                if bits & b:
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(m for m, _ in self.samples),
+                "sm_max_mhz": self.max_mhz, "reasons": sorted(reasons),
+                "samples": len(self.samples), "source": self.source}
 
 
 def _dist():
@@ -302,7 +367,166 @@ def run_gpu(args):
     }
     if not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds, docs)
+    if not args.no_secondary and world == 1 and args.workload == "bf16_8k" and not docs:
+        del qs, kc, vc, out, m, l
+        torch.cuda.empty_cache()
+        line["secondary"] = secondary_records(dev, flush)
     return line
+
+
+def _timed(step, steps, warmup, flush, stream, index):
+    """Runs ``warmup`` untimed steps, then ``steps`` steps each preceded by an
+    L2 flush; returns the CUDA-event time of every step (ms, on ``stream``) and
+    the clock record of the timed region."""
+    import torch
+    for _ in range(warmup):
+        flush.fill_(1.0)
+        step()
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    with ClockSampler(index) as clk:
+        for i in range(steps):
+            flush.fill_(float(i & 7))
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in zip(starts, ends)], clk.summary()
+
+
+def _imbalance(w, rs, segs):
+    """Per virtual rank (query segment): visible (query, key) pairs and the
+    128x128 tile products the kernel schedules; max/mean of each (1.0 is a
+    perfect balance)."""
+    from blockwise_attention_online_gb300 import segment_work
+    lens = [w.S // w.n_chunks] * w.n_chunks
+    pairs, tiles = segment_work(w.B, w.Hq, w.Hkv, w.D, segs, lens, rs, w.causal)
+    mp, mt = sum(pairs) / len(pairs), sum(tiles) / len(tiles)
+    return {"pairs_max_over_mean": round(max(pairs) / mp, 4),
+            "tiles_max_over_mean": round(max(tiles) / mt, 4),
+            "pairs_per_rank": pairs, "tiles_per_rank": tiles}
+
+
+def secondary_records(dev, flush, steps_small=5):
+    """Further workloads, timed the same way as the headline (L2 flushed per
+    step, CUDA events on the launching stream, clocks sampled): the other
+    configurations of the forward (with the per-virtual-rank work imbalance of
+    each layout), the backward, and the HBM-bound merge kernels."""
+    import torch
+    from blockwise_attention_online_gb300 import (device_status, merge_lse, merge_stats,
+                                                  ring_attention, ring_attention_bwd,
+                                                  stats_to_lse)
+    peak_b, _, hbm, _ = _peaks()
+    stream = torch.cuda.current_stream()
+    out = {"forward": [], "backward": [], "hbm_kernels": []}
+    cases = [("bf16_32k_causal", None, steps_small), ("bf16_128k_gqa_causal", "zigzag", steps_small),
+             ("bf16_128k_gqa_causal", "contiguous", steps_small),
+             ("bf16_128k_gqa_causal", "striped", steps_small), ("bf16_1m_causal", None, 2)]
+    for name, layout, n in cases:
+        w, qs, kc, vc, rs, segs = build_workload(name, layout, dev)
+        o = torch.empty_like(qs)
+        m = torch.empty(qs.shape[:3], device=dev, dtype=torch.float32)
+        l = torch.empty_like(m)
+
+        def step():
+            ring_attention(qs, kc, vc, chunk_spans=rs, q_segments=segs, causal=w.causal,
+                           out=o, m=m, l=l)
+
+        times, clk = _timed(step, n, 3, flush, stream, dev.index)
+        device_status()
+        ms = sum(times) / len(times)
+        tf = w.flops() / (ms * 1e-3) / 1e12
+        out["forward"].append({"workload": w.name, "layout": w.layout, "S": w.S, "Hq": w.Hq,
+                               "Hkv": w.Hkv, "causal": w.causal, "chunks": w.n_chunks,
+                               "steps": n, "warmup": 3, "ms_per_step": round(ms, 4),
+                               "tflops": round(tf, 2), "frac_of_peak": round(tf / peak_b, 4),
+                               "imbalance": _imbalance(w, rs, segs), "clocks": clk})
+        del qs, kc, vc, o, m, l
+        torch.cuda.empty_cache()
+    # backward of the headline workload
+    w, qs, kc, vc, rs, segs = build_workload("bf16_8k", None, dev)
+    O, m, l = ring_attention(qs, kc, vc, chunk_spans=rs, q_segments=segs, causal=w.causal)
+    g = torch.Generator(device=dev).manual_seed(99)
+    dout = torch.randn(qs.shape, device=dev, generator=g).to(torch.bfloat16)
+    dq = torch.empty(qs.shape, device=dev, dtype=torch.float32)
+    dk = [torch.empty(k.shape, device=dev, dtype=torch.float32) for k in kc]
+    dv = [torch.empty(v.shape, device=dev, dtype=torch.float32) for v in vc]
+
+    def bstep():
+        ring_attention_bwd(qs, kc, vc, O, dout, m, l, chunk_spans=rs, q_segments=segs,
+                           causal=w.causal, dq=dq, dk=dk, dv=dv)
+
+    times, clk = _timed(bstep, 20, 3, flush, stream, dev.index)
+    device_status()
+    ms = sum(times) / len(times)
+    tf = 2.5 * w.flops() / (ms * 1e-3) / 1e12
+    out["backward"].append({"workload": w.name, "layout": w.layout, "steps": 20, "warmup": 3,
+                            "flops_per_step": 2.5 * w.flops(), "ms_per_step": round(ms, 4),
+                            "tflops": round(tf, 2), "frac_of_peak": round(tf / peak_b, 4),
+                            "clocks": clk})
+    del qs, kc, vc, O, m, l, dout, dq, dk, dv
+    torch.cuda.empty_cache()
+    out["hbm_kernels"] = hbm_kernel_records(dev, flush, 32 * 32768, 20)
+    return out
+
+
+def hbm_kernel_records(dev, flush, rows, steps, D=128):
+    """The HBM-bound kernels, each timed over ``steps`` launches between L2
+    flushes: the statistics merge (ra_merge_stats), its log-sum-exp form
+    (ra_merge_lse) and ra_stats_to_lse, on ``rows`` rows of head_dim ``D``
+    (default: the rows of the 32K causal workload, 32 heads x 32768).
+    Algorithmic bytes per row: the merge reads both sides' u, l, m and writes
+    the accumulator's, 3 (4D + 8); the lse merge 3 (4D + 4); stats_to_lse
+    reads m, l and writes lse, 12."""
+    import torch
+    from blockwise_attention_online_gb300 import device_status, merge_lse, merge_stats, stats_to_lse
+    _, _, hbm, _ = _peaks()
+    stream = torch.cuda.current_stream()
+    g = torch.Generator(device=dev).manual_seed(7)
+    u_a = torch.randn(rows, D, device=dev, generator=g)
+    u_b = torch.randn(rows, D, device=dev, generator=g)
+    l_a = torch.rand(rows, device=dev, generator=g) + 1
+    l_b = torch.rand(rows, device=dev, generator=g) + 1
+    m_a = torch.randn(rows, device=dev, generator=g)
+    m_b = torch.randn(rows, device=dev, generator=g)
+    kern = [("ra_merge_stats", "merge_vec4_kernel",
+             lambda: merge_stats(u_a, l_a, m_a, u_b, l_b, m_b), 3 * (4 * D + 8)),
+            ("ra_merge_lse", "merge_lse_kernel",
+             lambda: merge_lse(u_a, m_a, u_b, m_b), 3 * (4 * D + 4)),
+            ("ra_stats_to_lse", "stats_to_lse_kernel",
+             lambda: stats_to_lse(m_a, l_a, l_b), 12)]
+    recs = []
+    for call, kname, fn, bpr in kern:
+        times, clk = _timed(fn, steps, 3, flush, stream, dev.index)
+        device_status()
+        ms = sum(times) / len(times)
+        gbs = rows * bpr / (ms * 1e-3) / 1e9
+        recs.append({"call": call, "kernel": kname, "rows": rows, "D": D,
+                     "bytes_per_row": bpr, "bytes_per_launch": rows * bpr,
+                     "ms_per_launch": round(ms, 5), "gbs": round(gbs, 1),
+                     "peak_gbs": hbm, "frac_of_peak": round(gbs / hbm, 4),
+                     "steps": steps, "warmup": 3, "clocks": clk})
+    return recs
+
+
+def run_gpu_merge(args):
+    """--pass merge: only the HBM-bound kernels (one JSON line)."""
+    import torch
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, device=dev, dtype=torch.float32)
+    recs = hbm_kernel_records(dev, flush, args.rows, args.steps)
+    head = recs[0]
+    return {"metric": "ra_merge_stats achieved HBM GB/s", "value": head["gbs"], "unit": "GB/s",
+            "n_gpus": 1, "steps": args.steps, "warmup": 3,
+            "ms_per_step": head["ms_per_launch"], "higher_is_better": True, "dtype": "f32",
+            "data": "synthetic: seeded fp32 statistics", "config": {"workload": "merge",
+                                                                    "rows": args.rows, "D": 128},
+            "roofline": {"bound": "hbm", "achieved": head["gbs"], "peak": head["peak_gbs"],
+                         "unit": "GB/s", "frac": head["frac_of_peak"], "traffic": None,
+                         "kernel": head["kernel"]},
+            "kernels": recs, "gpu_launches": 3 * args.steps}
 
 
 def run_gpu_bwd(args):
@@ -510,12 +734,16 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-secondary", action="store_true",
+                    help="skip the further records (other workloads, backward, merge kernels)")
+    ap.add_argument("--rows", type=int, default=32 * 32768,
+                    help="--pass merge: rows of the statistics (head_dim 128)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--docs", type=int, default=0,
                     help="pack the sequence into seeded documents of this mean length "
                          "(forward only; 0 = one document)")
-    ap.add_argument("--pass", dest="which", default="fwd", choices=["fwd", "bwd"],
-                    help="time the forward (default) or the backward pass")
+    ap.add_argument("--pass", dest="which", default="fwd", choices=["fwd", "bwd", "merge"],
+                    help="time the forward (default), the backward pass or the HBM-bound merge kernels")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -523,6 +751,8 @@ def main():
         line = run_reference(args)
     elif args.which == "bwd":
         line = run_gpu_bwd(args)
+    elif args.which == "merge":
+        line = run_gpu_merge(args)
     else:
         line = run_gpu(args)
     if line is not None:
