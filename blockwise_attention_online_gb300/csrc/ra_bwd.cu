@@ -16,6 +16,7 @@
 // Three launches on the caller's stream:
 //   bwd_prep_kernel    lse2 and delta per query row
 //   bwd_qtile_kernel   bounds of the key windows of each 128-row query tile
+//   bwd_colaux_kernel  per query tile, the column data of the dK/dV CTAs
 //   bwd_kernel<D>      two kinds of CTA in one grid:
 //     bwd_dkv_tile     one per (batch, key/value head, 128-row key tile):
 //                      walks every live query tile of the heads that read it
@@ -51,26 +52,34 @@ enum : int {
   kSiteBwdAcc = 36
 };
 
-// kDocs: the dK/dV CTAs of a launch with packed documents stage a (lo, hi)
-// key window per query column instead of its position (one more array).
+// kDocs: the dK/dV CTAs of a launch with packed documents walk only the
+// query tiles whose rows' key windows meet their key tile.
 template <int D, bool kDocs = true>
 struct BwdCfg {
   static constexpr int kBoxBytes = 128 * 128;     // 128 rows x 64 bf16 (one swizzle atom wide)
   static constexpr int kBoxes = (D + 63) / 64;    // D = 96: the second box is half zero fill
   static constexpr int kTileBytes = kBoxes * kBoxBytes;  // one 128-row bf16 tile
-  // shared memory: two resident tiles, two stages of two tiles, per-stage
-  // column data (-lse2, -delta, then the (lo, hi) key windows or, without
-  // documents, the positions), barriers
+  // shared memory of a dK/dV CTA: K and V resident; two stages, each of a Q
+  // and a dO tile and the query tile's column data (kColAuxBytes: the two
+  // column-bias tiles, then the key windows); the constant tile of ones the
+  // biases are multiplied with; barriers
   static constexpr int kRes0 = 0, kRes1 = kTileBytes;
   static constexpr int kStage0 = 2 * kTileBytes;
   static constexpr int kStageBytes = 2 * kTileBytes;
+  // A bias tile is a K = 16 operand of 128 rows (4 KB, no swizzle): row n
+  // holds a value of query column n as the sum of three bf16 numbers in K
+  // slots 0-2, the other slots zero. Stage s: [-lse2 / c, -delta, windows].
+  static constexpr int kBiasBytes = 128 * 16 * 2;
   static constexpr int kAux0 = kStage0 + 2 * kStageBytes;
-  static constexpr int kAuxBytes = (kDocs ? 4 : 3) * 128 * 4;
-  static constexpr int kBar = kAux0 + 2 * kAuxBytes;
+  static constexpr int kAuxBytes = kColAuxBytes;
+  static constexpr int kOnes = kAux0 + 2 * kAuxBytes;     // rows (1, 1, 1, 0, ...)
+  static constexpr int kBar = kOnes + kBiasBytes;
   static constexpr int kBarBytes = 256;
   static constexpr int kSmemBytes = kBar + kBarBytes + 1024;  // + alignment slack
   static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+  static_assert(kAux0 % 1024 == 0 && kAuxBytes % 1024 == 0, "bias tiles stay aligned");
 };
+
 
 // Chunk tables: the plan's own arrays, or their device-resident copies.
 __device__ __forceinline__ const KvSeg& bspan(const BwdPlan& p, int k) {
@@ -92,6 +101,21 @@ __device__ __forceinline__ void bwd_fence_maps(const BwdPlan& p, int c) {
     fence_tmap_acquire(p.ext_kmap + c);
     fence_tmap_acquire(p.ext_vmap + c);
   }
+}
+
+// Byte offset of row n's K slots 0-7 in a no-swizzle K = 16 operand tile
+// (8-row groups of two 128-byte core matrices; slots 8-15 at +128 stay zero).
+__device__ __forceinline__ uint32_t bias_row_offset(int n) { return (n >> 3) * 256 + (n & 7) * 16; }
+
+// x as hi + mid + lo, three bf16 numbers (error below 2^-26 |x|), in K slots
+// 0-2 of a row; the products with a row of ones add them up in fp32.
+__device__ __forceinline__ uint4 bias_split3(float x) {
+  const uint32_t h = pack_bf16x2(x, 0.f) & 0xffffu;
+  const float r1 = x - __uint_as_float(h << 16);
+  const uint32_t m = pack_bf16x2(r1, 0.f) & 0xffffu;
+  const float r2 = r1 - __uint_as_float(m << 16);
+  const uint32_t l = pack_bf16x2(r2, 0.f) & 0xffffu;
+  return make_uint4(h | (m << 16), l, 0u, 0u);
 }
 
 __device__ __forceinline__ int bwd_row_position(const BwdPlan& p, int row) {
@@ -167,6 +191,34 @@ __global__ void bwd_prep_kernel(const void* o, int o_fp32, int64_t o_sb, int64_t
   }
 }
 
+// Column data of the dK/dV CTAs for every 128-row query tile, laid out as it
+// will lie in shared memory (kColAuxBytes per tile; one thread per query row,
+// the rows past Sq of the last tile included): the bias rows -lse2 / c and
+// -delta, each as three bf16 parts (a row that sees no key, or lies past Sq,
+// gets -1e30, so that its probabilities are 0), and the row's key window.
+// The producer then fetches a query tile's column data with one bulk copy.
+__global__ void bwd_colaux_kernel(const __grid_constant__ BwdPlan p, uint8_t* colaux) {
+  const int64_t t = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t per_bh = int64_t(p.n_qtiles) * 128;
+  if (t >= int64_t(p.B) * p.Hq * per_bh) return;
+  const int64_t bh = t / per_bh;
+  const int row = int(t - bh * per_bh);
+  const bool valid = row < p.Sq;
+  const float l2 = valid ? p.lse2[bh * p.Sq + row] : kInf;
+  const float xl = l2 < kInf ? -l2 / p.scale_log2 : -1e30f;
+  const float xd = valid ? -p.delta[bh * p.Sq + row] : 0.f;
+  int lo = 0x7fffffff, hi = int(0x80000000);  // an empty window
+  if (valid) key_window(p, bwd_row_position(p, row), lo, hi);
+  uint8_t* tile = colaux + (bh * p.n_qtiles + row / 128) * int64_t(kColAuxBytes);
+  const int n = row & 127;
+  const uint32_t off = bias_row_offset(n);
+  *reinterpret_cast<uint4*>(tile + off) = bias_split3(xl);
+  *reinterpret_cast<uint4*>(tile + off + 128) = make_uint4(0u, 0u, 0u, 0u);
+  *reinterpret_cast<uint4*>(tile + 4096 + off) = bias_split3(xd);
+  *reinterpret_cast<uint4*>(tile + 4096 + off + 128) = make_uint4(0u, 0u, 0u, 0u);
+  reinterpret_cast<int2*>(tile + 8192)[n] = make_int2(lo, hi);
+}
+
 // One warp per 128-row query tile: bounds of its rows' key windows
 // (x: lowest lo, y: highest hi, z: highest lo, w: lowest hi). A key tile
 // inside [z, w] is visible to every row; one outside [x, y] to none.
@@ -193,18 +245,27 @@ __global__ void bwd_qtile_kernel(const __grid_constant__ BwdPlan p, int4* out) {
 
 // ------------------------------------------------------------ shared pieces
 struct BwdBars {
-  uint32_t res_full, st_full0, st_empty0, sdp_full, ew_done, acc_full, done;  // stage s: + 8 s
+  uint32_t res_full, st_full0, st_empty0, sdp_full, ew_done, acc_full, done, s_free;  // stage s: + 8 s
   uint32_t* tmem_slot;
   volatile int* abort_flag;
 };
 
-template <int D, bool kDocs = true>
+template <int D, bool kDocs = true, bool kBias = false>
 __device__ __forceinline__ void bwd_setup(uint8_t* smem_raw, uint32_t& base, uint8_t*& gbase,
                                           BwdBars& bb) {
   using C = BwdCfg<D, kDocs>;
   const uint32_t raw = smem_addr(smem_raw);
   base = (raw + 1023u) & ~1023u;
   gbase = smem_raw + (base - raw);
+  if constexpr (kBias) {
+    // the ones tile: 1.0 in K slots 0-2 of every row, the other slots zero
+    for (int n = threadIdx.x; n < 128; n += blockDim.x) {
+      *reinterpret_cast<uint4*>(gbase + C::kOnes + bias_row_offset(n)) =
+          make_uint4(0x3f803f80u, 0x00003f80u, 0u, 0u);
+      *reinterpret_cast<uint4*>(gbase + C::kOnes + bias_row_offset(n) + 128) = make_uint4(0, 0, 0, 0);
+    }
+    fence_proxy_async_smem();
+  }
   const uint32_t bars = base + C::kBar;
   bb.res_full = bars;
   bb.st_full0 = bars + 8;
@@ -213,18 +274,20 @@ __device__ __forceinline__ void bwd_setup(uint8_t* smem_raw, uint32_t& base, uin
   bb.ew_done = bars + 48;
   bb.acc_full = bars + 56;
   bb.done = bars + 64;
-  bb.tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::kBar + 72);
-  bb.abort_flag = reinterpret_cast<volatile int*>(gbase + C::kBar + 76);
+  bb.s_free = bars + 72;
+  bb.tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::kBar + 80);
+  bb.abort_flag = reinterpret_cast<volatile int*>(gbase + C::kBar + 84);
   if (threadIdx.x == 0) {
     mbar_init(bb.res_full, 1);
     for (int s = 0; s < 2; ++s) {
-      mbar_init(bb.st_full0 + 8 * s, 1 + 32);  // the copies' transaction count + 32 producer lanes
+      mbar_init(bb.st_full0 + 8 * s, 1);  // the copies' transaction count
       mbar_init(bb.st_empty0 + 8 * s, 1);
     }
     mbar_init(bb.sdp_full, 1);
     mbar_init(bb.ew_done, 256);
     mbar_init(bb.acc_full, 1);
     mbar_init(bb.done, 1);
+    mbar_init(bb.s_free, 256);
     *bb.abort_flag = 0;
     fence_mbar_init();
   }
@@ -246,16 +309,25 @@ __device__ __forceinline__ void bwd_teardown(uint32_t tmem) {
 
 // Issue one 128 x 128 x D product D[tmem] = A B^T, both operands K-major in
 // shared memory (the layout TMA writes for a [rows, D] tile).
+// acc: add to what the accumulator holds (a bias) instead of overwriting it.
 template <int D>
-__device__ __forceinline__ void issue_abt(uint32_t d_tmem, uint32_t sa, uint32_t sb) {
+__device__ __forceinline__ void issue_abt(uint32_t d_tmem, uint32_t sa, uint32_t sb,
+                                          bool acc = false) {
   using C = BwdCfg<D>;
   constexpr uint32_t kId = idesc_bf16_f32(128, 128, 0, 0);
   const uint64_t ad = sdesc_sw128(sa, 16, 1024), bd = sdesc_sw128(sb, 16, 1024);
 #pragma unroll
   for (int kk = 0; kk < D / 16; ++kk) {
     const uint64_t off = uint64_t(((kk >> 2) * C::kBoxBytes + (kk & 3) * 32) >> 4);
-    mma_ss(d_tmem, ad + off, bd + off, kId, kk > 0 ? 1u : 0u);
+    mma_ss(d_tmem, ad + off, bd + off, kId, (acc || kk > 0) ? 1u : 0u);
   }
+}
+
+// D[tmem] = ones . bias^T: every row of the 128 x 128 accumulator receives the
+// per-column bias (K = 16, both operands without swizzle).
+__device__ __forceinline__ void issue_bias(uint32_t d_tmem, uint32_t s_ones, uint32_t s_bias) {
+  constexpr uint32_t kId = idesc_bf16_f32(128, 128, 0, 0);
+  mma_ss(d_tmem, sdesc_noswizzle(s_ones, 128, 256), sdesc_noswizzle(s_bias, 128, 256), kId, 0u);
 }
 
 // D[tmem] (+)= A[tmem] B with A 128 x 128 bf16 in TMEM and B a [128 rows (the
@@ -304,7 +376,7 @@ __device__ __forceinline__ void bwd_dkv_tile(const BwdPlan& p, int cta) {
   uint32_t base;
   uint8_t* gbase;
   BwdBars bb;
-  bwd_setup<D, kDocs>(smem_raw, base, gbase, bb);
+  bwd_setup<D, kDocs, true>(smem_raw, base, gbase, bb);
   const uint32_t tmem = *bb.tmem_slot;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const unsigned long long budget = p.timeout_ns;
@@ -352,31 +424,18 @@ __device__ __forceinline__ void bwd_dkv_tile(const BwdPlan& p, int cta) {
       if (!ok) break;
       const uint32_t sQ = base + C::kStage0 + st * C::kStageBytes, sDO = sQ + C::kTileBytes;
       if (leader) {
-        mbar_arrive_expect_tx(bb.st_full0 + 8 * st, 2 * C::kTileBytes);
+        // Q, dO and the query tile's column data (bias tiles, key windows)
+        mbar_arrive_expect_tx(bb.st_full0 + 8 * st, 2 * C::kTileBytes + C::kAuxBytes);
 #pragma unroll
         for (int bx = 0; bx < C::kBoxes; ++bx) {
           tma_load_4d(sQ + bx * C::kBoxBytes, &p.qmap, bb.st_full0 + 8 * st, bx * 64, 128 * qt, h, b);
           tma_load_4d(sDO + bx * C::kBoxBytes, &p.domap, bb.st_full0 + 8 * st, bx * 64, 128 * qt, h, b);
         }
+        bulk_load(base + C::kAux0 + st * C::kAuxBytes,
+                  p.colaux + ((int64_t(b) * p.Hq + h) * p.n_qtiles + qt) * int64_t(kColAuxBytes),
+                  C::kAuxBytes, bb.st_full0 + 8 * st);
       }
-      // per-column data of this query tile: -lse2, -delta, then its key
-      // window (lo, hi) with documents, else its position
-      float* aux = reinterpret_cast<float*>(gbase + C::kAux0 + st * C::kAuxBytes);
-      const int64_t rowbase = (int64_t(b) * p.Hq + h) * p.Sq;
-      for (int i = lane; i < 128; i += 32) {
-        const int row = 128 * qt + i;
-        const bool valid = row < p.Sq;
-        aux[i] = valid ? -p.lse2[rowbase + row] : -kInf;
-        aux[128 + i] = valid ? -p.delta[rowbase + row] : 0.f;
-        if constexpr (kDocs) {
-          int lo = 0x7fffffff, hi = int(0x80000000);  // an empty window
-          if (valid) key_window(p, bwd_row_position(p, row), lo, hi);
-          reinterpret_cast<int2*>(aux + 256)[i] = make_int2(lo, hi);
-        } else {
-          reinterpret_cast<int*>(aux)[256 + i] = valid ? bwd_row_position(p, row) : int(0x80000000);
-        }
-      }
-      mbar_arrive(bb.st_full0 + 8 * st);
+      __syncwarp();
       ++j;
     }
     if (!ok) {
@@ -389,36 +448,70 @@ __device__ __forceinline__ void bwd_dkv_tile(const BwdPlan& p, int cta) {
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA warp
+    // Per pair j: S^T_j (into the S^T columns) as soon as the elementwise
+    // warps have read S^T_{j-1}; then, once they have written P^T_{j-1} and
+    // dS^T_{j-1} over dP^T_{j-1}, dV and dK of pair j - 1 and dP^T_j.
     const bool leader = elect_one();
     const uint32_t tS = tmem, tP = tmem + 128, tdV = tmem + 256, tdK = tmem + 384;
     bool ok = warp_wait(bb.res_full, 0, bb.abort_flag, budget, kSiteBwdKv);
+    // the query tiles of this key tile, in walk order (the walk is cheap to redo)
     QWalk<kDocs> w{0, g * p.n_qtiles, p.n_qtiles, hkv * g};
-    int h, qt, j = 0;
-    while (ok && w.next(p, kmin, kmax, h, qt)) {
-      const int st = j & 1;
-      const uint32_t sQ = base + C::kStage0 + st * C::kStageBytes, sDO = sQ + C::kTileBytes;
-      ok = warp_wait(bb.st_full0 + 8 * st, (j >> 1) & 1, bb.abort_flag, budget, kSiteBwdStage);
-      if (!ok) break;
-      tc_fence_after();
-      if (leader) {
-        issue_abt<D>(tS, sK, sQ);   // S^T  = K Q^T
-        issue_abt<D>(tP, sV, sDO);  // dP^T = V dO^T
-        mma_commit(bb.sdp_full);
+    int n = 0;
+    {
+      QWalk<kDocs> wc{0, g * p.n_qtiles, p.n_qtiles, hkv * g};
+      int hh, qq;
+      while (wc.next(p, kmin, kmax, hh, qq)) ++n;
+    }
+    auto stage_q = [&](int jj) { return base + C::kStage0 + (jj & 1) * C::kStageBytes; };
+    auto stage_b = [&](int jj) { return base + C::kAux0 + (jj & 1) * C::kAuxBytes; };
+    int h, qt;
+    if (ok && n > 0) {
+      w.next(p, kmin, kmax, h, qt);
+      ok = warp_wait(bb.st_full0, 0, bb.abort_flag, budget, kSiteBwdStage);
+      if (ok) {
+        tc_fence_after();
+        if (leader) {
+          issue_bias(tS, base + C::kOnes, stage_b(0));                      // -lse2 / c per column
+          issue_abt<D>(tS, sK, stage_q(0), true);                           // S^T += K Q^T
+          issue_bias(tP, base + C::kOnes, stage_b(0) + C::kBiasBytes);      // -delta per column
+          issue_abt<D>(tP, sV, stage_q(0) + C::kTileBytes, true);           // dP^T += V dO^T
+          mma_commit(bb.sdp_full);
+        }
+        __syncwarp();
       }
-      __syncwarp();
+    }
+    for (int j = 0; ok && j < n; ++j) {
+      const bool more = j + 1 < n;
+      if (more) {
+        w.next(p, kmin, kmax, h, qt);
+        ok = warp_wait(bb.s_free, j & 1, bb.abort_flag, budget, kSiteBwdSdp) &&
+             warp_wait(bb.st_full0 + 8 * ((j + 1) & 1), ((j + 1) >> 1) & 1, bb.abort_flag, budget,
+                       kSiteBwdStage);
+        if (!ok) break;
+        tc_fence_after();
+        if (leader) {
+          issue_bias(tS, base + C::kOnes, stage_b(j + 1));
+          issue_abt<D>(tS, sK, stage_q(j + 1), true);
+        }
+        __syncwarp();
+      }
       ok = warp_wait(bb.ew_done, j & 1, bb.abort_flag, budget, kSiteBwdDs);
       if (!ok) break;
       tc_fence_after();
       if (leader) {
-        issue_tmem_a<D>(tdV, tS, sDO, j > 0);  // dV += P^T dO
-        issue_tmem_a<D>(tdK, tP, sQ, j > 0);   // dK += dS^T Q
-        mma_commit(bb.st_empty0 + 8 * st);
+        issue_tmem_a<D>(tdV, tP, stage_q(j) + C::kTileBytes, j > 0);   // dV += P^T dO
+        issue_tmem_a<D>(tdK, tP + 32, stage_q(j), j > 0);             // dK += dS^T Q
+        mma_commit(bb.st_empty0 + 8 * (j & 1));
+        if (more) {
+          issue_bias(tP, base + C::kOnes, stage_b(j + 1) + C::kBiasBytes);
+          issue_abt<D>(tP, sV, stage_q(j + 1) + C::kTileBytes, true);
+          mma_commit(bb.sdp_full);
+        }
       }
       __syncwarp();
-      ++j;
     }
     if (leader) {
-      if (ok && j > 0) mma_commit(bb.acc_full);
+      if (ok && n > 0) mma_commit(bb.acc_full);
       mma_commit(bb.done);
     }
     __syncwarp();
@@ -444,9 +537,8 @@ __device__ __forceinline__ void bwd_dkv_tile(const BwdPlan& p, int cta) {
            warp_wait(bb.sdp_full, j & 1, bb.abort_flag, budget, kSiteBwdSdp);
       if (!ok) break;
       tc_fence_after();
-      const float* aux = reinterpret_cast<const float*>(gbase + C::kAux0 + st * C::kAuxBytes);
-      const int4* awin = reinterpret_cast<const int4*>(aux + 256);  // two columns' windows
-      const int* apos = reinterpret_cast<const int*>(aux) + 256;     // positions
+      // the key windows of the query tile's rows (lo, hi), after the bias tiles
+      const int4* awin = reinterpret_cast<const int4*>(gbase + C::kAux0 + st * C::kAuxBytes + 2 * C::kBiasBytes);
       // a mask is needed only where some key of the tile lies outside some
       // row's window (after some row's position, without documents), or
       // where the key tile is ragged
@@ -457,64 +549,51 @@ __device__ __forceinline__ void bwd_dkv_tile(const BwdPlan& p, int cta) {
       } else {
         masked = masked || (p.causal && kmax > p.qtile_pos[qt].w);
       }
-#pragma unroll 1
-      for (int i = 2 * hw; i < 2 * hw + 2; ++i) {
-        // the chunk's column data first (shared-memory broadcasts), so that
-        // their latency overlaps the TMEM loads' wait
-        float4 nl[8], nd[8];
+      // S^T and dP^T arrive with their column biases already added:
+      // P^T = 2^(c S^T), dS^T = P^T dP^T. Both halves of this warpgroup's 64
+      // columns are read first, so that S^T's columns are free for the next
+      // pair's product at once; P^T and dS^T then go over dP^T's columns
+      // (those this warpgroup read): P^T at [64 hw, 64 hw + 32), dS^T at
+      // [64 hw + 32, 64 hw + 64), the TMEM A operands of dV and dK.
+      uint32_t sv[2][32], dp[2][32];
+      tmem_ld32(tS + 64 * hw, sv[0]);
+      tmem_ld32(tS + 64 * hw + 32, sv[1]);
+      tmem_ld32(tP + 64 * hw, dp[0]);
+      tmem_ld32(tP + 64 * hw + 32, dp[1]);
+      tmem_ld_wait();
+      reg_fence(sv[0]);
+      reg_fence(sv[1]);
+      reg_fence(dp[0]);
+      reg_fence(dp[1]);
+      tc_fence_before();
+      mbar_arrive(bb.s_free);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          nl[k] = *reinterpret_cast<const float4*>(aux + 32 * i + 4 * k);
-          nd[k] = *reinterpret_cast<const float4*>(aux + 128 + 32 * i + 4 * k);
-        }
-        uint32_t s[32], dp[32];
-        tmem_ld32(tS + 32 * i, s);
-        tmem_ld32(tP + 32 * i, dp);
-        tmem_ld_wait();
-        reg_fence(s);
-        reg_fence(dp);
-        if (kDocs && masked) {
+      for (int q = 0; q < 2; ++q) {
+        const int i = 2 * hw + q;  // 32-column chunk of the tile
+        if (masked) {
           // a score outside its column's window (or of a missing key row)
           // becomes -inf: p = 0 and dS = 0
 #pragma unroll
           for (int c = 0; c < 32; c += 2) {
-            const int4 w = awin[(32 * i + c) / 2];
-            if (!krow_ok || kpos < w.x || kpos > w.y) s[c] = 0xff800000u;
-            if (!krow_ok || kpos < w.z || kpos > w.w) s[c + 1] = 0xff800000u;
+            const int4 w = awin[(32 * i + c) / 2];  // two columns' windows
+            if (!krow_ok || kpos < w.x || kpos > w.y) sv[q][c] = 0xff800000u;
+            if (!krow_ok || kpos < w.z || kpos > w.w) sv[q][c + 1] = 0xff800000u;
           }
         }
         uint32_t pp[16], pd[16];
 #pragma unroll
-        for (int c = 0; c < 32; c += 4) {
-          const float4 lse = nl[c / 4], del = nd[c / 4];   // negated
-          const uint64_t x01 = fma2(f2(__uint_as_float(s[c]), __uint_as_float(s[c + 1])), c2x2,
-                                    f2(lse.x, lse.y));
-          const uint64_t x23 = fma2(f2(__uint_as_float(s[c + 2]), __uint_as_float(s[c + 3])), c2x2,
-                                    f2(lse.z, lse.w));
-          float x0, x1, x2, x3;
-          f2_split(x01, x0, x1);
-          f2_split(x23, x2, x3);
-          float p0 = ex2(x0), p1 = ex2(x1), p2 = ex2(x2), p3 = ex2(x3);
-          if (!kDocs && masked) {
-            const int4 qp4 = *reinterpret_cast<const int4*>(apos + 32 * i + c);
-            if (!krow_ok || (p.causal && kpos > qp4.x)) p0 = 0.f;
-            if (!krow_ok || (p.causal && kpos > qp4.y)) p1 = 0.f;
-            if (!krow_ok || (p.causal && kpos > qp4.z)) p2 = 0.f;
-            if (!krow_ok || (p.causal && kpos > qp4.w)) p3 = 0.f;
-          }
-          const uint64_t t01 = add2(f2(__uint_as_float(dp[c]), __uint_as_float(dp[c + 1])), f2(del.x, del.y));
-          const uint64_t t23 = add2(f2(__uint_as_float(dp[c + 2]), __uint_as_float(dp[c + 3])), f2(del.z, del.w));
-          float d0, d1, d2, d3;
-          f2_split(mul2(f2(p0, p1), t01), d0, d1);
-          f2_split(mul2(f2(p2, p3), t23), d2, d3);
+        for (int c = 0; c < 32; c += 2) {
+          float x0, x1;
+          f2_split(mul2(f2(__uint_as_float(sv[q][c]), __uint_as_float(sv[q][c + 1])), c2x2), x0, x1);
+          const float p0 = ex2(x0), p1 = ex2(x1);
+          float d0, d1;
+          f2_split(mul2(f2(p0, p1), f2(__uint_as_float(dp[q][c]), __uint_as_float(dp[q][c + 1]))), d0,
+                   d1);
           pp[c / 2] = pack_bf16x2(p0, p1);
-          pp[c / 2 + 1] = pack_bf16x2(p2, p3);
           pd[c / 2] = pack_bf16x2(d0, d1);
-          pd[c / 2 + 1] = pack_bf16x2(d2, d3);
         }
-        // P^T over S^T's columns, dS^T over dP^T's: inside this half, already read
-        tmem_st16(tS + 64 * hw + 16 * (i - 2 * hw), pp);
-        tmem_st16(tP + 64 * hw + 16 * (i - 2 * hw), pd);
+        tmem_st16(tP + 64 * hw + 16 * q, pp);
+        tmem_st16(tP + 64 * hw + 32 + 16 * q, pd);
       }
       tmem_st_wait();
       tc_fence_before();
@@ -567,15 +646,79 @@ __device__ __forceinline__ void bwd_dkv_tile(const BwdPlan& p, int cta) {
 }
 
 // ------------------------------------------------------------ dQ
+// Shared memory of a dQ CTA: dO resident, rings of three K and three V tiles
+// (K_j is read by S_j and, later, by dQ_j; V_j by dP_j), barriers. Q lives in
+// tensor memory (the A operand of S = Q K^T), which leaves the shared memory
+// for the third V tile.
+template <int D>
+struct DqCfg {
+  static constexpr int kTileBytes = BwdCfg<D>::kTileBytes;
+  static constexpr int kBoxes = BwdCfg<D>::kBoxes;
+  static constexpr int kBoxBytes = BwdCfg<D>::kBoxBytes;
+  static constexpr int kKSlots = 3, kVSlots = 3;
+  static constexpr int kDO = 0;
+  static constexpr int kK0 = kTileBytes;
+  static constexpr int kV0 = kK0 + kKSlots * kTileBytes;
+  static constexpr int kBar = kV0 + kVSlots * kTileBytes;
+  static constexpr int kSmemBytes = kBar + 256 + 1024;  // + alignment slack
+  static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+};
+
+// One dQ CTA per (batch, query head, 128-row query tile): for every live key
+// tile j, S_j = Q K_j^T and dP_j = dO V_j^T (TMEM), dS_j = P_j (dP_j - delta)
+// by the elementwise warps into a TMEM region of its own, and dQ += dS_j K_j.
+// The products of tile j + 1 are issued as soon as the elementwise warps have
+// read S_j and dP_j, so they run while dS_j is computed; dQ_j follows.
+// TMEM: S [0,128), dP [128,256), dQ [256,256+D), dS (bf16) [384,448), Q (bf16,
+// written by the elementwise warps at the start) [448,448+D/2).
 template <int D>
 __device__ __forceinline__ void bwd_dq_tile(const BwdPlan& p, int cta) {
-  using C = BwdCfg<D>;
+  using C = DqCfg<D>;
   extern __shared__ uint8_t smem_raw[];
-  uint32_t base;
-  uint8_t* gbase;
-  BwdBars bb;
-  bwd_setup<D>(smem_raw, base, gbase, bb);
-  const uint32_t tmem = *bb.tmem_slot;
+  const uint32_t raw = smem_addr(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* const gbase = smem_raw + (base - raw);
+  // barriers (8 bytes each): Q/dO, K ring full/empty, V ring full/empty, then
+  // the single ones; the TMEM address and the abort flag after them
+  constexpr int kOffK = 8, kOffV = kOffK + 16 * C::kKSlots, kOffS = kOffV + 16 * C::kVSlots;
+  constexpr int kOffSlot = kOffS + 56;
+  static_assert(kOffSlot + 8 <= 256, "barrier area");
+  const uint32_t bars = base + C::kBar;
+  const uint32_t b_res = bars, b_kfull0 = bars + kOffK, b_kempty0 = bars + kOffK + 8 * C::kKSlots,
+                 b_vfull0 = bars + kOffV, b_vempty0 = bars + kOffV + 8 * C::kVSlots,
+                 b_sfull = bars + kOffS, b_sdpfree = bars + kOffS + 8, b_dsfull = bars + kOffS + 16,
+                 b_dsfree = bars + kOffS + 24, b_acc = bars + kOffS + 32, b_done = bars + kOffS + 40,
+                 b_qready = bars + kOffS + 48;
+  uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::kBar + kOffSlot);
+  volatile int* const abort_flag = reinterpret_cast<volatile int*>(gbase + C::kBar + kOffSlot + 4);
+  if (threadIdx.x == 0) {
+    mbar_init(b_res, 1);
+    for (int i = 0; i < C::kKSlots; ++i) {
+      mbar_init(b_kfull0 + 8 * i, 1);
+      mbar_init(b_kempty0 + 8 * i, 1);
+    }
+    for (int i = 0; i < C::kVSlots; ++i) {
+      mbar_init(b_vfull0 + 8 * i, 1);
+      mbar_init(b_vempty0 + 8 * i, 1);
+    }
+    mbar_init(b_sfull, 1);
+    mbar_init(b_sdpfree, 256);
+    mbar_init(b_dsfull, 256);
+    mbar_init(b_dsfree, 1);
+    mbar_init(b_acc, 1);
+    mbar_init(b_done, 1);
+    mbar_init(b_qready, 256);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if ((threadIdx.x >> 5) == 1) {
+    tmem_alloc(smem_addr(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const unsigned long long budget = p.timeout_ns;
 
@@ -594,97 +737,143 @@ __device__ __forceinline__ void bwd_dq_tile(const BwdPlan& p, int cta) {
     wlo = qw.x;
     whi = qw.y;
   }
-  const uint32_t sQ = base + C::kRes0, sDO = base + C::kRes1;
+  const uint32_t sDO = base + C::kDO;
 
   if (warp == 0) {
     // ---------------------------------------------------------- producer
     const bool leader = elect_one();
     if (leader) {
-      mbar_arrive_expect_tx(bb.res_full, 2 * C::kTileBytes);
+      mbar_arrive_expect_tx(b_res, C::kTileBytes);
 #pragma unroll
-      for (int bx = 0; bx < C::kBoxes; ++bx) {
-        tma_load_4d(sQ + bx * C::kBoxBytes, &p.qmap, bb.res_full, bx * 64, 128 * qt, hq, b);
-        tma_load_4d(sDO + bx * C::kBoxBytes, &p.domap, bb.res_full, bx * 64, 128 * qt, hq, b);
-      }
+      for (int bx = 0; bx < C::kBoxes; ++bx)
+        tma_load_4d(sDO + bx * C::kBoxBytes, &p.domap, b_res, bx * 64, 128 * qt, hq, b);
     }
-    int j = 0;
+    int jk = 0, jv = 0, fenced = -1;  // tiles whose K, V copies were issued
     bool ok = true;
-    int fenced = -1;
     for (int k = 0; ok && k < p.n_kvsegs; ++k) {
       const KvSeg& sg = bspan(p, k);
       int tb, te;
       bwd_live_tiles(p, k, wlo, whi, tb, te);
-      for (int t = tb; t < te; ++t) {
-        const int st = j & 1;
-        ok = warp_wait(bb.st_empty0 + 8 * st, ((j >> 1) & 1) ^ 1, bb.abort_flag, budget, kSiteBwdEmpty);
+      for (int t = tb; ok && t < te; ++t) {
+        const int ks = jk % C::kKSlots, vs = jv % C::kVSlots;
+        ok = warp_wait(b_kempty0 + 8 * ks, ((jk / C::kKSlots) & 1) ^ 1, abort_flag, budget, kSiteBwdEmpty);
         if (!ok) break;
-        const uint32_t sK = base + C::kStage0 + st * C::kStageBytes, sV = sK + C::kTileBytes;
         if (leader) {
           if (sg.chunk != fenced) {
             bwd_fence_maps(p, sg.chunk);
             fenced = sg.chunk;
           }
-          mbar_arrive_expect_tx(bb.st_full0 + 8 * st, 2 * C::kTileBytes);
+          mbar_arrive_expect_tx(b_kfull0 + 8 * ks, C::kTileBytes);
 #pragma unroll
-          for (int bx = 0; bx < C::kBoxes; ++bx) {
-            tma_load_4d(sK + bx * C::kBoxBytes, bkmap(p, sg.chunk), bb.st_full0 + 8 * st, bx * 64,
-                        sg.row0 + 128 * t, hkv, b);
-            tma_load_4d(sV + bx * C::kBoxBytes, bvmap(p, sg.chunk), bb.st_full0 + 8 * st, bx * 64,
-                        sg.row0 + 128 * t, hkv, b);
-          }
+          for (int bx = 0; bx < C::kBoxes; ++bx)
+            tma_load_4d(base + C::kK0 + ks * C::kTileBytes + bx * C::kBoxBytes, bkmap(p, sg.chunk),
+                        b_kfull0 + 8 * ks, bx * 64, sg.row0 + 128 * t, hkv, b);
         }
-        mbar_arrive(bb.st_full0 + 8 * st);
-        ++j;
+        ++jk;
+        __syncwarp();
+        ok = warp_wait(b_vempty0 + 8 * vs, ((jv / C::kVSlots) & 1) ^ 1, abort_flag, budget, kSiteBwdEmpty);
+        if (!ok) break;
+        if (leader) {
+          mbar_arrive_expect_tx(b_vfull0 + 8 * vs, C::kTileBytes);
+#pragma unroll
+          for (int bx = 0; bx < C::kBoxes; ++bx)
+            tma_load_4d(base + C::kV0 + vs * C::kTileBytes + bx * C::kBoxBytes, bvmap(p, sg.chunk),
+                        b_vfull0 + 8 * vs, bx * 64, sg.row0 + 128 * t, hkv, b);
+        }
+        ++jv;
+        __syncwarp();
       }
     }
-    if (!ok) {
-      drain_wait(bb.res_full, 0, budget);
-      for (int s = 0; s < 2; ++s) {
-        const int last = (j - 1 - s) >= 0 ? ((j - 1 - s) & ~1) + s : -1;
-        if (last >= 0 && last < j) drain_wait(bb.st_full0 + 8 * s, (last >> 1) & 1, budget);
+    if (!ok && leader) {
+      // let the copies in flight land before the CTA goes away: the last copy
+      // issued into each slot
+      drain_wait(b_res, 0, budget);
+      for (int i = 0; i < C::kKSlots; ++i) {
+        const int last = jk - 1 - ((jk - 1 - i) % C::kKSlots + C::kKSlots) % C::kKSlots;
+        if (last >= 0) drain_wait(b_kfull0 + 8 * i, (last / C::kKSlots) & 1, budget);
+      }
+      for (int i = 0; i < C::kVSlots; ++i) {
+        const int last = jv - 1 - ((jv - 1 - i) % C::kVSlots + C::kVSlots) % C::kVSlots;
+        if (last >= 0) drain_wait(b_vfull0 + 8 * i, (last / C::kVSlots) & 1, budget);
       }
     }
+    __syncwarp();
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA warp
     const bool leader = elect_one();
-    const uint32_t tS = tmem, tP = tmem + 128, tdQ = tmem + 256;
-    bool ok = warp_wait(bb.res_full, 0, bb.abort_flag, budget, kSiteBwdKv);
-    int j = 0;
-    for (int k = 0; ok && k < p.n_kvsegs; ++k) {
+    const uint32_t tS = tmem, tP = tmem + 128, tdQ = tmem + 256, tdS = tmem + 384;
+    const uint32_t tQ = tmem + 448;
+    constexpr uint32_t kIdQ = idesc_bf16_f32(128, D, 0, 1);
+    constexpr uint32_t kIdS = idesc_bf16_f32(128, 128, 0, 0);
+    // live key tiles of this query tile
+    int n = 0;
+    for (int k = 0; k < p.n_kvsegs; ++k) {
       int tb, te;
       bwd_live_tiles(p, k, wlo, whi, tb, te);
-      for (int t = tb; t < te; ++t) {
-        const int st = j & 1;
-        const uint32_t sK = base + C::kStage0 + st * C::kStageBytes, sV = sK + C::kTileBytes;
-        ok = warp_wait(bb.st_full0 + 8 * st, (j >> 1) & 1, bb.abort_flag, budget, kSiteBwdStage);
-        if (!ok) break;
+      n += te - tb;
+    }
+    bool ok = warp_wait(b_res, 0, abort_flag, budget, kSiteBwdKv) &&
+              warp_wait(b_qready, 0, abort_flag, budget, kSiteBwdKv);
+    auto issue_sdp = [&](int jj) {
+      const uint32_t sK = base + C::kK0 + (jj % C::kKSlots) * C::kTileBytes;
+      const uint32_t sV = base + C::kV0 + (jj % C::kVSlots) * C::kTileBytes;
+      // S = Q K^T: Q (bf16, two per column) is the TMEM A operand, K a K-major B
+      const uint64_t kd = sdesc_sw128(sK, 16, 1024);
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk)
+        mma_ts(tS, tQ + 8 * kk, kd + uint64_t(((kk >> 2) * C::kBoxBytes + (kk & 3) * 32) >> 4), kIdS,
+               kk > 0 ? 1u : 0u);
+      issue_abt<D>(tP, sDO, sV);  // dP = dO V^T
+      mma_commit(b_vempty0 + 8 * (jj % C::kVSlots));
+      mma_commit(b_sfull);
+    };
+    if (ok && n > 0) {
+      ok = warp_wait(b_kfull0, 0, abort_flag, budget, kSiteBwdStage) &&
+           warp_wait(b_vfull0, 0, abort_flag, budget, kSiteBwdStage);
+      if (ok) {
         tc_fence_after();
-        if (leader) {
-          issue_abt<D>(tS, sQ, sK);   // S  = Q K^T
-          issue_abt<D>(tP, sDO, sV);  // dP = dO V^T
-          mma_commit(bb.sdp_full);
-        }
+        if (leader) issue_sdp(0);
         __syncwarp();
-        ok = warp_wait(bb.ew_done, j & 1, bb.abort_flag, budget, kSiteBwdDs);
-        if (!ok) break;
-        tc_fence_after();
-        if (leader) {
-          issue_tmem_a<D>(tdQ, tS, sK, j > 0);  // dQ += dS K
-          mma_commit(bb.st_empty0 + 8 * st);
-        }
-        __syncwarp();
-        ++j;
       }
     }
+    for (int jj = 0; ok && jj < n; ++jj) {
+      if (jj + 1 < n) {
+        const int j1 = jj + 1;
+        ok = warp_wait(b_sdpfree, jj & 1, abort_flag, budget, kSiteBwdSdp) &&
+             warp_wait(b_kfull0 + 8 * (j1 % C::kKSlots), (j1 / C::kKSlots) & 1, abort_flag, budget,
+                       kSiteBwdStage) &&
+             warp_wait(b_vfull0 + 8 * (j1 % C::kVSlots), (j1 / C::kVSlots) & 1, abort_flag, budget,
+                       kSiteBwdStage);
+        if (!ok) break;
+        tc_fence_after();
+        if (leader) issue_sdp(j1);
+        __syncwarp();
+      }
+      ok = warp_wait(b_dsfull, jj & 1, abort_flag, budget, kSiteBwdDs);
+      if (!ok) break;
+      tc_fence_after();
+      if (leader) {
+        // dQ += dS K: dS (bf16) is the TMEM A operand, K_j an MN-major B
+        const uint32_t sK = base + C::kK0 + (jj % C::kKSlots) * C::kTileBytes;
+        const uint64_t bd = sdesc_sw128(sK, C::kBoxBytes, 1024);
+#pragma unroll
+        for (int kk = 0; kk < 128 / 16; ++kk)
+          mma_ts(tdQ, tdS + 8 * kk, bd + uint64_t((kk * 16 * 128) >> 4), kIdQ,
+                 (jj > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(b_dsfree);
+        mma_commit(b_kempty0 + 8 * (jj % C::kKSlots));
+      }
+      __syncwarp();
+    }
     if (leader) {
-      if (ok && j > 0) mma_commit(bb.acc_full);
-      mma_commit(bb.done);
+      if (ok && n > 0) mma_commit(b_acc);
+      mma_commit(b_done);
     }
     __syncwarp();
-    drain_wait(bb.done, 0, budget);
+    drain_wait(b_done, 0, budget);
   } else if (warp >= 4) {
     // ---------------------------------------------------------- elementwise
-    const int hw = (warp - 4) >> 2;              // column half of this warpgroup
+    const int hw = (warp - 4) >> 2;              // key-column half of this warpgroup
     const int sub = warp & 3;
     const int r = sub * 32 + lane;               // query row of the tile
     const int grow = 128 * qt + r;
@@ -696,14 +885,44 @@ __device__ __forceinline__ void bwd_dq_tile(const BwdPlan& p, int cta) {
     if (rvalid) key_window(p, bwd_row_position(p, grow), rlo, rhi);
     const uint32_t lane_off = uint32_t(sub * 32) << 16;
     const uint32_t tS = tmem + lane_off, tP = tmem + 128 + lane_off, tdQ = tmem + 256 + lane_off;
+    const uint32_t tdS = tmem + 384 + lane_off;
     const uint64_t c2x2 = f2(p.scale_log2, p.scale_log2), nlse = f2(-lse, -lse), ndel = f2(-del, -del);
+    {
+      // this row's Q into TMEM (row = lane, two bf16 per column): warpgroup h
+      // writes head-dim elements [64h, 64h + 64); rows past Sq are zero
+      constexpr int kWords = D / 2 - 32 * 0;  // words of a full row
+      const int w0 = 32 * hw, nw = min(32, kWords - w0);
+      uint32_t qw[32];
+      const uint4* src = reinterpret_cast<const uint4*>(
+          p.q + int64_t(b) * p.q_sb + int64_t(hq) * p.q_sh + int64_t(grow) * p.q_sr + 2 * w0);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const uint4 v = (rvalid && 4 * i < nw) ? src[i] : make_uint4(0u, 0u, 0u, 0u);
+        qw[4 * i] = v.x;
+        qw[4 * i + 1] = v.y;
+        qw[4 * i + 2] = v.z;
+        qw[4 * i + 3] = v.w;
+      }
+      const uint32_t tQ = tmem + 448 + lane_off + w0;
+      if (nw == 32) {
+        tmem_st32(tQ, qw);
+      } else if (nw == 16) {
+        uint32_t h16[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) h16[i] = qw[i];
+        tmem_st16(tQ, h16);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(b_qready);
+    }
     int j = 0;
     bool ok = true;
     for (int k = 0; ok && k < p.n_kvsegs; ++k) {
       const KvSeg& sg = bspan(p, k);
       int tb, te;
       bwd_live_tiles(p, k, wlo, whi, tb, te);
-      for (int t = tb; t < te; ++t) {
+      for (int t = tb; t < te; ++t, ++j) {
         // visible keys of this row: the range [C0, L) of the key tile
         int L = min(128, sg.len - 128 * t), C0 = 0;
         if (p.causal || p.n_docs) {
@@ -716,56 +935,61 @@ __device__ __forceinline__ void bwd_dq_tile(const BwdPlan& p, int cta) {
             if (rlo > first) C0 = min(L, (rlo - first - 1) / sg.step + 1);
           }
         }
-        ok = warp_wait(bb.sdp_full, j & 1, bb.abort_flag, budget, kSiteBwdSdp);
+        ok = warp_wait(b_sfull, j & 1, abort_flag, budget, kSiteBwdSdp);
         if (!ok) break;
         tc_fence_after();
-        {
-          // this warpgroup's 64 key columns, one TMEM wait
-          const int hh = hw;
-          uint32_t s[2][32], dp[2][32];
-          tmem_ld32(tS + 64 * hh, s[0]);
-          tmem_ld32(tS + 64 * hh + 32, s[1]);
-          tmem_ld32(tP + 64 * hh, dp[0]);
-          tmem_ld32(tP + 64 * hh + 32, dp[1]);
-          tmem_ld_wait();
-          reg_fence(s[0]);
-          reg_fence(s[1]);
-          reg_fence(dp[0]);
-          reg_fence(dp[1]);
+        uint32_t sv[2][32], dp[2][32];
+        tmem_ld32(tS + 64 * hw, sv[0]);
+        tmem_ld32(tS + 64 * hw + 32, sv[1]);
+        tmem_ld32(tP + 64 * hw, dp[0]);
+        tmem_ld32(tP + 64 * hw + 32, dp[1]);
+        tmem_ld_wait();
+        reg_fence(sv[0]);
+        reg_fence(sv[1]);
+        reg_fence(dp[0]);
+        reg_fence(dp[1]);
+        // S and dP are in registers: the next tile's products may overwrite them
+        tc_fence_before();
+        mbar_arrive(b_sdpfree);
+        uint32_t pd[2][16];
 #pragma unroll
-          for (int q = 0; q < 2; ++q) {
-            const int i = 2 * hh + q;
-            if (L < 128 || C0 > 0) {
+        for (int q = 0; q < 2; ++q) {
+          const int i = 2 * hw + q;
+          if (L < 128 || C0 > 0) {
 #pragma unroll
-              for (int c = 0; c < 32; ++c)
-                if (32 * i + c >= L || 32 * i + c < C0) s[q][c] = 0xff800000u;  // -inf: p = 0
-            }
-            uint32_t pd[16];
+            for (int c = 0; c < 32; ++c)
+              if (32 * i + c >= L || 32 * i + c < C0) sv[q][c] = 0xff800000u;  // -inf: p = 0
+          }
 #pragma unroll
-            for (int c = 0; c < 32; c += 2) {
-              float x0, x1;
-              f2_split(fma2(f2(__uint_as_float(s[q][c]), __uint_as_float(s[q][c + 1])), c2x2, nlse),
-                       x0, x1);
-              const uint64_t pr = f2(ex2(x0), ex2(x1));
-              float d0, d1;
-              f2_split(mul2(pr, add2(f2(__uint_as_float(dp[q][c]), __uint_as_float(dp[q][c + 1])), ndel)),
-                       d0, d1);
-              pd[c / 2] = pack_bf16x2(d0, d1);
-            }
-            tmem_st16(tS + 64 * hh + 16 * q, pd);  // dS inside this half of S, already read
+          for (int c = 0; c < 32; c += 2) {
+            float x0, x1;
+            f2_split(fma2(f2(__uint_as_float(sv[q][c]), __uint_as_float(sv[q][c + 1])), c2x2, nlse),
+                     x0, x1);
+            const uint64_t pr = f2(ex2(x0), ex2(x1));
+            float d0, d1;
+            f2_split(mul2(pr, add2(f2(__uint_as_float(dp[q][c]), __uint_as_float(dp[q][c + 1])), ndel)),
+                     d0, d1);
+            pd[q][c / 2] = pack_bf16x2(d0, d1);
           }
         }
+        // the previous tile's dQ product must have read its dS
+        if (j > 0) {
+          ok = warp_wait(b_dsfree, (j - 1) & 1, abort_flag, budget, kSiteBwdDs);
+          if (!ok) break;
+          tc_fence_after();
+        }
+        tmem_st16(tdS + 32 * hw, pd[0]);
+        tmem_st16(tdS + 32 * hw + 16, pd[1]);
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(bb.ew_done);
-        ++j;
+        mbar_arrive(b_dsfull);
       }
     }
     if (ok) {
       // ---- epilogue: dQ row times scale
       const bool any = j > 0;
       if (any) {
-        ok = warp_wait(bb.acc_full, 0, bb.abort_flag, budget, kSiteBwdAcc);
+        ok = warp_wait(b_acc, 0, abort_flag, budget, kSiteBwdAcc);
         tc_fence_after();
       }
       if (ok) {
@@ -824,7 +1048,12 @@ int launch_bwd_d(const BwdPlan& plan, const void* o, int o_fp32, int64_t o_sb, i
   if (e != cudaSuccess) return e;
   bwd_qtile_kernel<<<unsigned((plan.n_qtiles + 3) / 4), 128, 0, cs>>>(plan, qtile_pos);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  constexpr int kSmem = BwdCfg<D>::kSmemBytes;
+  const int64_t aux_threads = int64_t(plan.B) * plan.Hq * plan.n_qtiles * 128;
+  bwd_colaux_kernel<<<unsigned((aux_threads + 255) / 256), 256, 0, cs>>>(
+      plan, const_cast<uint8_t*>(plan.colaux));
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  constexpr int kSmem = BwdCfg<D>::kSmemBytes > DqCfg<D>::kSmemBytes ? BwdCfg<D>::kSmemBytes
+                                                                    : DqCfg<D>::kSmemBytes;
   const bool docs = plan.n_docs > 0;
   auto kern = docs ? bwd_kernel<D, true> : bwd_kernel<D, false>;
   if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem)) !=

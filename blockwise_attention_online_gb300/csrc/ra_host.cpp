@@ -741,6 +741,8 @@ ra_status run_bwd(const ra_problem* pb, const void* q, const ra_q_segment* segs,
   static thread_local ra::BwdPlan plan;
   std::memset(&plan, 0, sizeof(plan));
   if ((st = make_map(&plan.qmap, q, c.D, c.Sq, c.Hq, c.B, p.q_strides, "q")) != RA_OK) return st;
+  plan.q = static_cast<const uint16_t*>(q);
+  plan.q_sb = p.q_strides.batch; plan.q_sh = p.q_strides.head; plan.q_sr = p.q_strides.row;
   if ((st = make_map(&plan.domap, dout, c.D, c.Sq, c.Hq, c.B, p.o_strides, "dout")) != RA_OK)
     return st;
   // chunk tables: in the plan, or assembled here for device memory
@@ -820,7 +822,9 @@ ra_status run_bwd(const ra_problem* pb, const void* q, const ra_q_segment* segs,
   // per query row: lse2, delta; per query tile: key window bounds
   const size_t rows = size_t(c.B * c.Hq * c.Sq);
   auto up = [](size_t n) { return (n + 255) & ~size_t(255); };
-  const size_t tables_off = 2 * up(rows * 4) + up(size_t(plan.n_qtiles) * 16);
+  const size_t colaux_off = 2 * up(rows * 4) + up(size_t(plan.n_qtiles) * 16);
+  const size_t colaux_bytes = size_t(c.B * c.Hq) * size_t(plan.n_qtiles) * ra::kColAuxBytes;
+  const size_t tables_off = colaux_off + up(colaux_bytes);
   const size_t bytes = tables_off + (ext_tables ? lay.bytes : 0);
   cudaMemPool_t pool = nullptr;
   if ((st = lib_pool(&pool)) != RA_OK) return st;
@@ -833,6 +837,7 @@ ra_status run_bwd(const ra_problem* pb, const void* q, const ra_q_segment* segs,
   plan.lse2 = lse2;
   plan.delta = delta;
   plan.qtile_pos = qtile_pos;
+  plan.colaux = reinterpret_cast<const uint8_t*>(scratch + colaux_off);
   if (ext_tables) {
     char* t = scratch + tables_off;
     plan.ext_kmap = reinterpret_cast<const CUtensorMap*>(t + lay.kmap);

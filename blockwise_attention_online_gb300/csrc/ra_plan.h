@@ -173,6 +173,10 @@ struct alignas(128) BwdPlan {
   const float* delta;                // [B, Hq, Sq]
   const int4* qtile_pos;             // [n_qtiles]: key windows of its rows: lowest lo,
                                      // highest hi, highest lo, lowest hi
+  const uint8_t* colaux;             // [B * Hq][n_qtiles][kColAuxBytes]: per query tile
+                                     // the dK/dV CTA's column data (see ra_bwd.cu)
+  const uint16_t* q;                 // Q itself (bf16) and its element strides, read by the
+  int64_t q_sb, q_sh, q_sr;          //   dQ CTAs into tensor memory
   float* dq;                         // [B, Hq, Sq, D] fp32, dense
   float* dk[kTcMaxChunks];           // [B, Hkv, len_c, D] fp32, dense
   float* dv[kTcMaxChunks];
@@ -199,6 +203,11 @@ struct alignas(128) BwdPlan {
   const QPiece* ext_qp;                       // [n_qpieces]
 };
 static_assert(sizeof(BwdPlan) <= 32000, "backward plan must fit the parameter space");
+
+// Column data of one 128-row query tile for the dK/dV CTAs, as it lies in
+// shared memory: two K = 16 bias operand tiles (-lse2 / c and -delta, 4 KB
+// each) and the rows' key windows (int2 lo, hi; 1 KB).
+constexpr int kColAuxBytes = 2 * 4096 + 128 * 8;
 
 // Byte layout of the backward's device-resident chunk tables.
 struct BwdTablesLayout {

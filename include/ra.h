@@ -212,10 +212,13 @@ ra_status ra_stats_to_lse(int64_t rows, const float* m, const float* l, float* l
  * When the last rounds of work are split across CTAs (bf16 path), the call
  * allocates a scratch buffer of up to about 21 MB from the library's memory
  * pool on `stream` (cudaMallocFromPoolAsync) and frees it with cudaFreeAsync
- * on the same stream.
- * Limits of this build (RA_ERR_UNSUPPORTED beyond them): bf16 at most 32
- * non-empty chunks and 64 spans over all chunks; fp32 at most 256 chunks and
- * 320 spans; at most 64 spans over all query segments.
+ * on the same stream. A bf16 problem with more than 32 chunks, 64 key spans or
+ * 64 query spans keeps its chunk tables (tensor maps, spans) in device
+ * memory: a further ~256 bytes per chunk from the same allocation, filled by
+ * one copy from the host on `stream`.
+ * Limits of this build (RA_ERR_UNSUPPORTED beyond them): bf16 at most 4096
+ * chunks, 8192 key spans and 8192 query spans; fp32 at most 256 chunks, 320
+ * key spans and 64 query spans.
  */
 ra_status ra_ring_attention(const ra_problem* problem, const void* q,
                             const ra_q_segment* segs, int32_t nsegs,
@@ -247,8 +250,10 @@ typedef struct {
  * problem->o_strides (multiples of 8 elements). Outputs, fp32 and dense: dq
  * [B, Hq, Sq, D]; grads[k].dk, grads[k].dv [B, Hkv, len_k, D] for every chunk
  * with len_k > 0 (all zero when no query sees the chunk). The call takes a
- * small scratch (two floats per query row, 16 bytes per 128-row query tile)
- * from the library's memory pool on `stream` and frees it again.
+ * scratch buffer from the library's memory pool on `stream` and frees it
+ * again: two floats per query row and 9232 bytes per 128-row query tile and
+ * query head (the key/value CTAs' per-column data, about 72 bytes per query
+ * row).
  * bf16 inputs only (RA_ERR_UNSUPPORTED for RA_F32); head_dim 64, 96 or 128; the
  * chunk and span limits of ra_ring_attention's bf16 path.
  */
@@ -283,8 +288,10 @@ ra_status ra_ring_attention_bwd(const ra_problem* problem, const void* q,
  *   parts that must start cleared are cleared by each call on its stream.
  *   Calls whose kernels overlap on the GPU (other streams, other threads)
  *   race on the array: serialise them.
- * - A problem whose split needs more scratch than the array holds is rejected
- *   with RA_ERR_UNSUPPORTED before anything is launched.
+ * - The array also holds the device-resident chunk tables of problems with
+ *   more than 32 chunks or 64 spans (copied in on `stream`). A problem whose
+ *   split scratch and chunk tables need more than the array holds is
+ *   rejected with RA_ERR_UNSUPPORTED before anything is launched.
  * Arguments, layouts and results are those of ra_ring_attention.
  */
 #define RA_NOALLOC_SCRATCH_BYTES (24u << 20)

@@ -16,7 +16,7 @@ import pytest
 import torch
 
 import oracle
-from blockwise_attention_online_gb300 import layouts, ring_attention, ring_attention_bwd
+from blockwise_attention_online_gb300 import device_status, layouts, ring_attention, ring_attention_bwd
 from _util import f64
 
 pytestmark = pytest.mark.gpu
@@ -58,6 +58,7 @@ def _layout_bwd(q, k, v, do, kind, P, causal, out_dtype=None):
     dq, dk, dv = ring_attention_bwd(qs, kc, vc, O, dos, m, l, chunk_spans=rs, q_segments=segs,
                                     causal=causal)
     torch.cuda.synchronize()
+    device_status()
     dq = layouts.to_global(dq.cpu(), kind, P)
     dk = torch.cat([t.cpu() for t in dk], dim=2)
     dv = torch.cat([t.cpu() for t in dv], dim=2)
@@ -98,6 +99,7 @@ def test_backward_ragged_rows_and_chunks():
     O, m, l = ring_attention(qd, kc, vc, q_segments=segs, causal=True)
     dq, dk, dv = ring_attention_bwd(qd, kc, vc, O, dod, m, l, q_segments=segs, causal=True)
     torch.cuda.synchronize()
+    device_status()
     rq, rk, rv = oracle.attention_backward(f64(q), f64(k), f64(v), f64(do),
                                            np.arange(qpos0, 700), np.arange(700), True, 128 ** -0.5)
     _check("dq", dq, rq)
@@ -115,6 +117,7 @@ def test_backward_with_fp32_output_and_unseen_chunk():
     O, m, l = ring_attention(qd, kc, vc, causal=True, out_dtype=torch.float32)
     dq, dk, dv = ring_attention_bwd(qd, kc, vc, O, dod, m, l, causal=True)
     torch.cuda.synchronize()
+    device_status()
     rq, rk, rv = oracle.attention_backward(f64(q), f64(k), f64(v), f64(do), np.arange(256),
                                            np.arange(512), True, 64 ** -0.5)
     _check("dq", dq, rq)
@@ -136,6 +139,7 @@ def test_backward_chunking_invariance_at_8k():
     vc = [t.contiguous() for t in vc]
     dq8, dk8, dv8 = ring_attention_bwd(qd, kc, vc, O, dod, m, l, causal=True)
     torch.cuda.synchronize()
+    device_status()
     for a, b in ((dq8, dq1), (torch.cat(dk8, dim=2), dk1[0]), (torch.cat(dv8, dim=2), dv1[0])):
         assert torch.isfinite(a).all()
         # identical arithmetic per tile: the same values
