@@ -113,3 +113,48 @@ def ring_attention_backward(q, k_chunks, v_chunks, dout, q_pos, k_pos_chunks, ca
         dk_chunks.append(dkc)
         dv_chunks.append(dvc)
     return dq, dk_chunks, dv_chunks
+
+
+def gradient_rounding_bounds(q, k, v, dout, q_pos, k_pos, causal, scale, docs=None,
+                             u=2.0 ** -8):
+    """Elementwise bounds on the rounding error of a backward that rounds the
+    probabilities P and the score gradients dS to a number format of unit
+    roundoff ``u`` (bf16: 2^-8) before multiplying them, given the exact row
+    statistics and O, and accumulates the products in fp32.
+
+    This is the tolerance of the parity tests, derived from that arithmetic;
+    it is not part of the method. With the exact P, dS of the definition and
+    their rounded forms P~, dS~ (|P~ - P| <= u P, |dS~ - dS| <= u |dS|):
+
+        |dV~ - dV| <= u P^T |dO|
+        |dQ~ - dQ| <= scale u |dS| |K|
+        |dK~ - dK| <= scale u |dS|^T |Q|
+
+    (the fp32 parts -- the scores, exp2, the row term, the accumulation --
+    contribute errors some thousand times smaller). With grouped heads the
+    key/value bounds add up over the group's query heads, like the gradients.
+    Returns (bdq, bdk, bdv) of the shapes of q, k, v.
+    """
+    q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
+    B, Hq, Sq, D = q.shape
+    Hkv = k.shape[1]
+    g = _head_group(Hq, Hkv)
+    vis = _visible(q_pos, k_pos, causal, docs)
+    bdq, bdk, bdv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+    if Sq == 0 or k.shape[2] == 0:
+        return bdq, bdk, bdv
+    for b in range(B):
+        for h in range(Hq):
+            kh, vh = k[b, h // g], v[b, h // g]
+            s = np.where(vis, scale * (q[b, h] @ kh.T), -np.inf)
+            mrow = s.max(axis=1)
+            seen = np.isfinite(mrow)
+            w = np.exp(s - np.where(seen, mrow, 0.0)[:, None])
+            lrow = w.sum(axis=1)
+            p = np.where(seen[:, None], w / np.where(seen, lrow, 1.0)[:, None], 0.0)
+            dp = dout[b, h] @ vh.T
+            ads = np.abs(p * (dp - (p * dp).sum(axis=1, keepdims=True)))
+            bdv[b, h // g] += u * (p.T @ np.abs(dout[b, h]))
+            bdq[b, h] = scale * u * (ads @ np.abs(kh))
+            bdk[b, h // g] += scale * u * (ads.T @ np.abs(q[b, h]))
+    return bdq, bdk, bdv

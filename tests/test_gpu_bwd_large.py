@@ -1,11 +1,11 @@
 """Backward pass at the full 128K GQA causal size, in the launch configuration
 `bench.py --pass bwd --workload bf16_128k_gqa_causal` times (16 zigzag chunks
-walked in ring order): sampled dQ rows against the fp64 definition (each row
-exact against all of its visible keys), and every gradient element through
-chunking invariance against a one-chunk run ("Ring Attention: Distributed
-Reads with Online Softmax", section "Backward must aggregate shared
-dependencies": the distributed gradients must match a single-device
-reference).
+walked in ring order): sampled dQ rows and sampled dK, dV key rows against
+the fp64 definition (each exact against every visible (query, key) pair that
+contributes to it), and every gradient element through chunking invariance
+against a one-chunk run ("Ring Attention: Distributed Reads with Online
+Softmax", section "Backward must aggregate shared dependencies": the
+distributed gradients must match a single-device reference).
 
 Tolerance as in tests/test_gpu_bwd.py: max|err| <= 1e-2 * max|ref| per
 gradient (P and dS are rounded to bf16 before their products).
@@ -72,6 +72,34 @@ def test_bwd_128k_gqa_zigzag_sampled_rows_and_invariance():
     refs, gots = np.stack(refs), np.stack(gots)
     err = np.abs(gots - refs).max()
     assert err <= TOL * np.abs(refs).max(), f"sampled dq rows: max-abs {err:.3e}"
+
+    # sampled key rows of dK and dV of key/value head 0 (query heads 0..3),
+    # from the last 2048 positions: with the causal mask exactly the query
+    # rows [S - 2048, S) see them, so each is exact against all of its terms
+    tail = 2048
+    keys = sorted({S - 1, S - 2, S - tail, S - tail + 1, S - tail // 2}
+                  | {int(x) for x in np.random.default_rng(6).integers(S - tail, S, size=6)})
+    kh, vh = f64(k[0, 0]), f64(v[0, 0])
+    ref_dk = np.zeros((len(keys), w.D))
+    ref_dv = np.zeros((len(keys), w.D))
+    kpos = np.arange(S)
+    for h in range(group):
+        qh, doh = f64(q[0, h]), f64(do[0, h])
+        for r0 in range(S - tail, S, 256):
+            r1 = min(S, r0 + 256)
+            sc = (qh[r0:r1] @ kh.T) * w.scale
+            sc[kpos[None, :] > np.arange(r0, r1)[:, None]] = -np.inf
+            pm = np.exp(sc - sc.max(axis=1, keepdims=True))
+            pm /= pm.sum(axis=1, keepdims=True)
+            delta = (doh[r0:r1] * (pm @ vh)).sum(axis=1)
+            pk = pm[:, keys]
+            ds = pk * (doh[r0:r1] @ vh[keys].T - delta[:, None])
+            ref_dv += pk.T @ doh[r0:r1]
+            ref_dk += w.scale * (ds.T @ qh[r0:r1])
+    for name, got, ref in (("sampled dk rows", dk[0, 0, keys], ref_dk),
+                           ("sampled dv rows", dv[0, 0, keys], ref_dv)):
+        err = np.abs(f64(got) - ref).max()
+        assert err <= TOL * np.abs(ref).max(), f"{name}: max-abs {err:.3e}"
 
     # every element against a one-chunk run of the same problem
     O1, m1, l1 = ring_attention(q, [k], [v], causal=True)

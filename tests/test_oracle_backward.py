@@ -168,3 +168,58 @@ def test_planted_mistakes_fail_the_autograd_pin(kind):
     # the unplanted copy passes
     ok = oracle.attention_backward(q, k, v, do, pos, pos, True, 0.5)
     assert max(np.abs(a - b).max() for a, b in zip(ok, ref)) <= 1e-12
+
+
+def _bf16(x):
+    return torch.from_numpy(np.ascontiguousarray(x)).to(torch.bfloat16).double().numpy()
+
+
+def _rounded_backward(q, k, v, do, pos_q, pos_k, causal, scale, round_fn):
+    """The definition with P and dS passed through ``round_fn`` before their
+    products (single head group of one head each)."""
+    s = np.where(olay_vis(pos_q, pos_k, causal), scale * (q @ k.T), -np.inf)
+    m = s.max(axis=1)
+    w = np.exp(s - m[:, None])
+    p = w / w.sum(axis=1, keepdims=True)
+    dp = do @ v.T
+    ds = p * (dp - (p * dp).sum(axis=1, keepdims=True))
+    pr, dsr = round_fn(p), round_fn(ds)
+    return scale * (dsr @ k), scale * (dsr.T @ q), pr.T @ do
+
+
+def olay_vis(pos_q, pos_k, causal):
+    return (pos_k[None, :] <= pos_q[:, None]) if causal else np.ones((len(pos_q), len(pos_k)), bool)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_rounding_bounds_hold_for_bf16_rounded_probabilities(causal):
+    """The elementwise bound of the parity tests holds for a backward that
+    rounds P and dS to bf16 (unit roundoff 2^-8), and is not loose: the worst
+    element uses a sizeable share of it. Coarser rounding (unit roundoff
+    2^-5) breaks it."""
+    rng = np.random.default_rng(21)
+    Sq, Sk, D = 96, 160, 32
+    q = _bf16(rng.standard_normal((Sq, D)))
+    k = _bf16(rng.standard_normal((Sk, D)))
+    v = _bf16(rng.standard_normal((Sk, D)))
+    do = _bf16(rng.standard_normal((Sq, D)))
+    pq, pk = np.arange(Sk - Sq, Sk), np.arange(Sk)
+    scale = D ** -0.5
+    ref = oracle.attention_backward(q[None, None], k[None, None], v[None, None], do[None, None],
+                                    pq, pk, causal, scale)
+    bnd = oracle.gradient_rounding_bounds(q[None, None], k[None, None], v[None, None],
+                                          do[None, None], pq, pk, causal, scale)
+    got = _rounded_backward(q, k, v, do, pq, pk, causal, scale, _bf16)
+    worst = 0.0
+    for g, r, bd in zip(got, ref, bnd):
+        err = np.abs(g - r[0, 0])
+        assert (err <= bd[0, 0] + 1e-12).all()
+        worst = max(worst, float((err / np.maximum(bd[0, 0], 1e-300)).max()))
+    assert worst > 0.05, worst
+
+    def coarse(x):  # round to 5 significant bits: unit roundoff 2^-5
+        e = np.floor(np.log2(np.where(x != 0, np.abs(x), 1.0)))
+        return np.round(x / 2.0 ** (e - 4)) * 2.0 ** (e - 4)
+
+    got = _rounded_backward(q, k, v, do, pq, pk, causal, scale, coarse)
+    assert any((np.abs(g - r[0, 0]) > bd[0, 0]).any() for g, r, bd in zip(got, ref, bnd))
