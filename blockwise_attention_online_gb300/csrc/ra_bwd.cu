@@ -14,9 +14,8 @@
 //   dK_c = scale dS_c^T Q        dQ   = scale sum_c dS_c K_c
 //
 // Three launches on the caller's stream:
-//   bwd_prep_kernel    lse2 and delta per query row
-//   bwd_qtile_kernel   bounds of the key windows of each 128-row query tile
-//   bwd_colaux_kernel  per query tile, the column data of the dK/dV CTAs
+//   bwd_prep_kernel    per query row lse2 and delta, per query tile the
+//                      column data of the dK/dV CTAs and its key-window bounds
 //   bwd_kernel<D>      two kinds of CTA in one grid:
 //     bwd_dkv_tile     one per (batch, key/value head, 128-row key tile):
 //                      walks every live query tile of the heads that read it
@@ -143,104 +142,94 @@ __device__ __forceinline__ void bwd_live_tiles(const BwdPlan& p, int k, int lo, 
 }
 
 // ------------------------------------------------------------ preparation
-// Two query rows per warp, 16 lanes per row, 8 head_dim elements per lane
-// (head_dim <= 128), so that every load is coalesced: delta = sum_d dO * O
-// (O as the forward wrote it) and lse2 = m log2(e) + log2(l), +inf for a row
-// that sees no key.
-__global__ void bwd_prep_kernel(const void* o, int o_fp32, int64_t o_sb, int64_t o_sh,
-                                int64_t o_sr, const uint16_t* dout, const float* m,
-                                const float* l, int B, int Hq, int Sq, int D, float* lse2,
-                                float* delta) {
-  const int lane = threadIdx.x & 31, sl = lane & 15;
-  const int64_t row = ((int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5) * 2 + (lane >> 4);
-  const int64_t rows = int64_t(B) * Hq * Sq;
-  const bool active = row < rows;
-  float acc = 0.f;
-  if (active && sl < D / 8) {
-    const int64_t bh = row / Sq, i = row - bh * Sq;
-    const int64_t b = bh / Hq, h = bh - b * Hq;
-    const int64_t off = b * o_sb + h * o_sh + i * o_sr + 8 * sl;
-    const uint4 g = *reinterpret_cast<const uint4*>(dout + off);
-    const uint32_t w[4] = {g.x, g.y, g.z, g.w};
-    if (o_fp32) {
-      const float4* o4 = reinterpret_cast<const float4*>(static_cast<const float*>(o) + off);
-      const float4 a = o4[0], bq = o4[1];
-      const float ov[8] = {a.x, a.y, a.z, a.w, bq.x, bq.y, bq.z, bq.w};
+// One block of 128 threads per (batch x query head, 128-row query tile), one
+// thread per query row (the rows past Sq of the last tile included):
+//   delta = sum_d dO * O (O as the forward wrote it) and
+//   lse2 = m log2(e) + log2(l) (+inf for a row that sees no key);
+//   the dK/dV CTAs' column data of the tile, laid out as it will lie in
+//   shared memory (kColAuxBytes per tile): the bias rows -lse2 / c and
+//   -delta, each as three bf16 parts (-1e30 for a row that sees no key or
+//   lies past Sq, so that its probabilities are 0), and the row's key window;
+//   for batch x head 0, the bounds of the tile's key windows (x: lowest lo,
+//   y: highest hi, z: highest lo, w: lowest hi): a key tile inside [z, w] is
+//   visible to every row, one outside [x, y] to none.
+template <int D>
+__global__ void __launch_bounds__(128) bwd_prep_kernel(const __grid_constant__ BwdPlan p,
+                                                       const void* o, int o_fp32, int64_t o_sb,
+                                                       int64_t o_sh, int64_t o_sr,
+                                                       const uint16_t* dout, const float* m,
+                                                       const float* l, float* lse2, float* delta,
+                                                       int4* qtile_pos, uint8_t* colaux) {
+  const int qt = blockIdx.x % p.n_qtiles;
+  const int bh = blockIdx.x / p.n_qtiles;
+  const int b = bh / p.Hq, h = bh - b * p.Hq;
+  const int n = threadIdx.x;
+  const int row = 128 * qt + n;
+  const bool valid = row < p.Sq;
+  float dl = 0.f, l2 = kInf;
+  int lo = 0x7fffffff, hi = int(0x80000000);  // an empty window
+  if (valid) {
+    const int64_t off = int64_t(b) * o_sb + int64_t(h) * o_sh + int64_t(row) * o_sr;
+    const uint4* g = reinterpret_cast<const uint4*>(dout + off);
+    float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll 4
+    for (int k = 0; k < D / 8; ++k) {
+      const uint4 gv = g[k];
+      const uint32_t w[4] = {gv.x, gv.y, gv.z, gv.w};
+      if (o_fp32) {
+        const float4* o4 = reinterpret_cast<const float4*>(static_cast<const float*>(o) + off) + 2 * k;
+        const float4 a = o4[0], c = o4[1];
+        const float ov[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        acc = fmaf(__uint_as_float(w[k] << 16), ov[2 * k], acc);
-        acc = fmaf(__uint_as_float(w[k] & 0xffff0000u), ov[2 * k + 1], acc);
-      }
-    } else {
-      const uint4 a = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(o) + off);
-      const uint32_t v[4] = {a.x, a.y, a.z, a.w};
+        for (int e = 0; e < 4; ++e) {
+          acc0 = fmaf(__uint_as_float(w[e] << 16), ov[2 * e], acc0);
+          acc1 = fmaf(__uint_as_float(w[e] & 0xffff0000u), ov[2 * e + 1], acc1);
+        }
+      } else {
+        const uint4 ovv = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(o) + off)[k];
+        const uint32_t v[4] = {ovv.x, ovv.y, ovv.z, ovv.w};
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        acc = fmaf(__uint_as_float(w[k] << 16), __uint_as_float(v[k] << 16), acc);
-        acc = fmaf(__uint_as_float(w[k] & 0xffff0000u), __uint_as_float(v[k] & 0xffff0000u), acc);
+        for (int e = 0; e < 4; ++e) {
+          acc0 = fmaf(__uint_as_float(w[e] << 16), __uint_as_float(v[e] << 16), acc0);
+          acc1 = fmaf(__uint_as_float(w[e] & 0xffff0000u), __uint_as_float(v[e] & 0xffff0000u), acc1);
+        }
       }
     }
+    dl = acc0 + acc1;
+    const int64_t srow = int64_t(bh) * p.Sq + row;
+    const float lr = l[srow];
+    l2 = lr > 0.f ? fmaf(m[srow], kLog2e, log2f(lr)) : kInf;
+    delta[srow] = dl;
+    lse2[srow] = l2;
+    key_window(p, bwd_row_position(p, row), lo, hi);
   }
-  // sum over the 16 lanes of each row (the xor offsets stay inside a half)
-#pragma unroll
-  for (int d = 8; d > 0; d >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, d);
-  if (active && sl == 0) {
-    delta[row] = acc;
-    const float lr = l[row];
-    lse2[row] = lr > 0.f ? fmaf(m[row], kLog2e, log2f(lr)) : kInf;
-  }
-}
-
-// Column data of the dK/dV CTAs for every 128-row query tile, laid out as it
-// will lie in shared memory (kColAuxBytes per tile; one thread per query row,
-// the rows past Sq of the last tile included): the bias rows -lse2 / c and
-// -delta, each as three bf16 parts (a row that sees no key, or lies past Sq,
-// gets -1e30, so that its probabilities are 0), and the row's key window.
-// The producer then fetches a query tile's column data with one bulk copy.
-__global__ void bwd_colaux_kernel(const __grid_constant__ BwdPlan p, uint8_t* colaux) {
-  const int64_t t = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
-  const int64_t per_bh = int64_t(p.n_qtiles) * 128;
-  if (t >= int64_t(p.B) * p.Hq * per_bh) return;
-  const int64_t bh = t / per_bh;
-  const int row = int(t - bh * per_bh);
-  const bool valid = row < p.Sq;
-  const float l2 = valid ? p.lse2[bh * p.Sq + row] : kInf;
-  const float xl = l2 < kInf ? -l2 / p.scale_log2 : -1e30f;
-  const float xd = valid ? -p.delta[bh * p.Sq + row] : 0.f;
-  int lo = 0x7fffffff, hi = int(0x80000000);  // an empty window
-  if (valid) key_window(p, bwd_row_position(p, row), lo, hi);
-  uint8_t* tile = colaux + (bh * p.n_qtiles + row / 128) * int64_t(kColAuxBytes);
-  const int n = row & 127;
-  const uint32_t off = bias_row_offset(n);
-  *reinterpret_cast<uint4*>(tile + off) = bias_split3(xl);
-  *reinterpret_cast<uint4*>(tile + off + 128) = make_uint4(0u, 0u, 0u, 0u);
-  *reinterpret_cast<uint4*>(tile + 4096 + off) = bias_split3(xd);
-  *reinterpret_cast<uint4*>(tile + 4096 + off + 128) = make_uint4(0u, 0u, 0u, 0u);
+  uint8_t* tile = colaux + (int64_t(bh) * p.n_qtiles + qt) * int64_t(kColAuxBytes);
+  const uint32_t boff = bias_row_offset(n);
+  *reinterpret_cast<uint4*>(tile + boff) = bias_split3(l2 < kInf ? -l2 / p.scale_log2 : -1e30f);
+  *reinterpret_cast<uint4*>(tile + boff + 128) = make_uint4(0u, 0u, 0u, 0u);
+  *reinterpret_cast<uint4*>(tile + 4096 + boff) = bias_split3(-dl);
+  *reinterpret_cast<uint4*>(tile + 4096 + boff + 128) = make_uint4(0u, 0u, 0u, 0u);
   reinterpret_cast<int2*>(tile + 8192)[n] = make_int2(lo, hi);
-}
-
-// One warp per 128-row query tile: bounds of its rows' key windows
-// (x: lowest lo, y: highest hi, z: highest lo, w: lowest hi). A key tile
-// inside [z, w] is visible to every row; one outside [x, y] to none.
-__global__ void bwd_qtile_kernel(const __grid_constant__ BwdPlan p, int4* out) {
-  const int t = int((int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5);
-  const int lane = threadIdx.x & 31;
-  if (t >= p.n_qtiles) return;  // whole warps
-  int4 w = make_int4(0x7fffffff, -1, -1, 0x7fffffff);
-  const int r1 = min(p.Sq, 128 * t + 128);
-  for (int r = 128 * t + lane; r < r1; r += 32) {
-    int lo, hi;
-    key_window(p, bwd_row_position(p, r), lo, hi);
-    w.x = min(w.x, lo);
-    w.y = max(w.y, hi);
-    w.z = max(w.z, lo);
-    w.w = min(w.w, hi);
+  if (bh == 0) {
+    // the same positions for every batch element and head: one block per tile
+    __shared__ int4 red[4];
+    int4 w = valid ? make_int4(lo, hi, lo, hi) : make_int4(0x7fffffff, -1, -1, 0x7fffffff);
+    w.x = __reduce_min_sync(0xffffffffu, w.x);
+    w.y = __reduce_max_sync(0xffffffffu, w.y);
+    w.z = __reduce_max_sync(0xffffffffu, w.z);
+    w.w = __reduce_min_sync(0xffffffffu, w.w);
+    if ((n & 31) == 0) red[n >> 5] = w;
+    __syncthreads();
+    if (n == 0) {
+      for (int i = 1; i < 4; ++i) {
+        w.x = min(w.x, red[i].x);
+        w.y = max(w.y, red[i].y);
+        w.z = max(w.z, red[i].z);
+        w.w = min(w.w, red[i].w);
+      }
+      qtile_pos[qt] = w;
+    }
   }
-  w.x = __reduce_min_sync(0xffffffffu, w.x);
-  w.y = __reduce_max_sync(0xffffffffu, w.y);
-  w.z = __reduce_max_sync(0xffffffffu, w.z);
-  w.w = __reduce_min_sync(0xffffffffu, w.w);
-  if (lane == 0) out[t] = w;
 }
 
 // ------------------------------------------------------------ shared pieces
@@ -1040,18 +1029,12 @@ int launch_bwd_d(const BwdPlan& plan, const void* o, int o_fp32, int64_t o_sb, i
                  int64_t o_sr, const void* dout, const float* m, const float* l, float* lse2,
                  float* delta, int4* qtile_pos, void* stream) {
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
-  const int64_t rows = int64_t(plan.B) * plan.Hq * plan.Sq;
-  bwd_prep_kernel<<<unsigned((rows * 16 + 255) / 256), 256, 0, cs>>>(
-      o, o_fp32, o_sb, o_sh, o_sr, static_cast<const uint16_t*>(dout), m, l, plan.B, plan.Hq,
-      plan.Sq, D, lse2, delta);
+  const int64_t tiles = int64_t(plan.B) * plan.Hq * plan.n_qtiles;
+  bwd_prep_kernel<D><<<unsigned(tiles), 128, 0, cs>>>(
+      plan, o, o_fp32, o_sb, o_sh, o_sr, static_cast<const uint16_t*>(dout), m, l, lse2, delta,
+      qtile_pos, const_cast<uint8_t*>(plan.colaux));
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  bwd_qtile_kernel<<<unsigned((plan.n_qtiles + 3) / 4), 128, 0, cs>>>(plan, qtile_pos);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  const int64_t aux_threads = int64_t(plan.B) * plan.Hq * plan.n_qtiles * 128;
-  bwd_colaux_kernel<<<unsigned((aux_threads + 255) / 256), 256, 0, cs>>>(
-      plan, const_cast<uint8_t*>(plan.colaux));
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
   constexpr int kSmem = BwdCfg<D>::kSmemBytes > DqCfg<D>::kSmemBytes ? BwdCfg<D>::kSmemBytes
                                                                     : DqCfg<D>::kSmemBytes;
   const bool docs = plan.n_docs > 0;
