@@ -31,6 +31,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "ring_attention fwd TFLOP/s (bf16, causal-adjusted) and % of GB300 tensor peak"
 L2_FLUSH_BYTES = 512 << 20  # > 129 MB L2
+E2E_STREAMS = 3
 
 
 def _peaks():
@@ -285,9 +286,10 @@ def run_gpu(args):
 
     # End to end through the host-buffer entry point: every step copies that
     # step's inputs from pinned host memory to the device, runs the ring pass
-    # and copies O, m, l back. Steps alternate over two streams, so one step's
-    # copies overlap the other step's kernel (each call has its own device
-    # copies).
+    # and copies O, m, l back. Steps rotate over three streams, so that one
+    # step's input copies run while another step's kernel runs and a third
+    # step's outputs come back (copies in the two directions use separate copy
+    # engines; each call has its own device buffers).
     e2e = None
     if not args.no_e2e:
         from blockwise_attention_online_gb300 import ring_attention_host
@@ -296,16 +298,16 @@ def run_gpu(args):
         hv = [x.cpu().pin_memory() for x in vc]
         outs = [(torch.empty(out.shape, dtype=out.dtype).pin_memory(),
                  torch.empty(m.shape, dtype=torch.float32).pin_memory(),
-                 torch.empty(l.shape, dtype=torch.float32).pin_memory()) for _ in range(2)]
+                 torch.empty(l.shape, dtype=torch.float32).pin_memory()) for _ in range(E2E_STREAMS)]
         h2d = hq.numel() * hq.element_size() + sum(x.numel() * x.element_size() for x in hk + hv)
         d2h = sum(t.numel() * t.element_size() for t in outs[0])
         n_e2e = max(3, min(args.steps, 100))
-        streams = [torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)]
+        streams = [torch.cuda.Stream(device=dev) for _ in range(E2E_STREAMS)]
 
         def e2e_step(i):
-            ho, hm, hl = outs[i % 2]
+            ho, hm, hl = outs[i % E2E_STREAMS]
             ring_attention_host(hq, hk, hv, chunk_spans=rs, q_segments=segs, causal=w.causal,
-                                out=ho, m=hm, l=hl, docs=docs, stream=streams[i % 2])
+                                out=ho, m=hm, l=hl, docs=docs, stream=streams[i % E2E_STREAMS])
 
         for i in range(4):
             e2e_step(i)
@@ -320,7 +322,7 @@ def run_gpu(args):
         e2e = {"value": round(whole_job_tflops(flops, n_e2e, world, el * 1e3), 3),
                "unit": "TFLOP/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-               "steps": n_e2e, "streams": 2,
+               "steps": n_e2e, "streams": E2E_STREAMS,
                "call": "ra_ring_attention_host (pinned host buffers)"}
         device_status()
 
