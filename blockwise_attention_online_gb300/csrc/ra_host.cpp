@@ -45,7 +45,14 @@ ra_status ok() {
 constexpr int64_t kPosLimit = (int64_t(1) << 31) - 1;
 // Fixed cost of a stream-K unit in key-tile steps (measured: a unit switch
 // costs about two tile steps of a long unit).
-constexpr int64_t kUnitCost = 2;
+// Weights of the stream-K split, in half key-tile steps: a plain step 2, the
+// fixed cost of a unit 4 (measured: a unit switch costs about two steps of a
+// long unit), and a step of a unit whose rows lie in more than one packed
+// document 3 (its rows have different key windows, so its steps mask element
+// by element; of the factors tried, 1.5 balanced best).
+constexpr int64_t kTileCost = 2;
+constexpr int64_t kUnitCost = 4;
+constexpr int64_t kMixedTileCost = 3;
 constexpr int64_t kRowLimit = (int64_t(1) << 31) - 256;
 
 // A flattened monotone span of rows with global positions.
@@ -475,26 +482,36 @@ ra_status run_tc(const Common& c, const ra_problem& p, const void* q,
   plan.n_units = int32_t(units);
   if (units == 0) return ok();
 
-  // live key tiles of every query-tile pair (the same for every head)
-  std::vector<int64_t> work(npairs, 0);
+  // live key tiles of every query-tile pair (the same for every head), and
+  // the cost of one of its steps: a pair whose rows lie in more than one
+  // packed document costs kMixedTileCost per step
+  std::vector<int64_t> work(npairs, 0), step_cost(npairs, kTileCost);
   for (int64_t qp = 0; qp < npairs; ++qp) {
     int64_t r0 = qp * ra::kTcRowsPerUnit, r1 = std::min(c.Sq, r0 + ra::kTcRowsPerUnit);
     int64_t qmin, qmax;
     qrange_of_rows(c.qspans, r0, r1, &qmin, &qmax);
     for (const Span& kv : c.kvspans) work[qp] += live_tiles(c, kv, qmin, qmax);
+    if (c.n_docs > 0) {
+      int lo_min, lo_max, unused;
+      ra::key_window(c, int(qmin), lo_min, unused);
+      ra::key_window(c, int(qmax), lo_max, unused);
+      if (lo_min != lo_max) step_cost[qp] = kMixedTileCost;  // different documents
+    }
   }
-  // visit order of the pairs: longest first when the work differs (causal,
-  // documents)
+  // visit order of the pairs: costliest first when the work differs
+  // (causal, documents)
   std::vector<int32_t> order(npairs);
   std::iota(order.begin(), order.end(), 0);
   plan.has_order = 0;
   if (npairs <= ra::kTcMaxOrder && (c.causal || c.n_docs > 0)) {
-    std::stable_sort(order.begin(), order.end(),
-                     [&](int32_t a, int32_t b) { return work[a] > work[b]; });
+    std::stable_sort(order.begin(), order.end(), [&](int32_t a, int32_t b) {
+      return work[a] * step_cost[a] > work[b] * step_cost[b];
+    });
     for (int64_t i = 0; i < npairs; ++i) plan.order[i] = uint16_t(order[i]);
     plan.has_order = 1;
   }
   auto unit_tiles = [&](int64_t u) { return work[order[u / BH]]; };
+  auto unit_step_cost = [&](int64_t u) { return step_cost[order[u / BH]]; };
 
   const int sms = num_sms();
   if (sms <= 0) return cuda_status(cudaErrorNoDevice, "querying the SM count");
@@ -521,25 +538,31 @@ ra_status run_tc(const Common& c, const ra_problem& p, const void* q,
   }
   if (T > (int64_t(1) << 30)) return fail(RA_ERR_UNSUPPORTED, "stream-K range too large");
   plan.sk_total = int32_t(T);
-  // CTA boundaries on the tile line: the tail units are weighed as their
-  // tiles plus kUnitCost for the unit's fixed costs (its Q load, the switch
-  // of the softmax warps, its epilogue), and the weighted line is cut in G
-  // equal shares; a cut inside a unit's fixed cost moves to its first tile.
-  // With equal units this is the plain cut of the tiles in G shares; with
-  // many short units (causal starts, packed documents) the CTAs that get
-  // them take fewer tiles.
+  // CTA boundaries on the tile line: each tail unit is weighed as its tiles
+  // times its step cost plus kUnitCost for the unit's fixed costs (its Q
+  // load, the switch of the softmax warps, its epilogue), and the weighted
+  // line is cut in G equal shares; a cut inside a unit's fixed cost moves to
+  // its first tile. With equal units this is the plain cut of the tiles in G
+  // shares; with many short units (causal starts, packed documents) or
+  // costlier steps the CTAs that get them take fewer tiles.
   {
-    const int64_t W = T + kUnitCost * sk_units;
+    int64_t W = 0;
+    for (int64_t i = 0; i < sk_units; ++i)
+      W += kUnitCost + unit_step_cost(R * G + i) * (plan.sk_prefix[i + 1] - plan.sk_prefix[i]);
     int64_t i = 0, q = 0;  // unit i starts at weight q
     plan.sk_bound[0] = 0;
     for (int64_t c = 1; c <= G; ++c) {
       const int64_t x = c * W / G;
-      while (i < sk_units && q + kUnitCost + (plan.sk_prefix[i + 1] - plan.sk_prefix[i]) <= x) {
-        q += kUnitCost + (plan.sk_prefix[i + 1] - plan.sk_prefix[i]);
+      while (i < sk_units) {
+        const int64_t wi = kUnitCost + unit_step_cost(R * G + i) *
+                                           (plan.sk_prefix[i + 1] - plan.sk_prefix[i]);
+        if (q + wi > x) break;
+        q += wi;
         ++i;
       }
       const int64_t n = i < sk_units ? plan.sk_prefix[i + 1] - plan.sk_prefix[i] : 0;
-      const int64_t in = std::min(n, std::max<int64_t>(0, x - q - kUnitCost));
+      const int64_t f = i < sk_units ? unit_step_cost(R * G + i) : 1;
+      const int64_t in = std::min(n, std::max<int64_t>(0, x - q - kUnitCost) / f);
       plan.sk_bound[c] = int32_t(i < sk_units ? plan.sk_prefix[i] + in : T);
     }
     plan.sk_bound[G] = int32_t(T);
