@@ -567,6 +567,16 @@ ra_status run_tc(const Common& c, const ra_problem& p, const void* q,
     }
     plan.sk_bound[G] = int32_t(T);
   }
+  for (int64_t cta = 0; cta < G; ++cta) {
+    const int64_t a = plan.sk_bound[cta];
+    int64_t lo = 0, hi = sk_units - 1;
+    while (lo < hi) {
+      const int64_t mid = (lo + hi + 1) >> 1;
+      if (plan.sk_prefix[mid] <= a) lo = mid; else hi = mid - 1;
+    }
+    while (lo > 0 && plan.sk_prefix[lo] == a && plan.sk_prefix[lo - 1] == a) --lo;
+    plan.sk_first[cta] = int16_t(lo);
+  }
   // does any CTA boundary fall strictly inside a unit?
   bool split = false;
   for (int64_t cta = 1; cta < G && !split; ++cta) {

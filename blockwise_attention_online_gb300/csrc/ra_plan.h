@@ -86,7 +86,7 @@ constexpr int kTcMaxKvSegs = 64;
 constexpr int kTcMaxChunksAll = 4096;
 constexpr int kTcMaxKvSegsAll = 8192;
 constexpr int kTcMaxQPiecesAll = 8192;  // query spans (the plan holds kMaxQPieces)
-constexpr int kTcMaxOrder = 8192;  // q-tile pairs that can be LPT-ordered
+constexpr int kTcMaxOrder = 7936;  // q-tile pairs that can be LPT-ordered
 constexpr int kTcRowsPerUnit = 256;  // two 128-row query tiles per work unit
 constexpr int kTcMaxSkUnits = 320;   // units in the stream-K tail (< 2 x grid)
 constexpr int kTcMaxGrid = 160;      // CTAs of one launch (one per SM)
@@ -124,6 +124,10 @@ struct alignas(128) TcPlan {
   TcScratch scratch;                 // null pointers when no unit is split
   int32_t sk_prefix[kTcMaxSkUnits + 1];
   int32_t sk_bound[kTcMaxGrid + 1];
+  // first stream-K unit of CTA c: the last unit starting at or before
+  // sk_bound[c], stepped back over empty units starting there (placed by the
+  // host: the walk then starts with one read instead of a search)
+  int16_t sk_first[kTcMaxGrid];
   int32_t chunk_seg_begin[kTcMaxChunks + 1];
   QPiece qp[kMaxQPieces];
   KvSeg ks[kTcMaxKvSegs];

@@ -16,6 +16,15 @@
 // m, l stay in registers and O in TMEM for the whole walk; only the final
 // O = u / l (or u itself for chunk statistics) goes back to HBM.
 //
+// The softmax comes in two forms, chosen per launch. Without a document mask
+// it takes two passes over S: the row max first (one TMEM read of all 128
+// columns), then the exponentials, with O rescaled when the max grows by more
+// than 2^8. With packed documents (short units, masked tiles) it takes one
+// pass: each 32-column chunk is exponentiated against the row's reference max,
+// which moves (with O, the sums and the P already written rescaled) only when
+// a chunk's max exceeds it by more than 2^32. Both are exact softmax; each form
+// measured faster on its own kind of workload.
+//
 // Warp roles (384 threads):
 //   warp 0      TMA producer: Q tiles once per unit, then K_j, V_j into a ring
 //               of shared-memory stages. The pages overlap the transfer of the
@@ -65,9 +74,15 @@ using namespace ptx;
 
 constexpr int kThreads = 384;
 constexpr float kNegInf = -__builtin_huge_valf();
-// Rescale O and l only when the running max (log2 units) grows by more than
-// this: p = 2^(s - m_ref) then stays below 2^8, exact enough in bf16/fp32.
+// Two-pass softmax (no document mask): O and l are rescaled only when the
+// running max (log2 units) grows by more than this, so p = 2^(s - m_ref) stays
+// below 2^8.
 constexpr float kRescaleLog2 = 8.0f;
+// One-pass softmax (packed documents): a row's exponent offset (its reference
+// max, log2 units) moves, with O, l and lr rescaled, only when a chunk's max
+// exceeds it by more than this: then p = 2^(s - m_ref) <= 2^32, and a sum of
+// 2^24 such terms times any |V| below 2^60 stays inside fp32's range.
+constexpr float kRefSlackLog2 = 32.0f;
 
 template <int D>
 struct Cfg {
@@ -246,14 +261,7 @@ struct Walker {
     k = 0;
     a = p.sk_bound[blockIdx.x];
     b = p.sk_bound[blockIdx.x + 1];
-    // last unit starting at or before a; step back over empty units at a
-    int lo = 0, hi = p.sk_units - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (p.sk_prefix[mid] <= a) lo = mid; else hi = mid - 1;
-    }
-    while (lo > 0 && p.sk_prefix[lo] == a && p.sk_prefix[lo - 1] == a) --lo;
-    i = lo;
+    i = p.sk_first[blockIdx.x];
   }
   __device__ __forceinline__ bool next(const TcPlan& p, Item& it) {
     if (k < p.dp_rounds) {
@@ -318,7 +326,45 @@ __device__ __forceinline__ void wg_bar(int id) {
   asm volatile("bar.sync %0, 128;" ::"r"(id) : "memory");
 }
 
+// Rare path of the softmax: O (D fp32 columns at tO) times alpha.
 template <int D>
+__device__ __noinline__ void rescale_o(uint32_t tO, float alpha) {
+#pragma unroll 1
+  for (int cc = 0; cc < D / 16; ++cc) {
+    uint32_t o[16];
+    tmem_ld16(tO + 16 * cc, o);
+    tmem_ld_wait();
+    reg_fence(o);
+#pragma unroll
+    for (int c = 0; c < 16; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+    tmem_st16(tO + 16 * cc, o);
+  }
+}
+
+// Rare path of the softmax: the first n P chunks (bf16 pairs at tS) times
+// alpha, rounded again; returns their sums (the lr accumulators).
+__device__ __noinline__ float4 rescale_p(uint32_t tS, int n, float alpha) {
+  float racc[4] = {0.f, 0.f, 0.f, 0.f};
+  tmem_st_wait();
+#pragma unroll 1
+  for (int cc = 0; cc < n; ++cc) {
+    uint32_t w[16];
+    tmem_ld16(tS + 16 * cc, w);
+    tmem_ld_wait();
+    reg_fence(w);
+#pragma unroll
+    for (int c = 0; c < 16; ++c) {
+      const float a = __uint_as_float(w[c] << 16) * alpha;
+      const float b = __uint_as_float(w[c] & 0xffff0000u) * alpha;
+      w[c] = pack_bf16x2(a, b);
+      add_bf16x2_halves(racc[2 * (c & 1)], racc[2 * (c & 1) + 1], w[c]);
+    }
+    tmem_st16(tS + 16 * cc, w);
+  }
+  return make_float4(racc[0], racc[1], racc[2], racc[3]);
+}
+
+template <int D, bool kOnePass>
 __global__ void __launch_bounds__(kThreads, 1) tc_ring_kernel(const __grid_constant__ TcPlan p) {
   using C = Cfg<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -594,7 +640,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ring_kernel(const __grid_const
       const bool rvalid = grow < p.Sq;
       // keys this row may see: positions [rlo, rhi]
       int rlo = 0, rhi = 0x7ffffffe;
-      if (rvalid) key_window(p, row_position(p, grow), rlo, rhi);
+      if (rvalid && (p.causal || p.n_docs > 0)) key_window(p, row_position(p, grow), rlo, rhi);
       float m_ref = kNegInf, mx = kNegInf, l = 0.f, lr = 0.f;
       if (n > 0) {
         TileIter iter;
@@ -622,98 +668,179 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ring_kernel(const __grid_const
           if (!ok) break;
           ++sc;
           tc_fence_after();
-          // Pass 1: row max. All 128 columns are read with a single wait (the
-          // load latency is paid once); pass 2 reads S again in 32-column
-          // chunks inside a compact loop: the hot code shares each scheduler's
-          // instruction cache with the MMA warp, and a small footprint measured
-          // faster than a fully unrolled single pass.
-          float mx0 = kNegInf, mx1 = kNegInf;
-          {
-            uint32_t s[4][32];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) tmem_ld32(tS + 32 * i, s[i]);
-            tmem_ld_wait();
-#pragma unroll
-            for (int i = 0; i < 4; ++i) reg_fence(s[i]);
-            if (L < 128 || C0 > 0) {
-#pragma unroll
-              for (int i = 0; i < 4; ++i)
-#pragma unroll
+          if constexpr (kOnePass) {
+            // One pass over S in 32-column chunks. The exponent offset is the
+            // row's reference max m_ref (log2 units): set from the max of the
+            // row's first visible chunk and moved only when a chunk's max exceeds
+            // it by more than kRefSlackLog2, so p = 2^(s*c2 - m_ref) stays below
+            // 2^kRefSlackLog2 (far from overflow; floating point is scale
+            // invariant, and O, l, lr carry the same scale). Each chunk's max is
+            // reduced first, as a shallow tree; a chunk that moves the reference
+            // first rescales O, the sums and this step's P chunks already
+            // written (warp-uniform, since TMEM access is warp-collective; rows
+            // that keep their reference take alpha = 1).
+            const uint64_t c2x2 = f2(c2, c2);
+            uint64_t lacc[2] = {0, 0};
+            float racc[4] = {0.f, 0.f, 0.f, 0.f};
+            float rmax = kNegInf;
+  #pragma unroll 1
+            for (int i = 0; i < 4; ++i) {
+              uint32_t s[32];
+              tmem_ld32(tS + 32 * i, s);
+              tmem_ld_wait();
+              reg_fence(s);
+              if (L < 128 || C0 > 0) {
+  #pragma unroll
                 for (int c = 0; c < 32; ++c)
-                  if (32 * i + c >= L || 32 * i + c < C0) s[i][c] = 0xff800000u;  // -inf
-            }
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-#pragma unroll
-              for (int c = 0; c < 32; c += 4) {
-                mx0 = max3(mx0, __uint_as_float(s[i][c]), __uint_as_float(s[i][c + 1]));
-                mx1 = max3(mx1, __uint_as_float(s[i][c + 2]), __uint_as_float(s[i][c + 3]));
+                  if (32 * i + c >= L || 32 * i + c < C0) s[c] = 0xff800000u;  // -inf
               }
-          }
-          const float rmax = fmaxf(mx0, mx1);
-          mx = fmaxf(mx, rmax);
-          const float mnew = rmax * c2;
-          // The O rescale touches TMEM with warp-collective loads and stores, so
-          // the whole warp takes the branch when any of its rows needs it; rows
-          // that do not need it keep their reference max (alpha = 1).
-          const bool grow_ref = mnew > m_ref + kRescaleLog2;
-          if (__any_sync(0xffffffffu, grow_ref)) {
-            const float m_to = grow_ref ? mnew : m_ref;
-            const float alpha = grow_ref ? ex2(m_ref - mnew) : 1.f;
-            l *= alpha;
-            lr *= alpha;
-            if (j > 0) {
-#pragma unroll 1
-              for (int cc = 0; cc < D / 16; ++cc) {
-                uint32_t o[16];
-                tmem_ld16(tO + 16 * cc, o);
-                tmem_ld_wait();
-                reg_fence(o);
-#pragma unroll
-                for (int c = 0; c < 16; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
-                tmem_st16(tO + 16 * cc, o);
+              float cm;
+              {
+                float t[8];
+  #pragma unroll
+                for (int a = 0; a < 8; ++a)
+                  t[a] = max3(__uint_as_float(s[4 * a]), __uint_as_float(s[4 * a + 1]),
+                              fmaxf(__uint_as_float(s[4 * a + 2]), __uint_as_float(s[4 * a + 3])));
+                cm = max3(max3(t[0], t[1], t[2]), max3(t[3], t[4], t[5]), fmaxf(t[6], t[7]));
               }
+              rmax = fmaxf(rmax, cm);
+              const bool move = cm * c2 > m_ref + kRefSlackLog2;  // any finite cm when m_ref = -inf
+              if (__any_sync(0xffffffffu, move)) {
+                const float m_to = move ? cm * c2 : m_ref;
+                const float alpha = move ? ex2(m_ref - m_to) : 1.f;  // 0 from -inf
+                l *= alpha;
+                lr *= alpha;
+                if (j > 0) rescale_o<D>(tO, alpha);
+                float a0, a1, a2, a3;
+                f2_split(lacc[0], a0, a1);
+                f2_split(lacc[1], a2, a3);
+                lacc[0] = f2(a0 * alpha, a1 * alpha);
+                lacc[1] = f2(a2 * alpha, a3 * alpha);
+                const float4 rs = rescale_p(tS, i, alpha);
+                racc[0] = rs.x;
+                racc[1] = rs.y;
+                racc[2] = rs.z;
+                racc[3] = rs.w;
+                m_ref = m_to;
+              }
+              const float off = (m_ref == kNegInf) ? 0.f : m_ref;
+              const uint64_t noff = f2(-off, -off);
+              uint32_t pk[16];
+  #pragma unroll
+              for (int c = 0; c < 16; ++c) {
+                float x0, x1;
+                f2_split(fma2(f2(__uint_as_float(s[2 * c]), __uint_as_float(s[2 * c + 1])), c2x2, noff),
+                         x0, x1);
+                const float a = ex2(x0), b = ex2(x1);
+                lacc[c & 1] = add2(lacc[c & 1], f2(a, b));
+                const uint32_t w = pack_bf16x2(a, b);
+                add_bf16x2_halves(racc[2 * (c & 1)], racc[2 * (c & 1) + 1], w);
+                pk[c] = w;
+              }
+              tmem_st16(tS + 16 * i, pk);
             }
-            m_ref = m_to;
-          }
-          const float off = (m_ref == kNegInf) ? 0.f : m_ref;
-          // p = 2^(s*c2 - off) two at a time; l sums the fp32 p (returned), lr
-          // sums the bf16-rounded p that P.V actually uses (normalises O)
-          const uint64_t c2x2 = f2(c2, c2), noff = f2(-off, -off);
-          uint64_t lacc[2] = {0, 0};
-          float racc[4] = {0.f, 0.f, 0.f, 0.f};
-          // Pass 2: S chunk i (columns 32i..) -> P columns 16i.., already read.
-#pragma unroll 1
-          for (int i = 0; i < 4; ++i) {
-            uint32_t s[32];
-            tmem_ld32(tS + 32 * i, s);
-            tmem_ld_wait();
-            reg_fence(s);
-            if (L < 128 || C0 > 0) {
-#pragma unroll
-              for (int c = 0; c < 32; ++c)
-                if (32 * i + c >= L || 32 * i + c < C0) s[c] = 0xff800000u;  // -inf
+            mx = fmaxf(mx, rmax);
+            {
+              float a0, a1, a2, a3;
+              f2_split(lacc[0], a0, a1);
+              f2_split(lacc[1], a2, a3);
+              l += (a0 + a1) + (a2 + a3);
+              lr += (racc[0] + racc[1]) + (racc[2] + racc[3]);
             }
-            uint32_t pk[16];
-#pragma unroll
-            for (int c = 0; c < 16; ++c) {
-              float x0, x1;
-              f2_split(fma2(f2(__uint_as_float(s[2 * c]), __uint_as_float(s[2 * c + 1])), c2x2, noff),
-                       x0, x1);
-              const float a = ex2(x0), b = ex2(x1);
-              lacc[c & 1] = add2(lacc[c & 1], f2(a, b));
-              const uint32_t w = pack_bf16x2(a, b);
-              add_bf16x2_halves(racc[2 * (c & 1)], racc[2 * (c & 1) + 1], w);
-              pk[c] = w;
+          } else {
+            // Pass 1: row max. All 128 columns are read with a single wait (the
+            // load latency is paid once); pass 2 reads S again in 32-column
+            // chunks inside a compact loop: the hot code shares each scheduler's
+            // instruction cache with the MMA warp, and a small footprint measured
+            // faster than a fully unrolled single pass.
+            float mx0 = kNegInf, mx1 = kNegInf;
+            {
+              uint32_t s[4][32];
+  #pragma unroll
+              for (int i = 0; i < 4; ++i) tmem_ld32(tS + 32 * i, s[i]);
+              tmem_ld_wait();
+  #pragma unroll
+              for (int i = 0; i < 4; ++i) reg_fence(s[i]);
+              if (L < 128 || C0 > 0) {
+  #pragma unroll
+                for (int i = 0; i < 4; ++i)
+  #pragma unroll
+                  for (int c = 0; c < 32; ++c)
+                    if (32 * i + c >= L || 32 * i + c < C0) s[i][c] = 0xff800000u;  // -inf
+              }
+  #pragma unroll
+              for (int i = 0; i < 4; ++i)
+  #pragma unroll
+                for (int c = 0; c < 32; c += 4) {
+                  mx0 = max3(mx0, __uint_as_float(s[i][c]), __uint_as_float(s[i][c + 1]));
+                  mx1 = max3(mx1, __uint_as_float(s[i][c + 2]), __uint_as_float(s[i][c + 3]));
+                }
             }
-            tmem_st16(tS + 16 * i, pk);
-          }
-          {
-            float a0, a1, a2, a3;
-            f2_split(lacc[0], a0, a1);
-            f2_split(lacc[1], a2, a3);
-            l += (a0 + a1) + (a2 + a3);
-            lr += (racc[0] + racc[1]) + (racc[2] + racc[3]);
+            const float rmax = fmaxf(mx0, mx1);
+            mx = fmaxf(mx, rmax);
+            const float mnew = rmax * c2;
+            // The O rescale touches TMEM with warp-collective loads and stores, so
+            // the whole warp takes the branch when any of its rows needs it; rows
+            // that do not need it keep their reference max (alpha = 1).
+            const bool grow_ref = mnew > m_ref + kRescaleLog2;
+            if (__any_sync(0xffffffffu, grow_ref)) {
+              const float m_to = grow_ref ? mnew : m_ref;
+              const float alpha = grow_ref ? ex2(m_ref - mnew) : 1.f;
+              l *= alpha;
+              lr *= alpha;
+              if (j > 0) {
+  #pragma unroll 1
+                for (int cc = 0; cc < D / 16; ++cc) {
+                  uint32_t o[16];
+                  tmem_ld16(tO + 16 * cc, o);
+                  tmem_ld_wait();
+                  reg_fence(o);
+  #pragma unroll
+                  for (int c = 0; c < 16; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+                  tmem_st16(tO + 16 * cc, o);
+                }
+              }
+              m_ref = m_to;
+            }
+            const float off = (m_ref == kNegInf) ? 0.f : m_ref;
+            // p = 2^(s*c2 - off) two at a time; l sums the fp32 p (returned), lr
+            // sums the bf16-rounded p that P.V actually uses (normalises O)
+            const uint64_t c2x2 = f2(c2, c2), noff = f2(-off, -off);
+            uint64_t lacc[2] = {0, 0};
+            float racc[4] = {0.f, 0.f, 0.f, 0.f};
+            // Pass 2: S chunk i (columns 32i..) -> P columns 16i.., already read.
+  #pragma unroll 1
+            for (int i = 0; i < 4; ++i) {
+              uint32_t s[32];
+              tmem_ld32(tS + 32 * i, s);
+              tmem_ld_wait();
+              reg_fence(s);
+              if (L < 128 || C0 > 0) {
+  #pragma unroll
+                for (int c = 0; c < 32; ++c)
+                  if (32 * i + c >= L || 32 * i + c < C0) s[c] = 0xff800000u;  // -inf
+              }
+              uint32_t pk[16];
+  #pragma unroll
+              for (int c = 0; c < 16; ++c) {
+                float x0, x1;
+                f2_split(fma2(f2(__uint_as_float(s[2 * c]), __uint_as_float(s[2 * c + 1])), c2x2, noff),
+                         x0, x1);
+                const float a = ex2(x0), b = ex2(x1);
+                lacc[c & 1] = add2(lacc[c & 1], f2(a, b));
+                const uint32_t w = pack_bf16x2(a, b);
+                add_bf16x2_halves(racc[2 * (c & 1)], racc[2 * (c & 1) + 1], w);
+                pk[c] = w;
+              }
+              tmem_st16(tS + 16 * i, pk);
+            }
+            {
+              float a0, a1, a2, a3;
+              f2_split(lacc[0], a0, a1);
+              f2_split(lacc[1], a2, a3);
+              l += (a0 + a1) + (a2 + a3);
+              lr += (racc[0] + racc[1]) + (racc[2] + racc[3]);
+            }
           }
           tmem_st_wait();
           tc_fence_before();
@@ -930,10 +1057,10 @@ void tc_scratch_carve(void* base, int grid, int D, TcScratch* s) {
   s->flags = reinterpret_cast<unsigned*>(b);
 }
 
-template <int D>
+template <int D, bool kOnePass>
 static int launch_d(const TcPlan& plan, void* stream) {
-  cudaError_t e = cudaFuncSetAttribute(tc_ring_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       Cfg<D>::kSmemBytes);
+  cudaError_t e = cudaFuncSetAttribute(tc_ring_kernel<D, kOnePass>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::kSmemBytes);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(plan.grid);
@@ -946,17 +1073,20 @@ static int launch_d(const TcPlan& plan, void* stream) {
   attr[0].val.cooperative = plan.scratch.flags != nullptr ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, tc_ring_kernel<D>, plan);
+  e = cudaLaunchKernelEx(&cfg, tc_ring_kernel<D, kOnePass>, plan);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
 int launch_tc_bf16(const TcPlan& plan, int D, void* stream) {
   if (plan.grid <= 0) return cudaSuccess;
+  // packed documents: the one-pass softmax (short, masked units); otherwise
+  // the two-pass one
+  const bool one = plan.n_docs > 0;
   switch (D) {
-    case 128: return launch_d<128>(plan, stream);
-    case 96: return launch_d<96>(plan, stream);
-    default: return launch_d<64>(plan, stream);
+    case 128: return one ? launch_d<128, true>(plan, stream) : launch_d<128, false>(plan, stream);
+    case 96: return one ? launch_d<96, true>(plan, stream) : launch_d<96, false>(plan, stream);
+    default: return one ? launch_d<64, true>(plan, stream) : launch_d<64, false>(plan, stream);
   }
 }
 
