@@ -312,7 +312,9 @@ ra_status cuda_status(int err, const char* what) {
 // Stream-ordered allocations of the library come from one pool per device.
 // The pool keeps up to kPoolKeepBytes mapped across synchronisations (the
 // default pool would return everything at each synchronisation, and the next
-// call would wait while memory is mapped again).
+// call would wait while memory is mapped again). It never makes a stream wait
+// for another stream's free in order to reuse a block: calls on different
+// streams stay independent, and the pool maps more memory instead.
 constexpr uint64_t kPoolKeepBytes = uint64_t(4) << 30;
 
 ra_status lib_pool(cudaMemPool_t* out) {
@@ -335,7 +337,11 @@ ra_status lib_pool(cudaMemPool_t* out) {
     e = cudaMemPoolCreate(&pool, &props);
     if (e != cudaSuccess) return cuda_status(e, "creating the library memory pool");
     uint64_t keep = kPoolKeepBytes;
+    int no_cross_stream_wait = 0;
     e = cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep);
+    if (e == cudaSuccess)
+      e = cudaMemPoolSetAttribute(pool, cudaMemPoolReuseAllowInternalDependencies,
+                                  &no_cross_stream_wait);
     if (e != cudaSuccess) {
       cudaMemPoolDestroy(pool);
       return cuda_status(e, "configuring the library memory pool");
@@ -902,6 +908,57 @@ bool is_dense(const ra_strides& s, int64_t B, int64_t H, int64_t rows, int64_t D
          (B <= 1 || s.batch == H * rows * D);
 }
 
+// Start of the allocation that holds host pointer p (pinned memory the driver
+// knows), or 0 when the driver cannot tell.
+uintptr_t host_allocation_start(const void* p) {
+  static PFN_cuPointerGetAttribute_v4000 get_attr = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuPointerGetAttribute", &fn, 4000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_attr = reinterpret_cast<PFN_cuPointerGetAttribute_v4000>(fn);
+  });
+  CUdeviceptr start = 0;
+  if (!get_attr || !p ||
+      get_attr(&start, CU_POINTER_ATTRIBUTE_RANGE_START_ADDR, reinterpret_cast<CUdeviceptr>(p)) !=
+          CUDA_SUCCESS)
+    return 0;
+  return static_cast<uintptr_t>(start);
+}
+
+// One host<->device copy. A copy whose source and destination both continue
+// the previous one's is merged into it, but only inside one host allocation
+// (`host_alloc`, 0 if unknown: never merged); the device side is always one
+// pool allocation.
+struct Copy {
+  char* dst;
+  const char* src;
+  size_t n;
+  uintptr_t host_alloc;
+};
+
+void add_copy(std::vector<Copy>& v, void* dst, const void* src, size_t n, uintptr_t host_alloc) {
+  if (n == 0) return;
+  char* d = static_cast<char*>(dst);
+  const char* s = static_cast<const char*>(src);
+  if (!v.empty() && host_alloc != 0 && v.back().host_alloc == host_alloc &&
+      v.back().dst + v.back().n == d && v.back().src + v.back().n == s) {
+    v.back().n += n;
+    return;
+  }
+  v.push_back({d, s, n, host_alloc});
+}
+
+cudaError_t issue_copies(const std::vector<Copy>& v, cudaMemcpyKind kind, cudaStream_t s) {
+  cudaError_t e = cudaSuccess;
+  for (size_t i = 0; e == cudaSuccess && i < v.size(); ++i)
+    e = cudaMemcpyAsync(v[i].dst, v[i].src, v[i].n, kind, s);
+  return e;
+}
+
 ra_status run_host(const ra_problem* pb, const void* q, const ra_q_segment* segs, int32_t nsegs,
                    const ra_kv_chunk* chunks, int32_t nchunks, void* o, float* m, float* l,
                    void* stream) {
@@ -936,23 +993,39 @@ ra_status run_host(const ra_problem* pb, const void* q, const ra_q_segment* segs
   char* base = nullptr;
   cudaError_t e = cudaMallocFromPoolAsync(reinterpret_cast<void**>(&base), total, pool, cs);
   if (e != cudaSuccess) return cuda_status(e, "allocating device copies");
-  // carve: q, o, m, l, then k and v of every chunk
+  // carve: o, m, l, then q, the k of every chunk and the v of every chunk, in
+  // that order, so that inputs adjacent on the host are adjacent here too
   char* at = base;
   auto take = [&](size_t n) { char* r = at; at += up(n); return r; };
-  void* dq = take(q_bytes);
   void* dout = take(o_bytes);
   float* dm = reinterpret_cast<float*>(take(rows * 4));
   float* dl = reinterpret_cast<float*>(take(rows * 4));
+  void* dq = take(q_bytes);
   std::vector<ra_kv_chunk> dch(chunks, chunks + nchunks);
   std::vector<void*> dk(nchunks, nullptr), dv(nchunks, nullptr);
+  for (int32_t k = 0; k < nchunks; ++k)
+    if (chunks[k].len > 0) dk[k] = take(kv_bytes[k]);
+  for (int32_t k = 0; k < nchunks; ++k)
+    if (chunks[k].len > 0) dv[k] = take(kv_bytes[k]);
   for (int32_t k = 0; k < nchunks; ++k) {
-    if (chunks[k].len > 0) {
-      dk[k] = take(kv_bytes[k]);
-      dv[k] = take(kv_bytes[k]);
-    }
     dch[k].k = dk[k];
     dch[k].v = dv[k];
   }
+  // the copies, with runs that are adjacent both on the host and on the device
+  // merged into one (q, then the k and v of chunk-major buffers; o, m, l)
+  std::vector<Copy> in, out;
+  auto h2d = [&](void* dst, const void* src, size_t n) {
+    add_copy(in, dst, src, n, n ? host_allocation_start(src) : 0);
+  };
+  auto d2h = [&](void* dst, const void* src, size_t n) {
+    add_copy(out, dst, src, n, n ? host_allocation_start(dst) : 0);
+  };
+  h2d(dq, q, q_bytes);
+  for (int32_t k = 0; k < nchunks; ++k) h2d(dk[k], chunks[k].k, kv_bytes[k]);
+  for (int32_t k = 0; k < nchunks; ++k) h2d(dv[k], chunks[k].v, kv_bytes[k]);
+  d2h(o, dout, o_bytes);
+  d2h(m, dm, rows * 4);
+  d2h(l, dl, rows * 4);
   ra_problem dp = p;
   const ra_strides dense_q = {c.Hq * c.Sq * c.D, c.Sq * c.D, c.D};
   dp.q_strides = dense_q;
@@ -962,25 +1035,15 @@ ra_status run_host(const ra_problem* pb, const void* q, const ra_q_segment* segs
     dch[k].k_strides = ds;
     dch[k].v_strides = ds;
   }
-  // one copy per buffer, issued only once the plan has been accepted
+  // issued only once the plan has been accepted
   const BeforeLaunch copy_in = [&]() -> ra_status {
-    cudaError_t err = cudaMemcpyAsync(dq, q, q_bytes, cudaMemcpyHostToDevice, cs);
-    for (int32_t k = 0; err == cudaSuccess && k < nchunks; ++k) {
-      if (kv_bytes[k] == 0) continue;
-      err = cudaMemcpyAsync(dk[k], chunks[k].k, kv_bytes[k], cudaMemcpyHostToDevice, cs);
-      if (err == cudaSuccess)
-        err = cudaMemcpyAsync(dv[k], chunks[k].v, kv_bytes[k], cudaMemcpyHostToDevice, cs);
-    }
-    return cuda_status(err, "copying inputs to the device");
+    return cuda_status(issue_copies(in, cudaMemcpyHostToDevice, cs),
+                       "copying inputs to the device");
   };
   st = run(&dp, dq, segs, nsegs, dch.data(), nchunks, dout, dm, dl, false, stream,
            ScratchSource::kAllocate, copy_in);
-  if (st == RA_OK) {
-    e = cudaMemcpyAsync(o, dout, o_bytes, cudaMemcpyDeviceToHost, cs);
-    if (e == cudaSuccess) e = cudaMemcpyAsync(m, dm, rows * 4, cudaMemcpyDeviceToHost, cs);
-    if (e == cudaSuccess) e = cudaMemcpyAsync(l, dl, rows * 4, cudaMemcpyDeviceToHost, cs);
-    st = cuda_status(e, "copying outputs to the host");
-  }
+  if (st == RA_OK)
+    st = cuda_status(issue_copies(out, cudaMemcpyDeviceToHost, cs), "copying outputs to the host");
   cudaFreeAsync(base, cs);
   return st;
 }

@@ -89,3 +89,51 @@ def test_two_streams_overlap_without_interference():
                                     chunk_spans=rs, q_segments=segs, causal=True)
         torch.cuda.synchronize()
         assert torch.equal(O, Od.cpu()) and torch.equal(m, md.cpu()) and torch.equal(l, ld.cpu())
+
+
+def _one_pinned_block(tensors, copy=True):
+    sizes = [t.numel() * t.element_size() for t in tensors]
+    buf = torch.empty(sum(sizes), dtype=torch.uint8, pin_memory=True)
+    views, at = [], 0
+    for t, n in zip(tensors, sizes):
+        view = buf[at:at + n].view(t.dtype).view(t.shape)
+        if copy:
+            view.copy_(t)
+        views.append(view)
+        at += n
+    return views
+
+
+def test_host_buffers_in_one_block():
+    """Q, the K chunks and the V chunks back to back in one pinned buffer, and
+    O, m, l in another: the entry point merges copies of tensors adjacent on
+    the host and on the device (ragged chunks of head_dim 96 leave padding
+    between some device copies, and one chunk is empty), with results equal to
+    the device entry point's."""
+    S, D, Hq, Hkv = 1500, 96, 4, 2
+    g = torch.Generator(device="cpu").manual_seed(31)
+    q = torch.randn(1, Hq, S, D, generator=g).bfloat16()
+    k = torch.randn(1, Hkv, S, D, generator=g).bfloat16()
+    v = torch.randn(1, Hkv, S, D, generator=g).bfloat16()
+    lens = [256, 300, 0, 128, 1, 431, 384]
+    assert sum(lens) == S
+    kc = [t.contiguous() for t in torch.split(k, lens, dim=2)]
+    vc = [t.contiguous() for t in torch.split(v, lens, dim=2)]
+    hq, *hkv = _one_pinned_block([q, *kc, *vc])
+    O_like = torch.empty(1, Hq, S, D, dtype=torch.bfloat16)
+    ml_like = torch.empty(1, Hq, S, dtype=torch.float32)
+    ho, hm, hl = _one_pinned_block([O_like, ml_like, ml_like], copy=False)
+    stream = torch.cuda.Stream()
+    for causal in (False, True):
+        O, m, l = ring_attention_host(hq, hkv[:len(lens)], hkv[len(lens):], causal=causal,
+                                      out=ho, m=hm, l=hl, stream=stream)
+        stream.synchronize()
+        Od, md, ld = ring_attention(q.to(DEV), [t.to(DEV) for t in kc],
+                                    [t.to(DEV) for t in vc], causal=causal)
+        torch.cuda.synchronize()
+        assert torch.equal(O, Od.cpu()) and torch.equal(m, md.cpu()) and torch.equal(l, ld.cpu())
+        pos = np.arange(S)
+        Oref, mref, lref = oracle.full_attention(f64(q), f64(k).repeat(2, axis=1),
+                                                 f64(v).repeat(2, axis=1), pos, pos, causal,
+                                                 D ** -0.5)
+        assert_bf16(O, m, l, Oref, mref, lref, what=f"one-block host buffers causal={causal}")
