@@ -80,12 +80,19 @@ struct BwdCfg {
 };
 
 
-// Chunk tables: the plan's own arrays, or their device-resident copies.
-__device__ __forceinline__ const KvSeg& bspan(const BwdPlan& p, int k) {
-  return p.ext_ks ? p.ext_ks[k] : p.ks[k];
+// Chunk tables: the plan's own arrays, or their device-resident copies (read
+// in separate branches, see ld_kvseg).
+__device__ __forceinline__ KvSeg bspan(const BwdPlan& p, int k) {
+  if (p.ext_ks != nullptr) return ld_kvseg(p.ext_ks + k);
+  return p.ks[k];
 }
 __device__ __forceinline__ int btile_begin(const BwdPlan& p, int k) {
-  return p.ext_ktb ? p.ext_ktb[k] : p.kseg_tile_begin[k];
+  if (p.ext_ktb != nullptr) return __ldg(p.ext_ktb + k);
+  return p.kseg_tile_begin[k];
+}
+__device__ __forceinline__ QPiece bqpiece(const BwdPlan& p, int i) {
+  if (p.ext_qp != nullptr) return ld_qpiece(p.ext_qp + i);
+  return p.qp[i];
 }
 __device__ __forceinline__ const CUtensorMap* bkmap(const BwdPlan& p, int c) {
   return p.ext_kmap ? p.ext_kmap + c : &p.kmap[c];
@@ -118,13 +125,12 @@ __device__ __forceinline__ uint4 bias_split3(float x) {
 }
 
 __device__ __forceinline__ int bwd_row_position(const BwdPlan& p, int row) {
-  const QPiece* qp = p.ext_qp ? p.ext_qp : p.qp;
   int lo = 0, hi = p.n_qpieces - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if (qp[mid].row0 <= row) lo = mid; else hi = mid - 1;
+    if (bqpiece(p, mid).row0 <= row) lo = mid; else hi = mid - 1;
   }
-  const QPiece& q = qp[lo];
+  const QPiece q = bqpiece(p, lo);
   return q.pos0 + q.step * (row - q.row0);
 }
 
@@ -132,7 +138,7 @@ __device__ __forceinline__ int bwd_row_position(const BwdPlan& p, int row) {
 // [lo, hi] of some row of a query tile.
 __device__ __forceinline__ void bwd_live_tiles(const BwdPlan& p, int k, int lo, int hi, int& tb,
                                                int& te) {
-  const KvSeg& s = bspan(p, k);
+  const KvSeg s = bspan(p, k);
   if (!p.causal && p.n_docs == 0) {
     tb = 0;
     te = s.ntiles;
@@ -383,7 +389,7 @@ __device__ __forceinline__ void bwd_dkv_tile(const BwdPlan& p, int cta) {
       if (btile_begin(p, mid) <= gt) ks = mid; else hi = mid - 1;
     }
   }
-  const KvSeg& sg = bspan(p, ks);
+  const KvSeg sg = bspan(p, ks);
   const int kt = gt - btile_begin(p, ks);
   const int krow0 = sg.row0 + 128 * kt;                 // first row within the chunk
   const int kvalid = min(128, sg.len - 128 * kt);       // rows of the tile that exist
@@ -597,10 +603,20 @@ __device__ __forceinline__ void bwd_dkv_tile(const BwdPlan& p, int cta) {
         tc_fence_after();
       }
       if (ok) {
-        const int clen = p.ext_chunk_len ? p.ext_chunk_len[sg.chunk] : p.chunk_len[sg.chunk];
+        int clen;
+        float *dkr, *dvr;
+        if (p.ext_chunk_len != nullptr) {
+          clen = __ldg(p.ext_chunk_len + sg.chunk);
+          dkr = reinterpret_cast<float*>(__ldg(reinterpret_cast<const unsigned long long*>(p.ext_dk) + sg.chunk));
+          dvr = reinterpret_cast<float*>(__ldg(reinterpret_cast<const unsigned long long*>(p.ext_dv) + sg.chunk));
+        } else {
+          clen = p.chunk_len[sg.chunk];
+          dkr = p.dk[sg.chunk];
+          dvr = p.dv[sg.chunk];
+        }
         const int64_t row = (int64_t(b) * p.Hkv + hkv) * clen + krow0 + r;
-        float* dkr = (p.ext_dk ? p.ext_dk[sg.chunk] : p.dk[sg.chunk]) + row * D;
-        float* dvr = (p.ext_dv ? p.ext_dv[sg.chunk] : p.dv[sg.chunk]) + row * D;
+        dkr += row * D;
+        dvr += row * D;
         // D / 32 column chunks, the first half of them (rounded up) to half 0
         constexpr int kNc = D / 32, kPer = (kNc + 1) / 2;
 #pragma unroll 1
@@ -740,7 +756,7 @@ __device__ __forceinline__ void bwd_dq_tile(const BwdPlan& p, int cta) {
     int jk = 0, jv = 0, fenced = -1;  // tiles whose K, V copies were issued
     bool ok = true;
     for (int k = 0; ok && k < p.n_kvsegs; ++k) {
-      const KvSeg& sg = bspan(p, k);
+      const KvSeg sg = bspan(p, k);
       int tb, te;
       bwd_live_tiles(p, k, wlo, whi, tb, te);
       for (int t = tb; ok && t < te; ++t) {
@@ -908,7 +924,7 @@ __device__ __forceinline__ void bwd_dq_tile(const BwdPlan& p, int cta) {
     int j = 0;
     bool ok = true;
     for (int k = 0; ok && k < p.n_kvsegs; ++k) {
-      const KvSeg& sg = bspan(p, k);
+      const KvSeg sg = bspan(p, k);
       int tb, te;
       bwd_live_tiles(p, k, wlo, whi, tb, te);
       for (int t = tb; t < te; ++t, ++j) {

@@ -27,6 +27,33 @@ constexpr int kMaxQPieces = 64;
 constexpr int kMaxDocs = 512;
 
 #if defined(__CUDACC__)
+// Loads of span records from device-resident tables (read-only path). The
+// kernels read a plan's own tables directly and a device-resident copy only
+// through these, in separate branches: one access that might point to either
+// would become a generic load, which costs a memory round trip even for the
+// plan's own arrays.
+__device__ __forceinline__ QPiece ld_qpiece(const QPiece* q) {
+  QPiece r;
+  r.row0 = __ldg(&q->row0);
+  r.len = __ldg(&q->len);
+  r.pos0 = __ldg(&q->pos0);
+  r.step = __ldg(&q->step);
+  r.seg = __ldg(&q->seg);
+  return r;
+}
+__device__ __forceinline__ KvSeg ld_kvseg(const KvSeg* k) {
+  KvSeg r;
+  r.chunk = __ldg(&k->chunk);
+  r.row0 = __ldg(&k->row0);
+  r.len = __ldg(&k->len);
+  r.pos0 = __ldg(&k->pos0);
+  r.step = __ldg(&k->step);
+  r.ntiles = __ldg(&k->ntiles);
+  return r;
+}
+#endif
+
+#if defined(__CUDACC__)
 #define RA_HD __host__ __device__ __forceinline__
 #else
 #define RA_HD inline

@@ -113,9 +113,13 @@ struct Unit {
   int lo, hi;  // key positions any row of the unit may see: [lo, hi]
 };
 
-// Query spans: the plan's own array, or its device-resident copy.
-__device__ __forceinline__ const QPiece& qpiece(const TcPlan& p, int i) {
-  return p.ext_qp ? p.ext_qp[i] : p.qp[i];
+// Plan tables live in the plan itself (the common case) or, for problems with
+// more chunks or spans than it holds, in device memory; the two are read in
+// separate branches (ld_qpiece / ld_kvseg for the device copies).
+// Query spans.
+__device__ __forceinline__ QPiece qpiece(const TcPlan& p, int i) {
+  if (p.ext_qp != nullptr) return ld_qpiece(p.ext_qp + i);
+  return p.qp[i];
 }
 
 __device__ __forceinline__ int find_piece(const TcPlan& p, int row) {
@@ -128,17 +132,18 @@ __device__ __forceinline__ int find_piece(const TcPlan& p, int row) {
 }
 
 __device__ __forceinline__ int row_position(const TcPlan& p, int row) {
-  const QPiece& q = qpiece(p, find_piece(p, row));
+  const QPiece q = qpiece(p, find_piece(p, row));
   return q.pos0 + q.step * (row - q.row0);
 }
 
-// Chunk tables: the plan's own arrays, or their device-resident copies when
-// the problem has more chunks or spans than the plan holds.
-__device__ __forceinline__ const KvSeg& span_of(const TcPlan& p, int k) {
-  return p.ext_ks ? p.ext_ks[k] : p.ks[k];
+// Chunk tables: key spans, the first span of every chunk, tensor maps.
+__device__ __forceinline__ KvSeg span_of(const TcPlan& p, int k) {
+  if (p.ext_ks != nullptr) return ld_kvseg(p.ext_ks + k);
+  return p.ks[k];
 }
 __device__ __forceinline__ int seg_begin(const TcPlan& p, int c) {
-  return p.ext_csb ? p.ext_csb[c] : p.chunk_seg_begin[c];
+  if (p.ext_csb != nullptr) return __ldg(p.ext_csb + c);
+  return p.chunk_seg_begin[c];
 }
 __device__ __forceinline__ const CUtensorMap* kmap_of(const TcPlan& p, int c) {
   return p.ext_kmap ? p.ext_kmap + c : &p.kmap[c];
@@ -150,7 +155,7 @@ __device__ __forceinline__ const CUtensorMap* vmap_of(const TcPlan& p, int c) {
 // Key tiles [tb, te) of span k that hold a position some row of the unit
 // may see (not entirely in its future, nor outside its documents).
 __device__ __forceinline__ void live_tiles(const TcPlan& p, int k, const Unit& U, int& tb, int& te) {
-  const KvSeg& s = span_of(p, k);
+  const KvSeg s = span_of(p, k);
   if (!p.causal && p.n_docs == 0) {
     tb = 0;
     te = s.ntiles;
@@ -172,7 +177,7 @@ __device__ __forceinline__ void decode_unit(const TcPlan& p, int u, Unit& U) {
   U.qseg = qpiece(p, i).seg;
   int qmin = 0x7fffffff, qmax = -1;
   for (; i < p.n_qpieces && qpiece(p, i).row0 < r1; ++i) {
-    const QPiece& q = qpiece(p, i);
+    const QPiece q = qpiece(p, i);
     const int a = max(U.qrow0, q.row0), e = min(r1, q.row0 + q.len);
     qmin = min(qmin, q.pos0 + q.step * (a - q.row0));
     qmax = max(qmax, q.pos0 + q.step * (e - 1 - q.row0));
@@ -456,7 +461,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ring_kernel(const __grid_const
         iter.seek(p, U, I.t0);
         int ks, t;
         for (int j = 0; ok && j < n && iter.next(p, U, ks, t); ++j) {
-          const KvSeg& sg = span_of(p, ks);
+          const KvSeg sg = span_of(p, ks);
           const int row = sg.row0 + 128 * t;
           if (p.ext_kmap != nullptr && sg.chunk != fenced) {  // maps copied in from the host
             fence_tmap_acquire(kmap_of(p, sg.chunk));
@@ -651,7 +656,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ring_kernel(const __grid_const
           // before S arrives; C0 > 0 only where a document starts inside it)
           int L, C0 = 0;
           {
-            const KvSeg& sg = span_of(p, ks);
+            const KvSeg sg = span_of(p, ks);
             L = min(128, sg.len - 128 * t);
             if (p.causal || p.n_docs) {
               const int first = sg.pos0 + sg.step * (128 * t);
