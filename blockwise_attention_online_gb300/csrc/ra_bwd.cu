@@ -77,7 +77,25 @@ struct BwdCfg {
   static constexpr int kSmemBytes = kBar + kBarBytes + 1024;  // + alignment slack
   static_assert(kSmemBytes <= 232448, "shared memory per CTA");
   static_assert(kAux0 % 1024 == 0 && kAuxBytes % 1024 == 0, "bias tiles stay aligned");
+  // epilogue: dK and dV as padded row-major fp32 tiles over the K/V and stage
+  // buffers (free once every product is complete)
+  static constexpr int kEpiPitch = D + 4;  // floats per staged row
+  static constexpr int kEpiK = 0, kEpiV = 128 * kEpiPitch * 4;
+  static_assert(kEpiV + 128 * kEpiPitch * 4 <= kAux0, "epilogue tiles fit the free buffers");
 };
+
+// Stores rows [0, nrows) of a staged fp32 tile (row pitch D + 4 floats) to
+// consecutive rows of `dst` (D floats each): the 256 elementwise threads,
+// warp e taking rows e, e + 8, ..., each lane 16 bytes of the row, so every
+// store instruction writes whole rows.
+template <int D>
+__device__ __forceinline__ void store_staged_rows(const float* stage, float* dst, int nrows, int e,
+                                                  int lane) {
+  if (lane >= D / 4) return;
+  for (int rr = e; rr < nrows; rr += 8)
+    reinterpret_cast<float4*>(dst + int64_t(rr) * D)[lane] =
+        reinterpret_cast<const float4*>(stage + rr * (D + 4))[lane];
+}
 
 
 // Chunk tables: the plan's own arrays, or their device-resident copies (read
@@ -595,56 +613,60 @@ __device__ __forceinline__ void bwd_dkv_tile(const BwdPlan& p, int cta) {
       mbar_arrive(bb.ew_done);
       ++j;
     }
+    // ---- epilogue: dK (times scale) and dV rows of this key tile. Each
+    // thread puts its row into padded row-major tiles in shared memory, then
+    // every warp stores whole rows. All eight warps reach the barrier, also
+    // after an abort (the abort flag then keeps the tiles from being stored).
+    const bool any = j > 0;
+    if (ok && any) {
+      ok = warp_wait(bb.acc_full, 0, bb.abort_flag, budget, kSiteBwdAcc);
+      tc_fence_after();
+    }
+    float* const stK = reinterpret_cast<float*>(gbase + C::kEpiK);
+    float* const stV = reinterpret_cast<float*>(gbase + C::kEpiV);
     if (ok) {
-      // ---- epilogue: dK (times scale) and dV rows of this key tile
-      const bool any = j > 0;
-      if (any) {
-        ok = warp_wait(bb.acc_full, 0, bb.abort_flag, budget, kSiteBwdAcc);
-        tc_fence_after();
-      }
-      if (ok) {
-        int clen;
-        float *dkr, *dvr;
-        if (p.ext_chunk_len != nullptr) {
-          clen = __ldg(p.ext_chunk_len + sg.chunk);
-          dkr = reinterpret_cast<float*>(__ldg(reinterpret_cast<const unsigned long long*>(p.ext_dk) + sg.chunk));
-          dvr = reinterpret_cast<float*>(__ldg(reinterpret_cast<const unsigned long long*>(p.ext_dv) + sg.chunk));
-        } else {
-          clen = p.chunk_len[sg.chunk];
-          dkr = p.dk[sg.chunk];
-          dvr = p.dv[sg.chunk];
-        }
-        const int64_t row = (int64_t(b) * p.Hkv + hkv) * clen + krow0 + r;
-        dkr += row * D;
-        dvr += row * D;
-        // D / 32 column chunks, the first half of them (rounded up) to half 0
-        constexpr int kNc = D / 32, kPer = (kNc + 1) / 2;
+      // D / 32 column chunks, the first half of them (rounded up) to half 0
+      constexpr int kNc = D / 32, kPer = (kNc + 1) / 2;
 #pragma unroll 1
-        for (int cc = hw * kPer; cc < min(kNc, (hw + 1) * kPer); ++cc) {
-          uint32_t a[32], v[32];
-          if (any) {
-            tmem_ld32(tdK + 32 * cc, a);
-            tmem_ld32(tdV + 32 * cc, v);
-            tmem_ld_wait();
-            reg_fence(a);
-            reg_fence(v);
-          } else {
+      for (int cc = hw * kPer; cc < min(kNc, (hw + 1) * kPer); ++cc) {
+        uint32_t a[32], v[32];
+        if (any) {
+          tmem_ld32(tdK + 32 * cc, a);
+          tmem_ld32(tdV + 32 * cc, v);
+          tmem_ld_wait();
+          reg_fence(a);
+          reg_fence(v);
+        } else {
 #pragma unroll
-            for (int c = 0; c < 32; ++c) a[c] = v[c] = 0u;
-          }
-          if (krow_ok) {
+          for (int c = 0; c < 32; ++c) a[c] = v[c] = 0u;
+        }
+        float4* const rk = reinterpret_cast<float4*>(stK + r * C::kEpiPitch + 32 * cc);
+        float4* const rv = reinterpret_cast<float4*>(stV + r * C::kEpiPitch + 32 * cc);
 #pragma unroll
-            for (int c = 0; c < 32; c += 4) {
-              reinterpret_cast<float4*>(dkr + 32 * cc)[c / 4] =
-                  make_float4(__uint_as_float(a[c]) * p.scale, __uint_as_float(a[c + 1]) * p.scale,
-                              __uint_as_float(a[c + 2]) * p.scale, __uint_as_float(a[c + 3]) * p.scale);
-              reinterpret_cast<float4*>(dvr + 32 * cc)[c / 4] =
-                  make_float4(__uint_as_float(v[c]), __uint_as_float(v[c + 1]),
-                              __uint_as_float(v[c + 2]), __uint_as_float(v[c + 3]));
-            }
-          }
+        for (int c = 0; c < 32; c += 4) {
+          rk[c / 4] = make_float4(__uint_as_float(a[c]) * p.scale, __uint_as_float(a[c + 1]) * p.scale,
+                                  __uint_as_float(a[c + 2]) * p.scale, __uint_as_float(a[c + 3]) * p.scale);
+          rv[c / 4] = make_float4(__uint_as_float(v[c]), __uint_as_float(v[c + 1]),
+                                  __uint_as_float(v[c + 2]), __uint_as_float(v[c + 3]));
         }
       }
+    }
+    named_bar_sync(1, 256);
+    if (*bb.abort_flag == 0) {
+      int clen;
+      float *dkr, *dvr;
+      if (p.ext_chunk_len != nullptr) {
+        clen = __ldg(p.ext_chunk_len + sg.chunk);
+        dkr = reinterpret_cast<float*>(__ldg(reinterpret_cast<const unsigned long long*>(p.ext_dk) + sg.chunk));
+        dvr = reinterpret_cast<float*>(__ldg(reinterpret_cast<const unsigned long long*>(p.ext_dv) + sg.chunk));
+      } else {
+        clen = p.chunk_len[sg.chunk];
+        dkr = p.dk[sg.chunk];
+        dvr = p.dv[sg.chunk];
+      }
+      const int64_t row0 = (int64_t(b) * p.Hkv + hkv) * clen + krow0;
+      store_staged_rows<D>(stK, dkr + row0 * D, kvalid, warp - 4, lane);
+      store_staged_rows<D>(stV, dvr + row0 * D, kvalid, warp - 4, lane);
     }
   }
   bwd_teardown(tmem);
@@ -667,6 +689,9 @@ struct DqCfg {
   static constexpr int kBar = kV0 + kVSlots * kTileBytes;
   static constexpr int kSmemBytes = kBar + 256 + 1024;  // + alignment slack
   static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+  // epilogue: dQ as a padded row-major fp32 tile over the dO and K buffers
+  static constexpr int kEpiPitch = D + 4;
+  static_assert(128 * kEpiPitch * 4 <= kBar, "epilogue tile fits the free buffers");
 };
 
 // One dQ CTA per (batch, query head, 128-row query tile): for every live key
@@ -990,38 +1015,41 @@ __device__ __forceinline__ void bwd_dq_tile(const BwdPlan& p, int cta) {
         mbar_arrive(b_dsfull);
       }
     }
+    // ---- epilogue: dQ rows times scale, through a padded row-major tile in
+    // shared memory (free once every product is complete), then whole-row
+    // stores; all eight warps reach the barrier, also after an abort
+    const bool any = j > 0;
+    if (ok && any) {
+      ok = warp_wait(b_acc, 0, abort_flag, budget, kSiteBwdAcc);
+      tc_fence_after();
+    }
+    float* const stQ = reinterpret_cast<float*>(gbase);
     if (ok) {
-      // ---- epilogue: dQ row times scale
-      const bool any = j > 0;
-      if (any) {
-        ok = warp_wait(b_acc, 0, abort_flag, budget, kSiteBwdAcc);
-        tc_fence_after();
-      }
-      if (ok) {
-        // the TMEM loads are warp-collective: every lane takes part, rows
-        // past Sq just do not store
-        float* dqr = p.dq + srow * D;
-        constexpr int kNc = D / 32, kPer = (kNc + 1) / 2;
+      // the TMEM loads are warp-collective: every lane takes part
+      constexpr int kNc = D / 32, kPer = (kNc + 1) / 2;
 #pragma unroll 1
-        for (int cc = hw * kPer; cc < min(kNc, (hw + 1) * kPer); ++cc) {
-          uint32_t a[32];
-          if (any) {
-            tmem_ld32(tdQ + 32 * cc, a);
-            tmem_ld_wait();
-            reg_fence(a);
-          } else {
+      for (int cc = hw * kPer; cc < min(kNc, (hw + 1) * kPer); ++cc) {
+        uint32_t a[32];
+        if (any) {
+          tmem_ld32(tdQ + 32 * cc, a);
+          tmem_ld_wait();
+          reg_fence(a);
+        } else {
 #pragma unroll
-            for (int c = 0; c < 32; ++c) a[c] = 0u;
-          }
-          if (rvalid) {
-#pragma unroll
-            for (int c = 0; c < 32; c += 4)
-              reinterpret_cast<float4*>(dqr + 32 * cc)[c / 4] =
-                  make_float4(__uint_as_float(a[c]) * p.scale, __uint_as_float(a[c + 1]) * p.scale,
-                              __uint_as_float(a[c + 2]) * p.scale, __uint_as_float(a[c + 3]) * p.scale);
-          }
+          for (int c = 0; c < 32; ++c) a[c] = 0u;
         }
+        float4* const rq = reinterpret_cast<float4*>(stQ + r * C::kEpiPitch + 32 * cc);
+#pragma unroll
+        for (int c = 0; c < 32; c += 4)
+          rq[c / 4] = make_float4(__uint_as_float(a[c]) * p.scale, __uint_as_float(a[c + 1]) * p.scale,
+                                  __uint_as_float(a[c + 2]) * p.scale, __uint_as_float(a[c + 3]) * p.scale);
       }
+    }
+    named_bar_sync(1, 256);
+    if (*abort_flag == 0) {
+      const int nrows = min(128, p.Sq - 128 * qt);
+      store_staged_rows<D>(stQ, p.dq + ((int64_t(b) * p.Hq + hq) * p.Sq + 128 * qt) * D, nrows,
+                           warp - 4, lane);
     }
   }
   bwd_teardown(tmem);
