@@ -190,42 +190,59 @@ __global__ void __launch_bounds__(128) bwd_prep_kernel(const __grid_constant__ B
   const int n = threadIdx.x;
   const int row = 128 * qt + n;
   const bool valid = row < p.Sq;
+  // delta of the tile's rows: eight lanes per row (each load instruction of a
+  // warp covers four consecutive rows), partial sums added by shuffles
+  __shared__ float sdl[128];
+  {
+    const int warp = n >> 5, lane = n & 31, grp = lane >> 3, l8 = lane & 7;
+    constexpr int kU2 = D / 32;  // 4-element pieces per lane
+#pragma unroll 1
+    for (int it = 0; it < 8; ++it) {
+      const int rl = warp * 32 + 4 * it + grp;
+      const int rr = 128 * qt + rl;
+      float acc = 0.f;
+      if (rr < p.Sq) {
+        const int64_t off = int64_t(b) * o_sb + int64_t(h) * o_sh + int64_t(rr) * o_sr;
+        const uint2* g2 = reinterpret_cast<const uint2*>(dout + off) + l8 * kU2;
+#pragma unroll
+        for (int e = 0; e < kU2; ++e) {
+          const uint2 gv = g2[e];
+          const float g0 = __uint_as_float(gv.x << 16), g1 = __uint_as_float(gv.x & 0xffff0000u);
+          const float g2v = __uint_as_float(gv.y << 16), g3 = __uint_as_float(gv.y & 0xffff0000u);
+          if (o_fp32) {
+            const float4 ov = reinterpret_cast<const float4*>(static_cast<const float*>(o) + off)[l8 * kU2 + e];
+            acc = fmaf(g0, ov.x, fmaf(g1, ov.y, fmaf(g2v, ov.z, fmaf(g3, ov.w, acc))));
+          } else {
+            const uint2 ov = reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(o) + off)[l8 * kU2 + e];
+            acc = fmaf(g0, __uint_as_float(ov.x << 16),
+                       fmaf(g1, __uint_as_float(ov.x & 0xffff0000u),
+                            fmaf(g2v, __uint_as_float(ov.y << 16),
+                                 fmaf(g3, __uint_as_float(ov.y & 0xffff0000u), acc))));
+          }
+        }
+      }
+      acc += __shfl_xor_sync(0xffffffffu, acc, 4);
+      acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+      acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+      if (l8 == 0) sdl[rl] = acc;
+    }
+  }
+  __syncthreads();
   float dl = 0.f, l2 = kInf;
   int lo = 0x7fffffff, hi = int(0x80000000);  // an empty window
   if (valid) {
-    const int64_t off = int64_t(b) * o_sb + int64_t(h) * o_sh + int64_t(row) * o_sr;
-    const uint4* g = reinterpret_cast<const uint4*>(dout + off);
-    float acc0 = 0.f, acc1 = 0.f;
-#pragma unroll 4
-    for (int k = 0; k < D / 8; ++k) {
-      const uint4 gv = g[k];
-      const uint32_t w[4] = {gv.x, gv.y, gv.z, gv.w};
-      if (o_fp32) {
-        const float4* o4 = reinterpret_cast<const float4*>(static_cast<const float*>(o) + off) + 2 * k;
-        const float4 a = o4[0], c = o4[1];
-        const float ov[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          acc0 = fmaf(__uint_as_float(w[e] << 16), ov[2 * e], acc0);
-          acc1 = fmaf(__uint_as_float(w[e] & 0xffff0000u), ov[2 * e + 1], acc1);
-        }
-      } else {
-        const uint4 ovv = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(o) + off)[k];
-        const uint32_t v[4] = {ovv.x, ovv.y, ovv.z, ovv.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          acc0 = fmaf(__uint_as_float(w[e] << 16), __uint_as_float(v[e] << 16), acc0);
-          acc1 = fmaf(__uint_as_float(w[e] & 0xffff0000u), __uint_as_float(v[e] & 0xffff0000u), acc1);
-        }
-      }
-    }
-    dl = acc0 + acc1;
+    dl = sdl[n];
     const int64_t srow = int64_t(bh) * p.Sq + row;
     const float lr = l[srow];
     l2 = lr > 0.f ? fmaf(m[srow], kLog2e, log2f(lr)) : kInf;
     delta[srow] = dl;
     lse2[srow] = l2;
-    key_window(p, bwd_row_position(p, row), lo, hi);
+    if (p.causal || p.n_docs > 0) {
+      key_window(p, bwd_row_position(p, row), lo, hi);
+    } else {
+      lo = 0;
+      hi = 0x7fffffff;
+    }
   }
   uint8_t* tile = colaux + (int64_t(bh) * p.n_qtiles + qt) * int64_t(kColAuxBytes);
   const uint32_t boff = bias_row_offset(n);

@@ -64,6 +64,8 @@ def _oracle_forward(q, k, v, qpos, kpos, causal, scale, docs=None):
     (2, 2, 1, 640, 64, "striped", 4, True),
     (1, 4, 2, 640, 96, "zigzag", 2, True),
     (1, 8, 2, 1024, 128, "contiguous", 8, True),
+    # more tile CTAs (96 key tiles, 96 query tiles) than SMs: several waves
+    (1, 4, 4, 3072, 64, "zigzag", 4, True),
 ])
 def test_gradients_within_rounding_bound(B, Hq, Hkv, S, D, kind, P, causal):
     q, k, v, do = _inputs(41, B, Hq, Hkv, S, D)
