@@ -120,8 +120,9 @@ class _Nvml:
 
 class ClockSampler:
     """SM clock and clock-event reasons sampled while a timed region runs:
-    NVML read every millisecond from a helper thread (so that a region of a few
-    milliseconds still gets samples), else nvidia-smi every 10 ms."""
+    NVML read every quarter millisecond from a helper thread (so that a region
+    of a few milliseconds still gets a dozen samples), else nvidia-smi every
+    10 ms."""
 
     def __init__(self, index):
         self.index = index
@@ -135,14 +136,14 @@ class ClockSampler:
         self.proc = None
         try:
             self.nv = _Nvml(self.index)
-            self.source = "nvml, 1 ms"
+            self.source = "nvml, 0.25 ms"
 
             def loop():
                 while not self._stop.is_set():
                     s = self.nv.sample()
                     if s is not None:
                         self.samples.append(s)
-                    time.sleep(0.001)
+                    time.sleep(0.00025)
 
             self.thread = threading.Thread(target=loop, daemon=True)
             self.thread.start()
@@ -280,22 +281,14 @@ def run_gpu(args):
     torch.cuda.synchronize()
     device_status()
 
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
-    with ClockSampler(dev.index) as clk:
-        for i in range(args.steps):
-            flush.fill_(float(i & 7))       # evict the previous step's data from L2
-            starts[i].record(stream)
-            step()
-            ends[i].record(stream)
-        torch.cuda.synchronize()
+    # K steps, each after an L2 flush, timed with CUDA events on the stream
+    times, clocks = _timed(step, args.steps, 0, flush, stream, dev.index)  # ms per launch
     if world > 1:
         dist.barrier()
     device_status()
-    times = [s.elapsed_time(e) for s, e in zip(starts, ends)]  # ms per launch
     total_ms = sum(times)
     max_ms = max_over_ranks(total_ms, dev)
     value = whole_job_tflops(flops, args.steps, world, max_ms)
@@ -314,16 +307,17 @@ def run_gpu(args):
         # buffer's adjacent tensors with one copy
         hq, *hkv = _pinned_block([qs, *kc, *vc])
         hk, hv = hkv[:len(kc)], hkv[len(kc):]
-        outs = [tuple(_pinned_block([out, m, l], copy=False)) for _ in range(E2E_STREAMS)]
+        ns = args.e2e_streams
+        outs = [tuple(_pinned_block([out, m, l], copy=False)) for _ in range(ns)]
         h2d = hq.numel() * hq.element_size() + sum(x.numel() * x.element_size() for x in hk + hv)
         d2h = sum(t.numel() * t.element_size() for t in outs[0])
         n_e2e = max(3, min(args.steps, 100))
-        streams = [torch.cuda.Stream(device=dev) for _ in range(E2E_STREAMS)]
+        streams = [torch.cuda.Stream(device=dev) for _ in range(ns)]
 
         def e2e_step(i):
-            ho, hm, hl = outs[i % E2E_STREAMS]
+            ho, hm, hl = outs[i % ns]
             ring_attention_host(hq, hk, hv, chunk_spans=rs, q_segments=segs, causal=w.causal,
-                                out=ho, m=hm, l=hl, docs=docs, stream=streams[i % E2E_STREAMS])
+                                out=ho, m=hm, l=hl, docs=docs, stream=streams[i % ns])
 
         for i in range(4):
             e2e_step(i)
@@ -338,7 +332,7 @@ def run_gpu(args):
         e2e = {"value": round(whole_job_tflops(flops, n_e2e, world, el * 1e3), 3),
                "unit": "TFLOP/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-               "steps": n_e2e, "streams": E2E_STREAMS,
+               "steps": n_e2e, "streams": ns,
                "call": "ra_ring_attention_host (pinned host buffers)"}
         device_status()
 
@@ -372,6 +366,9 @@ def run_gpu(args):
                              "recipe": "workloads.packed_documents(S, seed, mean_len)"}
                             if docs else None),
                    "l2": f"flushed before every step ({L2_FLUSH_BYTES >> 20} MiB write)",
+                   "timing": "CUDA events around each step on the launching stream; untimed "
+                             "device work queued before the first step, so that its host "
+                             "planning does not leave the device idle inside its events",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "pct_of_peak": round(100 * value / world / peak_b, 2),
         "roofline": {"bound": "tensor", "achieved": round(achieved, 3), "peak": peak_b,
@@ -379,7 +376,7 @@ def run_gpu(args):
                      "traffic": _traffic(kernel_key), "kernel": "tc_ring_kernel<128>",
                      "peak_source": f"{src} bf16 burst (MEASURED_PEAKS.json)" if src == "measured"
                      else "fallback 1.9 PFLOP/s"},
-        "clocks": clk.summary(),
+        "clocks": clocks,
         "gpu_launches": args.steps,
         "e2e": e2e,
     }
@@ -628,7 +625,7 @@ def run_gpu_bwd(args):
                      "unit": "TFLOP/s", "frac": round(achieved / peak_b, 4), "traffic": None,
                      "kernel": "bwd_kernel<128> (dK/dV and dQ CTAs, one step)",
                      "peak_source": f"{src} bf16 burst (MEASURED_PEAKS.json)"},
-        "clocks": clk.summary(),
+        "clocks": clocks,
         "gpu_launches": 3 * args.steps,
         "e2e": None,
     }
@@ -756,6 +753,8 @@ def main():
     ap.add_argument("--layout", default=None)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--e2e-streams", type=int, default=E2E_STREAMS,
+                    help="streams the end-to-end steps rotate over")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-secondary", action="store_true",
                     help="skip the further records (other workloads, backward, merge kernels)")
