@@ -585,22 +585,14 @@ def run_gpu_bwd(args):
         step()
     torch.cuda.synchronize()
     device_status()
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
-    with ClockSampler(dev.index) as clk:
-        for i in range(args.steps):
-            flush.fill_(float(i & 7))
-            starts[i].record(stream)
-            step()
-            ends[i].record(stream)
-        torch.cuda.synchronize()
+    times, clocks = _timed(step, args.steps, 0, flush, stream, dev.index)
     if world > 1:
         dist.barrier()
     device_status()
-    total_ms = sum(s_.elapsed_time(e_) for s_, e_ in zip(starts, ends))
+    total_ms = sum(times)
     max_ms = max_over_ranks(total_ms, dev)
     value = whole_job_tflops(flops, args.steps, world, max_ms)
     if world > 1:
