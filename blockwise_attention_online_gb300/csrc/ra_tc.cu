@@ -691,22 +691,27 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ring_kernel(const __grid_const
   #pragma unroll 1
             for (int i = 0; i < 4; ++i) {
               uint32_t s[32];
-              tmem_ld32(tS + 32 * i, s);
-              tmem_ld_wait();
-              reg_fence(s);
-              if (L < 128 || C0 > 0) {
+              float cm;
+              if (__any_sync(0xffffffffu, L < 32 * i + 32 || C0 > 32 * i)) {
+                // some row of this warp has masked columns in the chunk
+                tmem_ld32(tS + 32 * i, s);
+                tmem_ld_wait();
+                reg_fence(s);
   #pragma unroll
                 for (int c = 0; c < 32; ++c)
                   if (32 * i + c >= L || 32 * i + c < C0) s[c] = 0xff800000u;  // -inf
-              }
-              float cm;
-              {
                 float t[8];
   #pragma unroll
                 for (int a = 0; a < 8; ++a)
                   t[a] = max3(__uint_as_float(s[4 * a]), __uint_as_float(s[4 * a + 1]),
                               fmaxf(__uint_as_float(s[4 * a + 2]), __uint_as_float(s[4 * a + 3])));
                 cm = max3(max3(t[0], t[1], t[2]), max3(t[3], t[4], t[5]), fmaxf(t[6], t[7]));
+              } else {
+                // nothing masked: the load reduces the chunk to its max on the way
+                tmem_ld32_max(tS + 32 * i, s, cm);
+                tmem_ld_wait();
+                reg_fence(s);
+                asm volatile("" : "+f"(cm));
               }
               rmax = fmaxf(rmax, cm);
               const bool move = cm * c2 > m_ref + kRefSlackLog2;  // any finite cm when m_ref = -inf
@@ -759,7 +764,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ring_kernel(const __grid_const
             // instruction cache with the MMA warp, and a small footprint measured
             // faster than a fully unrolled single pass.
             float mx0 = kNegInf, mx1 = kNegInf;
-            {
+            if (__any_sync(0xffffffffu, L < 128 || C0 > 0)) {
+              // some row of this warp has masked columns: mask, then reduce
               uint32_t s[4][32];
   #pragma unroll
               for (int i = 0; i < 4; ++i) tmem_ld32(tS + 32 * i, s[i]);
@@ -780,6 +786,19 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ring_kernel(const __grid_const
                   mx0 = max3(mx0, __uint_as_float(s[i][c]), __uint_as_float(s[i][c + 1]));
                   mx1 = max3(mx1, __uint_as_float(s[i][c + 2]), __uint_as_float(s[i][c + 3]));
                 }
+            } else {
+              // nothing masked: the tensor-memory loads reduce each 32-column
+              // chunk to its max on the way (the values themselves are not
+              // needed in this pass)
+              uint32_t s[4][32];
+              float m4[4];
+  #pragma unroll
+              for (int i = 0; i < 4; ++i) tmem_ld32_max(tS + 32 * i, s[i], m4[i]);
+              tmem_ld_wait();
+  #pragma unroll
+              for (int i = 0; i < 4; ++i) asm volatile("" : "+f"(m4[i]));
+              mx0 = fmaxf(m4[0], m4[1]);
+              mx1 = fmaxf(m4[2], m4[3]);
             }
             const float rmax = fmaxf(mx0, mx1);
             mx = fmaxf(mx, rmax);
