@@ -759,14 +759,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ring_kernel(const __grid_const
             }
           } else {
             // Pass 1: row max. All 128 columns are read with a single wait (the
-            // load latency is paid once); pass 2 reads S again in 32-column
-            // chunks inside a compact loop: the hot code shares each scheduler's
-            // instruction cache with the MMA warp, and a small footprint measured
-            // faster than a fully unrolled single pass.
+            // load latency is paid once) and stay in registers; pass 2 turns
+            // them into P chunk by chunk without reading S again.
             float mx0 = kNegInf, mx1 = kNegInf;
+            uint32_t s[4][32];  // the row's scores, kept for pass 2
             if (__any_sync(0xffffffffu, L < 128 || C0 > 0)) {
               // some row of this warp has masked columns: mask, then reduce
-              uint32_t s[4][32];
   #pragma unroll
               for (int i = 0; i < 4; ++i) tmem_ld32(tS + 32 * i, s[i]);
               tmem_ld_wait();
@@ -790,13 +788,15 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ring_kernel(const __grid_const
               // nothing masked: the tensor-memory loads reduce each 32-column
               // chunk to its max on the way (the values themselves are not
               // needed in this pass)
-              uint32_t s[4][32];
               float m4[4];
   #pragma unroll
               for (int i = 0; i < 4; ++i) tmem_ld32_max(tS + 32 * i, s[i], m4[i]);
               tmem_ld_wait();
   #pragma unroll
-              for (int i = 0; i < 4; ++i) asm volatile("" : "+f"(m4[i]));
+              for (int i = 0; i < 4; ++i) {
+                reg_fence(s[i]);
+                asm volatile("" : "+f"(m4[i]));
+              }
               mx0 = fmaxf(m4[0], m4[1]);
               mx1 = fmaxf(m4[2], m4[3]);
             }
@@ -832,23 +832,14 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ring_kernel(const __grid_const
             const uint64_t c2x2 = f2(c2, c2), noff = f2(-off, -off);
             uint64_t lacc[2] = {0, 0};
             float racc[4] = {0.f, 0.f, 0.f, 0.f};
-            // Pass 2: S chunk i (columns 32i..) -> P columns 16i.., already read.
-  #pragma unroll 1
-            for (int i = 0; i < 4; ++i) {
-              uint32_t s[32];
-              tmem_ld32(tS + 32 * i, s);
-              tmem_ld_wait();
-              reg_fence(s);
-              if (L < 128 || C0 > 0) {
+            // Pass 2: S chunk i (columns 32i.., in registers) -> P columns 16i..
   #pragma unroll
-                for (int c = 0; c < 32; ++c)
-                  if (32 * i + c >= L || 32 * i + c < C0) s[c] = 0xff800000u;  // -inf
-              }
+            for (int i = 0; i < 4; ++i) {
               uint32_t pk[16];
   #pragma unroll
               for (int c = 0; c < 16; ++c) {
                 float x0, x1;
-                f2_split(fma2(f2(__uint_as_float(s[2 * c]), __uint_as_float(s[2 * c + 1])), c2x2, noff),
+                f2_split(fma2(f2(__uint_as_float(s[i][2 * c]), __uint_as_float(s[i][2 * c + 1])), c2x2, noff),
                          x0, x1);
                 const float a = ex2(x0), b = ex2(x1);
                 lacc[c & 1] = add2(lacc[c & 1], f2(a, b));
