@@ -16,14 +16,15 @@
 // m, l stay in registers and O in TMEM for the whole walk; only the final
 // O = u / l (or u itself for chunk statistics) goes back to HBM.
 //
-// The softmax comes in two forms, chosen per launch. Without a document mask
-// it takes two passes over S: the row max first (one TMEM read of all 128
-// columns), then the exponentials, with O rescaled when the max grows by more
-// than 2^8. With packed documents (short units, masked tiles) it takes one
-// pass: each 32-column chunk is exponentiated against the row's reference max,
-// which moves (with O, the sums and the P already written rescaled) only when
-// a chunk's max exceeds it by more than 2^32. Both are exact softmax; each form
-// measured faster on its own kind of workload.
+// The softmax comes in two forms, chosen per launch. The two-pass form reads
+// all 128 columns of S once (the row max of unmasked chunks reduced by the
+// load itself), keeps them in registers and then computes the exponentials,
+// with O rescaled when the max grows by more than 2^8. The one-pass form, for
+// packed documents without a causal mask (short, masked units), exponentiates
+// each 32-column chunk against the row's reference max, which moves (with O,
+// the sums and the P already written rescaled) only when a chunk's max exceeds
+// it by more than 2^32. Both are exact softmax; each form measured faster on
+// its own kind of workload.
 //
 // Warp roles (384 threads):
 //   warp 0      TMA producer: Q tiles once per unit, then K_j, V_j into a ring
@@ -524,9 +525,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ring_kernel(const __grid_const
     // The whole warp runs the walk and the waits, so every descriptor and
     // address stays warp-uniform; one elected lane issues each group of MMAs.
     // (Issuing from a single-lane branch measured 80-110 cycles per MMA, above
-    // the 64 cycles an M=128, N=128, K=16 MMA takes.) Per ring step the K/V
-    // waits come first (their copies landed long ago), so that each P_t wait
-    // is followed by one fence and the PV_t and S_t MMAs back to back.
+    // the 64 cycles an M=128, N=128, K=16 MMA takes.) Per ring step PV_0 goes
+    // out as soon as V_j and P_0 are there; the next K tile, whose copy can
+    // still be in flight then, is waited for only before the next S, which
+    // queues behind PV_0.
     {
       const bool leader = elect_one();
       int it = 0, qn = 0, un = 0;
@@ -564,14 +566,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ring_kernel(const __grid_const
           ok = warp_wait(b_kvfull0 + 8 * vst, (it / C::kStages) & 1, abort_flag, budget, kSiteMmaKv);
           if (!ok) break;
           ++it;
-          if (more) {
-            kst = it % C::kStages;
-            ok = warp_wait(b_kvfull0 + 8 * kst, (it / C::kStages) & 1, abort_flag, budget,
-                          kSiteMmaKv);
-            if (!ok) break;
-            ++it;
-          }
-          // query tile 0: PV, then the next S
+          // query tile 0: PV as soon as P_0 is there, then (once the next K
+          // tile has landed) the next S behind it in the same queue
           ok = warp_wait(b_pfull0, pc0 & 1, abort_flag, budget, kSiteMmaP);
           if (!ok) break;
           ++pc0;
@@ -583,12 +579,21 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ring_kernel(const __grid_const
           if (leader) {
             issue_pv(0, vst, j > 0);
             if (!more) mma_commit(b_ofull0);
-            if (more) {
+          }
+          __syncwarp();
+          if (more) {
+            kst = it % C::kStages;
+            ok = warp_wait(b_kvfull0 + 8 * kst, (it / C::kStages) & 1, abort_flag, budget,
+                          kSiteMmaKv);
+            if (!ok) break;
+            ++it;
+            tc_fence_after();
+            if (leader) {
               issue_qk(0, kst);
               mma_commit(b_sfull0);
             }
+            __syncwarp();
           }
-          __syncwarp();
           // query tile 1
           ok = warp_wait(b_pfull0 + 8, pc1 & 1, abort_flag, budget, kSiteMmaP);
           if (!ok) break;
@@ -1095,9 +1100,10 @@ static int launch_d(const TcPlan& plan, void* stream) {
 
 int launch_tc_bf16(const TcPlan& plan, int D, void* stream) {
   if (plan.grid <= 0) return cudaSuccess;
-  // packed documents: the one-pass softmax (short, masked units); otherwise
-  // the two-pass one
-  const bool one = plan.n_docs > 0;
+  // packed documents without a causal mask: the one-pass softmax (short,
+  // masked units; measured faster there); otherwise the two-pass one (also
+  // faster with documents under a causal mask, where units are longer)
+  const bool one = plan.n_docs > 0 && !plan.causal;
   switch (D) {
     case 128: return one ? launch_d<128, true>(plan, stream) : launch_d<128, false>(plan, stream);
     case 96: return one ? launch_d<96, true>(plan, stream) : launch_d<96, false>(plan, stream);

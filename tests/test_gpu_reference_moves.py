@@ -44,9 +44,9 @@ def _spiky(seed, Hq, S, D):
     return q.bfloat16(), k.bfloat16(), v.bfloat16(), scale
 
 
-# docs=[0, S]: one document over the whole sequence masks nothing but selects
-# the kernel's one-pass softmax (the form used with packed documents); without
-# it the two-pass form runs
+# docs=[0, S]: one document over the whole sequence masks nothing but, without
+# a causal mask, selects the kernel's one-pass softmax (the form used with
+# packed documents); otherwise the two-pass form runs
 FORMS = [None, "whole"]
 
 
@@ -70,16 +70,17 @@ def test_reference_moves_inside_tiles(causal, form):
 
 
 @pytest.mark.parametrize("form", FORMS)
-def test_reference_moves_with_fp32_output_and_split_units(form):
+@pytest.mark.parametrize("causal", [True, False])
+def test_reference_moves_with_fp32_output_and_split_units(form, causal):
     """The same rows with many query tiles per head (units split across CTAs,
     partial results merged) and fp32 O."""
     Hq, S, D = 8, 4096, 128
     q, k, v, scale = _spiky(42, Hq, S, D)
     kc = [t.contiguous().to(DEV) for t in torch.split(k, 1024, dim=2)]
     vc = [t.contiguous().to(DEV) for t in torch.split(v, 1024, dim=2)]
-    O, m, l = ring_attention(q.to(DEV), kc, vc, causal=True, out_dtype=torch.float32,
+    O, m, l = ring_attention(q.to(DEV), kc, vc, causal=causal, out_dtype=torch.float32,
                              docs=_docs(form, S))
     device_status()
     pos = np.arange(S)
-    Oref, mref, lref = oracle.full_attention(f64(q), f64(k), f64(v), pos, pos, True, scale)
-    assert_bf16(O, m, l, Oref, mref, lref, what="spiky rows fp32 O")
+    Oref, mref, lref = oracle.full_attention(f64(q), f64(k), f64(v), pos, pos, causal, scale)
+    assert_bf16(O, m, l, Oref, mref, lref, what=f"spiky rows fp32 O causal={causal}")
