@@ -98,6 +98,22 @@ __device__ __forceinline__ void store_staged_rows(const float* stage, float* dst
 }
 
 
+// Non-blocking check of an mbarrier phase, the same answer for the whole warp
+// (lane 0 tests, the warp follows).
+__device__ __forceinline__ bool warp_phase_done(uint32_t bar, uint32_t parity) {
+  uint32_t done = 0;
+  if ((threadIdx.x & 31) == 0) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+  }
+  return __shfl_sync(0xffffffffu, done, 0) != 0;
+}
+
 // Chunk tables: the plan's own arrays, or their device-resident copies (read
 // in separate branches, see ld_kvseg).
 __device__ __forceinline__ KvSeg bspan(const BwdPlan& p, int k) {
@@ -512,18 +528,24 @@ __device__ __forceinline__ void bwd_dkv_tile(const BwdPlan& p, int cta) {
     }
     for (int j = 0; ok && j < n; ++j) {
       const bool more = j + 1 < n;
+      const uint32_t next_full = bb.st_full0 + 8 * ((j + 1) & 1), next_par = ((j + 1) >> 1) & 1;
+      bool s_next = false;  // S^T_{j+1} already issued
       if (more) {
         w.next(p, kmin, kmax, h, qt);
-        ok = warp_wait(bb.s_free, j & 1, bb.abort_flag, budget, kSiteBwdSdp) &&
-             warp_wait(bb.st_full0 + 8 * ((j + 1) & 1), ((j + 1) >> 1) & 1, bb.abort_flag, budget,
-                       kSiteBwdStage);
+        ok = warp_wait(bb.s_free, j & 1, bb.abort_flag, budget, kSiteBwdSdp);
         if (!ok) break;
-        tc_fence_after();
-        if (leader) {
-          issue_bias(tS, base + C::kOnes, stage_b(j + 1));
-          issue_abt<D>(tS, sK, stage_q(j + 1), true);
+        // the next S^T under the elementwise work, if its stage has landed;
+        // otherwise after this pair's dV, dK (which need only the elementwise
+        // results)
+        if (warp_phase_done(next_full, next_par)) {
+          tc_fence_after();
+          if (leader) {
+            issue_bias(tS, base + C::kOnes, stage_b(j + 1));
+            issue_abt<D>(tS, sK, stage_q(j + 1), true);
+          }
+          __syncwarp();
+          s_next = true;
         }
-        __syncwarp();
       }
       ok = warp_wait(bb.ew_done, j & 1, bb.abort_flag, budget, kSiteBwdDs);
       if (!ok) break;
@@ -532,13 +554,25 @@ __device__ __forceinline__ void bwd_dkv_tile(const BwdPlan& p, int cta) {
         issue_tmem_a<D>(tdV, tP, stage_q(j) + C::kTileBytes, j > 0);   // dV += P^T dO
         issue_tmem_a<D>(tdK, tP + 32, stage_q(j), j > 0);             // dK += dS^T Q
         mma_commit(bb.st_empty0 + 8 * (j & 1));
-        if (more) {
+      }
+      __syncwarp();
+      if (more) {
+        if (!s_next) {
+          ok = warp_wait(next_full, next_par, bb.abort_flag, budget, kSiteBwdStage);
+          if (!ok) break;
+          tc_fence_after();
+        }
+        if (leader) {
+          if (!s_next) {
+            issue_bias(tS, base + C::kOnes, stage_b(j + 1));
+            issue_abt<D>(tS, sK, stage_q(j + 1), true);
+          }
           issue_bias(tP, base + C::kOnes, stage_b(j + 1) + C::kBiasBytes);
           issue_abt<D>(tP, sV, stage_q(j + 1) + C::kTileBytes, true);
           mma_commit(bb.sdp_full);
         }
+        __syncwarp();
       }
-      __syncwarp();
     }
     if (leader) {
       if (ok && n > 0) mma_commit(bb.acc_full);
