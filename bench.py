@@ -440,6 +440,30 @@ def secondary_records(dev, flush, steps_small=5):
     peak_b, _, hbm, _ = _peaks()
     stream = torch.cuda.current_stream()
     out = {"forward": [], "backward": [], "hbm_kernels": []}
+    # backward of the headline workload, first: like the headline it is timed
+    # before the long causal records below heat the GPU to its power cap
+    w, qs, kc, vc, rs, segs = build_workload("bf16_8k", None, dev)
+    O, m, l = ring_attention(qs, kc, vc, chunk_spans=rs, q_segments=segs, causal=w.causal)
+    g = torch.Generator(device=dev).manual_seed(99)
+    dout = torch.randn(qs.shape, device=dev, generator=g).to(torch.bfloat16)
+    dq = torch.empty(qs.shape, device=dev, dtype=torch.float32)
+    dk = [torch.empty(k.shape, device=dev, dtype=torch.float32) for k in kc]
+    dv = [torch.empty(v.shape, device=dev, dtype=torch.float32) for v in vc]
+
+    def bstep():
+        ring_attention_bwd(qs, kc, vc, O, dout, m, l, chunk_spans=rs, q_segments=segs,
+                           causal=w.causal, dq=dq, dk=dk, dv=dv)
+
+    times, clk = _timed(bstep, 20, 3, flush, stream, dev.index)
+    device_status()
+    ms = sum(times) / len(times)
+    tf = 2.5 * w.flops() / (ms * 1e-3) / 1e12
+    out["backward"].append({"workload": w.name, "layout": w.layout, "steps": 20, "warmup": 3,
+                            "flops_per_step": 2.5 * w.flops(), "ms_per_step": round(ms, 4),
+                            "tflops": round(tf, 2), "frac_of_peak": round(tf / peak_b, 4),
+                            "clocks": clk})
+    del qs, kc, vc, O, m, l, dout, dq, dk, dv
+    torch.cuda.empty_cache()
     cases = [("bf16_32k_causal", None, steps_small), ("bf16_128k_gqa_causal", "zigzag", steps_small),
              ("bf16_128k_gqa_causal", "contiguous", steps_small),
              ("bf16_128k_gqa_causal", "striped", steps_small), ("bf16_1m_causal", None, 2)]
@@ -464,29 +488,6 @@ def secondary_records(dev, flush, steps_small=5):
                                "imbalance": _imbalance(w, rs, segs), "clocks": clk})
         del qs, kc, vc, o, m, l
         torch.cuda.empty_cache()
-    # backward of the headline workload
-    w, qs, kc, vc, rs, segs = build_workload("bf16_8k", None, dev)
-    O, m, l = ring_attention(qs, kc, vc, chunk_spans=rs, q_segments=segs, causal=w.causal)
-    g = torch.Generator(device=dev).manual_seed(99)
-    dout = torch.randn(qs.shape, device=dev, generator=g).to(torch.bfloat16)
-    dq = torch.empty(qs.shape, device=dev, dtype=torch.float32)
-    dk = [torch.empty(k.shape, device=dev, dtype=torch.float32) for k in kc]
-    dv = [torch.empty(v.shape, device=dev, dtype=torch.float32) for v in vc]
-
-    def bstep():
-        ring_attention_bwd(qs, kc, vc, O, dout, m, l, chunk_spans=rs, q_segments=segs,
-                           causal=w.causal, dq=dq, dk=dk, dv=dv)
-
-    times, clk = _timed(bstep, 20, 3, flush, stream, dev.index)
-    device_status()
-    ms = sum(times) / len(times)
-    tf = 2.5 * w.flops() / (ms * 1e-3) / 1e12
-    out["backward"].append({"workload": w.name, "layout": w.layout, "steps": 20, "warmup": 3,
-                            "flops_per_step": 2.5 * w.flops(), "ms_per_step": round(ms, 4),
-                            "tflops": round(tf, 2), "frac_of_peak": round(tf / peak_b, 4),
-                            "clocks": clk})
-    del qs, kc, vc, O, m, l, dout, dq, dk, dv
-    torch.cuda.empty_cache()
     out["hbm_kernels"] = hbm_kernel_records(dev, flush, 32 * 32768, 20)
     return out
 
