@@ -43,15 +43,16 @@ ra_status ok() {
 }
 
 constexpr int64_t kPosLimit = (int64_t(1) << 31) - 1;
-// Fixed cost of a stream-K unit in key-tile steps (measured: a unit switch
-// costs about two tile steps of a long unit).
 // Weights of the stream-K split, in half key-tile steps: a plain step 2, the
 // fixed cost of a unit 4 (measured: a unit switch costs about two steps of a
-// long unit), and a step of a unit whose rows lie in more than one packed
+// long unit), 8 with packed documents (there a unit's fixed cost measured about
+// four steps: 8 balanced 8K with documents of mean 1024 and 4096 best, +6% and
+// +16% over 4), and a step of a unit whose rows lie in more than one packed
 // document 3 (its rows have different key windows, so its steps mask element
 // by element; of the factors tried, 1.5 balanced best).
 constexpr int64_t kTileCost = 2;
 constexpr int64_t kUnitCost = 4;
+constexpr int64_t kUnitCostDocs = 8;
 constexpr int64_t kMixedTileCost = 3;
 constexpr int64_t kRowLimit = (int64_t(1) << 31) - 256;
 
@@ -545,22 +546,23 @@ ra_status run_tc(const Common& c, const ra_problem& p, const void* q,
   if (T > (int64_t(1) << 30)) return fail(RA_ERR_UNSUPPORTED, "stream-K range too large");
   plan.sk_total = int32_t(T);
   // CTA boundaries on the tile line: each tail unit is weighed as its tiles
-  // times its step cost plus kUnitCost for the unit's fixed costs (its Q
+  // times its step cost plus unit_cost for the unit's fixed costs (its Q
   // load, the switch of the softmax warps, its epilogue), and the weighted
   // line is cut in G equal shares; a cut inside a unit's fixed cost moves to
   // its first tile. With equal units this is the plain cut of the tiles in G
   // shares; with many short units (causal starts, packed documents) or
   // costlier steps the CTAs that get them take fewer tiles.
   {
+    const int64_t unit_cost = c.n_docs > 0 ? kUnitCostDocs : kUnitCost;
     int64_t W = 0;
     for (int64_t i = 0; i < sk_units; ++i)
-      W += kUnitCost + unit_step_cost(R * G + i) * (plan.sk_prefix[i + 1] - plan.sk_prefix[i]);
+      W += unit_cost + unit_step_cost(R * G + i) * (plan.sk_prefix[i + 1] - plan.sk_prefix[i]);
     int64_t i = 0, q = 0;  // unit i starts at weight q
     plan.sk_bound[0] = 0;
     for (int64_t c = 1; c <= G; ++c) {
       const int64_t x = c * W / G;
       while (i < sk_units) {
-        const int64_t wi = kUnitCost + unit_step_cost(R * G + i) *
+        const int64_t wi = unit_cost + unit_step_cost(R * G + i) *
                                            (plan.sk_prefix[i + 1] - plan.sk_prefix[i]);
         if (q + wi > x) break;
         q += wi;
@@ -568,7 +570,7 @@ ra_status run_tc(const Common& c, const ra_problem& p, const void* q,
       }
       const int64_t n = i < sk_units ? plan.sk_prefix[i + 1] - plan.sk_prefix[i] : 0;
       const int64_t f = i < sk_units ? unit_step_cost(R * G + i) : 1;
-      const int64_t in = std::min(n, std::max<int64_t>(0, x - q - kUnitCost) / f);
+      const int64_t in = std::min(n, std::max<int64_t>(0, x - q - unit_cost) / f);
       plan.sk_bound[c] = int32_t(i < sk_units ? plan.sk_prefix[i] + in : T);
     }
     plan.sk_bound[G] = int32_t(T);
