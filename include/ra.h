@@ -307,13 +307,17 @@ ra_status ra_ring_attention_noalloc(const ra_problem* problem, const void* q,
  *
  * All work is stream-ordered on `stream`: the library takes device buffers
  * for Q, the chunks, O, m and l from its memory pool, copies the inputs in
- * (one cudaMemcpyAsync per buffer, issued only after the problem has been
- * validated and planned), runs the kernel of ra_ring_attention, copies O, m
- * and l out and releases the buffers. The call returns once all of that is
- * enqueued. The host buffers must stay valid and unchanged until `stream` has
- * passed this call (cudaStreamSynchronize, an event); page-locked (pinned)
- * host memory gives full copy bandwidth and truly asynchronous copies. Calls
- * on different streams overlap one call's copies with another call's kernel.
+ * (issued only after the problem has been validated and planned), runs the
+ * kernel of ra_ring_attention, copies O, m and l out and releases the
+ * buffers. The call returns once all of that is enqueued. Tensors that lie
+ * back to back inside one pinned host allocation (q, then the k of every
+ * chunk, then the v of every chunk; o, m, l) are copied with one
+ * cudaMemcpyAsync per run, others with one each. The host buffers must stay
+ * valid and unchanged until `stream` has passed this call
+ * (cudaStreamSynchronize, an event); page-locked (pinned) host memory gives
+ * full copy bandwidth and truly asynchronous copies. Calls on different
+ * streams overlap one call's copies with another call's kernel (no call
+ * waits for another stream's release of pool memory).
  *
  * Arguments, positions and results are those of ra_ring_attention, with two
  * differences: every pointer (q, chunks[k].k, chunks[k].v, o, m, l) is a host
