@@ -34,6 +34,10 @@
 //               here that is this multi-stage prefetch with full/empty mbarriers.
 //   warp 1      MMA issuer (the warp waits, one elected lane issues) and TMEM
 //               owner.
+//   warps 2-3   start-up helpers: tensor-map prefetch, and one read of every
+//               plan line the other roles' first walks need (those walks read
+//               the plan one dependent load after another; cached lines cut
+//               the time to the first copy and the first S).
 //   warps 4-7   softmax warpgroup for query tile 0 (TMEM lanes 0-127)
 //   warps 8-11  softmax warpgroup for query tile 1
 // The MMA order S0(j) S1(j) | PV0(j) S0(j+1) PV1(j) S1(j+1) | ... lets the
@@ -411,17 +415,6 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ring_kernel(const __grid_const
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 0 && lane == 0) {
-    prefetch_tmap(&p.qmap);
-    if (p.ext_kmap == nullptr) {
-      for (int c = 0; c < p.n_chunks; ++c) {
-        if (p.chunk_seg_begin[c] != p.chunk_seg_begin[c + 1]) {
-          prefetch_tmap(&p.kmap[c]);
-          prefetch_tmap(&p.vmap[c]);
-        }
-      }
-    }
-  }
   if (warp == 1) {
     tmem_alloc(smem_addr(tmem_slot), 512);
     tmem_relinquish();
@@ -624,6 +617,40 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ring_kernel(const __grid_const
       drain_wait(b_done, 0, budget);
     }
     __syncwarp();
+  } else if (warp == 2) {
+    // tensor maps into the TMA unit's cache ahead of their first copies, one
+    // lane per chunk (the chunk-table reads overlap)
+    if (lane == 0) prefetch_tmap(&p.qmap);
+    if (p.ext_kmap == nullptr) {
+#pragma unroll
+      for (int k = 0; k < kTcMaxChunks / 32; ++k) {
+        const int c = lane + 32 * k;
+        if (c < p.n_chunks && p.chunk_seg_begin[c] != p.chunk_seg_begin[c + 1]) {
+          prefetch_tmap(&p.kmap[c]);
+          prefetch_tmap(&p.vmap[c]);
+        }
+      }
+    }
+  } else {
+    // warp 3: the plan lines that the first walks of the other roles read one
+    // after another, read here all at once so that those reads hit
+    uint32_t v[12];
+    v[0] = uint32_t(p.sk_prefix[min(lane * 16, min(p.sk_units, kTcMaxSkUnits))]);
+    v[1] = uint32_t(p.sk_bound[min(lane * 16, min(p.grid, kTcMaxGrid))]);
+    v[2] = uint32_t(p.sk_first[max(0, min(lane * 32, min(p.grid, kTcMaxGrid) - 1))]);
+    v[3] = uint32_t(p.chunk_seg_begin[min(lane * 16, min(p.n_chunks, kTcMaxChunks))]);
+    v[4] = uint32_t(p.qp[min(lane, kMaxQPieces - 1)].row0);
+    v[5] = uint32_t(p.qp[min(lane + 32, kMaxQPieces - 1)].row0);
+    v[6] = uint32_t(p.ks[min(lane, kTcMaxKvSegs - 1)].ntiles);
+    v[7] = uint32_t(p.ks[min(lane + 32, kTcMaxKvSegs - 1)].ntiles);
+    v[8] = uint32_t(p.doc_bounds[min(lane * 16, min(p.n_docs, kMaxDocs))]);
+    v[9] = uint32_t(p.doc_bounds[min(lane * 16 + 512, min(p.n_docs, kMaxDocs))]);
+    v[10] = uint32_t(p.B + p.Hq + p.n_qpieces + p.dp_rounds);
+    v[11] = uint32_t(p.ext_ks != nullptr) + uint32_t(p.n_units);
+    uint32_t acc = 0;
+#pragma unroll
+    for (int i = 0; i < 12; ++i) acc ^= v[i];
+    asm volatile("" ::"r"(acc));
   }
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 200;\n" ::: "memory");
