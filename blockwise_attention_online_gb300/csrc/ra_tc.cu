@@ -522,6 +522,16 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ring_kernel(const __grid_const
     // out as soon as V_j and P_0 are there; the next K tile, whose copy can
     // still be in flight then, is waited for only before the next S, which
     // queues behind PV_0.
+    //
+    // In the two-pass form the warp polls its barriers instead of sleeping in
+    // try_wait: it then reacts to a landed K/V tile or a finished P at once
+    // (8K non-causal +2.6%, the long causal launches +2%). With packed
+    // documents (one-pass form) the polls' issue slots, taken from the
+    // softmax warps of the same scheduler, cost as much as they save.
+    auto mwait = [&](uint32_t bar, uint32_t parity, int site) {
+      if constexpr (kOnePass) return warp_wait(bar, parity, abort_flag, budget, site);
+      else return warp_wait_spin(bar, parity, abort_flag, budget, site);
+    };
     {
       const bool leader = elect_one();
       int it = 0, qn = 0, un = 0;
@@ -536,11 +546,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ring_kernel(const __grid_const
         decode_unit(p, I.u, U);
         const int n = (I.t1 < 0 ? U.n : I.t1) - I.t0;
         if (n == 0) continue;
-        ok = warp_wait(b_qfull, qn & 1, abort_flag, budget, kSiteMmaQ);
+        ok = mwait(b_qfull, qn & 1, kSiteMmaQ);
         if (!ok) break;
         ++qn;
         int kst = it % C::kStages;
-        ok = warp_wait(b_kvfull0 + 8 * kst, (it / C::kStages) & 1, abort_flag, budget, kSiteMmaKv);
+        ok = mwait(b_kvfull0 + 8 * kst, (it / C::kStages) & 1, kSiteMmaKv);
         if (!ok) break;
         ++it;
         tc_fence_after();
@@ -556,16 +566,16 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ring_kernel(const __grid_const
         for (int j = 0; j < n; ++j) {
           const bool more = j + 1 < n;
           const int vst = it % C::kStages;
-          ok = warp_wait(b_kvfull0 + 8 * vst, (it / C::kStages) & 1, abort_flag, budget, kSiteMmaKv);
+          ok = mwait(b_kvfull0 + 8 * vst, (it / C::kStages) & 1, kSiteMmaKv);
           if (!ok) break;
           ++it;
           // query tile 0: PV as soon as P_0 is there, then (once the next K
           // tile has landed) the next S behind it in the same queue
-          ok = warp_wait(b_pfull0, pc0 & 1, abort_flag, budget, kSiteMmaP);
+          ok = mwait(b_pfull0, pc0 & 1, kSiteMmaP);
           if (!ok) break;
           ++pc0;
           if (j == 0) {
-            ok = warp_wait(b_ofree0, (un & 1) ^ 1, abort_flag, budget, kSiteMmaO);
+            ok = mwait(b_ofree0, (un & 1) ^ 1, kSiteMmaO);
             if (!ok) break;
           }
           tc_fence_after();
@@ -576,8 +586,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ring_kernel(const __grid_const
           __syncwarp();
           if (more) {
             kst = it % C::kStages;
-            ok = warp_wait(b_kvfull0 + 8 * kst, (it / C::kStages) & 1, abort_flag, budget,
-                          kSiteMmaKv);
+            ok = mwait(b_kvfull0 + 8 * kst, (it / C::kStages) & 1, kSiteMmaKv);
             if (!ok) break;
             ++it;
             tc_fence_after();
@@ -588,11 +597,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ring_kernel(const __grid_const
             __syncwarp();
           }
           // query tile 1
-          ok = warp_wait(b_pfull0 + 8, pc1 & 1, abort_flag, budget, kSiteMmaP);
+          ok = mwait(b_pfull0 + 8, pc1 & 1, kSiteMmaP);
           if (!ok) break;
           ++pc1;
           if (j == 0) {
-            ok = warp_wait(b_ofree0 + 8, (un & 1) ^ 1, abort_flag, budget, kSiteMmaO);
+            ok = mwait(b_ofree0 + 8, (un & 1) ^ 1, kSiteMmaO);
             if (!ok) break;
           }
           tc_fence_after();

@@ -49,6 +49,34 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
   return __all_sync(0xffffffffu, ok);
 }
 
+// Polling version of warp_wait: the warp tests the phase without ever
+// sleeping, so it sees the completion at once, at the price of the issue slots
+// its polls take from the warps that share its scheduler. The clock and the
+// abort flag are read every 256 polls.
+__device__ __forceinline__ bool warp_wait_spin(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                               unsigned long long budget, int site) {
+  bool ok = true;
+  if (!ptx::mbar_test_wait(bar, parity)) {
+    const unsigned long long t0 = ptx::globaltimer();
+    for (uint32_t k = 1;; ++k) {
+      if (ptx::mbar_test_wait(bar, parity)) break;
+      if ((k & 255u) == 0) {
+        if (*abort_flag) {
+          ok = false;
+          break;
+        }
+        if (ptx::globaltimer() - t0 > budget) {
+          *abort_flag = 1;
+          record_error(0x100 | site);
+          ok = false;
+          break;
+        }
+      }
+    }
+  }
+  return __all_sync(0xffffffffu, ok);
+}
+
 // Wait used while tearing down after an abort: ignores the abort flag and
 // has its own generous budget (copies and MMAs already issued always finish;
 // the CTA must not exit before they do, whatever the normal wait budget is).
