@@ -145,8 +145,9 @@ struct alignas(128) TcPlan {
   int32_t n_units;
   // work split: every CTA first takes dp_rounds whole units round-robin, then
   // its share [sk_bound[c], sk_bound[c+1]) of the T key tiles of units
-  // dp_rounds*G .. (laid end to end, sk_prefix[i] = first tile of unit i)
-  int32_t grid, dp_rounds, sk_units, sk_total;
+  // dp_rounds*G .. (laid end to end, sk_prefix[i] = first tile of unit i).
+  // dp_snake: odd rounds hand the units to the CTAs in reverse order.
+  int32_t grid, dp_rounds, sk_units, sk_total, dp_snake;
   unsigned epoch;                    // value a published partial carries
   TcScratch scratch;                 // null pointers when no unit is split
   int32_t sk_prefix[kTcMaxSkUnits + 1];

@@ -251,7 +251,8 @@ struct TileIter {
   }
 };
 
-// A CTA's work, in order: whole units c, c+G, ... for dp_rounds rounds, then
+// A CTA's work, in order: whole units c, c+G, ... for dp_rounds rounds (in
+// odd rounds unit G-1-c instead when the plan says so), then
 // its share [sk_bound[c], sk_bound[c+1]) of the key tiles of the remaining
 // units laid end to end (a stream-K split; the host places the cuts so that
 // shares of tiles plus per-unit fixed costs are equal). A share may begin
@@ -275,7 +276,7 @@ struct Walker {
   }
   __device__ __forceinline__ bool next(const TcPlan& p, Item& it) {
     if (k < p.dp_rounds) {
-      it.u = blockIdx.x + k * p.grid;
+      it.u = ((p.dp_snake && (k & 1)) ? p.grid - 1 - int(blockIdx.x) : int(blockIdx.x)) + k * p.grid;
       it.t0 = 0;
       it.t1 = -1;  // the whole unit
       it.kind = kFull;
