@@ -517,8 +517,14 @@ ra_status run_tc(const Common& c, const ra_problem& p, const void* q,
     for (int64_t i = 0; i < npairs; ++i) plan.order[i] = uint16_t(order[i]);
     plan.has_order = 1;
   }
-  auto unit_tiles = [&](int64_t u) { return work[order[u / BH]]; };
-  auto unit_step_cost = [&](int64_t u) { return step_cost[order[u / BH]]; };
+  int pair_block = 1;
+  auto unit_rank = [&](int64_t u) {
+    int rank, b, hq;
+    ra::unit_coords(int(u), int(npairs), int(c.B), int(c.Hq), int(c.Hkv), pair_block, rank, b, hq);
+    return rank;
+  };
+  auto unit_tiles = [&](int64_t u) { return work[order[unit_rank(u)]]; };
+  auto unit_step_cost = [&](int64_t u) { return step_cost[order[unit_rank(u)]]; };
 
   const int sms = num_sms();
   if (sms <= 0) return cuda_status(cudaErrorNoDevice, "querying the SM count");
@@ -536,14 +542,21 @@ ra_status run_tc(const Common& c, const ra_problem& p, const void* q,
   }
   plan.grid = int32_t(G);
   plan.dp_rounds = int32_t(R);
-  // Units are ordered costliest first, so in plain round-robin CTA 0 takes
-  // the costliest unit of every round and falls further behind each round;
-  // CTAs that work on units sharing keys then drift apart and L2 reuse
-  // drops (32K causal: 21 GB of DRAM reads per launch instead of 8.6).
-  // Alternate rounds run in reverse CTA order to cancel the drift. With
-  // grouped query heads (Hq > Hkv) the reversal measured 3-5% slower on
-  // every layout of the 128K launch, so it is used only with Hq == Hkv.
-  plan.dp_snake = (R > 1 && c.Hq == c.Hkv) ? 1 : 0;
+  // Unit order of the whole-unit rounds. Pair-major units put every
+  // key/value stream (batch, key/value head) into every round, so the units
+  // sharing a stream's keys are few and far apart in time; with the long
+  // causal launches most of the key/value stream then came from DRAM (128K
+  // with 8 key/value heads: 171 GB per launch; 32K: 9.3 GB). Blocks of
+  // G / (Hq / Hkv) pair ranks with the stream outermost make each round one
+  // stream: 11 GB and 1.1 GB, +4-5% at 32K and 128K, +10% at 1M (whose clock
+  // the power cap sets: less DRAM traffic, a higher clock). Inside a round
+  // the CTAs take the pair ranks in order, so alternate rounds run in
+  // reverse CTA order; otherwise CTA 0 takes the costliest unit of every
+  // round and the CTAs drift apart.
+  plan.dp_snake = R > 1 ? 1 : 0;
+  if (R > 1)
+    pair_block = int(std::max<int64_t>(1, std::min<int64_t>(npairs, G / (c.Hq / c.Hkv))));
+  plan.pair_block = pair_block;
   plan.sk_units = int32_t(sk_units);
   int64_t T = 0;
   plan.sk_prefix[0] = 0;

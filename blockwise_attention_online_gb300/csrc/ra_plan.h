@@ -80,6 +80,24 @@ RA_HD void key_window(const Plan& p, int pos, int& lo, int& hi) {
   }
 }
 
+// Work unit u -> the rank of its query-tile pair in the visit order, its
+// batch and its query head. Units come in blocks of pair_block pair ranks
+// (the last block may be shorter); inside a block the key/value streams
+// (batch, key/value head) are outermost, then the pair, then the query heads
+// sharing the stream. pair_block = 1: pair-major, heads innermost.
+RA_HD void unit_coords(int u, int n_qpairs, int B, int Hq, int Hkv, int pair_block, int& rank,
+                       int& b, int& hq) {
+  const int gq = Hq / Hkv, BH = B * Hq;
+  const int blk = u / (pair_block * BH);
+  const int w = u - blk * (pair_block * BH);
+  const int pe = (n_qpairs - blk * pair_block) < pair_block ? (n_qpairs - blk * pair_block) : pair_block;
+  const int s = w / (pe * gq), rem = w - s * (pe * gq);
+  const int pi = rem / gq, j = rem - pi * gq;
+  rank = blk * pair_block + pi;
+  b = s / Hkv;
+  hq = (s - b * Hkv) * gq + j;
+}
+
 // Tiles [tb, te) of a monotone key span (positions pos0 + step * i, len rows,
 // 128-row tiles) that hold at least one position inside [lo, hi]. The host
 // (work estimates) and the kernels (tile walks) share this arithmetic, so
@@ -147,7 +165,8 @@ struct alignas(128) TcPlan {
   // its share [sk_bound[c], sk_bound[c+1]) of the T key tiles of units
   // dp_rounds*G .. (laid end to end, sk_prefix[i] = first tile of unit i).
   // dp_snake: odd rounds hand the units to the CTAs in reverse order.
-  int32_t grid, dp_rounds, sk_units, sk_total, dp_snake;
+  // pair_block: the unit order's block of pair ranks (unit_coords).
+  int32_t grid, dp_rounds, sk_units, sk_total, dp_snake, pair_block;
   unsigned epoch;                    // value a published partial carries
   TcScratch scratch;                 // null pointers when no unit is split
   int32_t sk_prefix[kTcMaxSkUnits + 1];

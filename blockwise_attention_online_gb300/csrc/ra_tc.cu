@@ -170,11 +170,11 @@ __device__ __forceinline__ void live_tiles(const TcPlan& p, int k, const Unit& U
 }
 
 __device__ __forceinline__ void decode_unit(const TcPlan& p, int u, Unit& U) {
-  const int BH = p.B * p.Hq;
-  const int rank = u / BH, bh = u - rank * BH;
+  int rank, ub, uhq;
+  unit_coords(u, p.n_qpairs, p.B, p.Hq, p.Hkv, p.pair_block, rank, ub, uhq);
   const int qpair = p.has_order ? int(p.order[rank]) : rank;
-  U.b = bh / p.Hq;
-  U.hq = bh - U.b * p.Hq;
+  U.b = ub;
+  U.hq = uhq;
   U.hkv = U.hq / (p.Hq / p.Hkv);
   U.qrow0 = qpair * kTcRowsPerUnit;
   const int r1 = min(U.qrow0 + kTcRowsPerUnit, p.Sq);
