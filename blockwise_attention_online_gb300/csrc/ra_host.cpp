@@ -261,10 +261,12 @@ ra_status get_encoder() {
   return RA_OK;
 }
 
-// 4-D bf16 map over [B, H, rows, D] with box 64 x 128 (one 128-byte swizzle
-// atom wide, one 128-row tile high); rows past `rows` read as zero.
+// 4-D bf16 map over [B, H, rows, D] with box 64 x box_rows (one 128-byte
+// swizzle atom wide; a 128-row tile high unless given); rows past `rows`
+// read as zero and are not written.
 ra_status make_map(CUtensorMap* map, const void* base, int64_t D, int64_t rows,
-                   int64_t H, int64_t B, const ra_strides& st, const char* what) {
+                   int64_t H, int64_t B, const ra_strides& st, const char* what,
+                   cuuint32_t box_rows = 128) {
   cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)rows, (cuuint64_t)H, (cuuint64_t)B};
   cuuint64_t strides[3] = {(cuuint64_t)st.row * 2, (cuuint64_t)st.head * 2,
                            (cuuint64_t)st.batch * 2};
@@ -272,7 +274,7 @@ ra_status make_map(CUtensorMap* map, const void* base, int64_t D, int64_t rows,
   if (rows == 1) strides[0] = std::max<cuuint64_t>(16, strides[0] & ~cuuint64_t(15));
   if (H == 1) strides[1] = std::max<cuuint64_t>(16, strides[1] & ~cuuint64_t(15));
   if (B == 1) strides[2] = std::max<cuuint64_t>(16, strides[2] & ~cuuint64_t(15));
-  cuuint32_t box[4] = {64, 128, 1, 1};
+  cuuint32_t box[4] = {64, box_rows, 1, 1};
   cuuint32_t estr[4] = {1, 1, 1, 1};
   CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base),
                         dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -422,6 +424,13 @@ ra_status run_tc(const Common& c, const ra_problem& p, const void* q,
   if ((st = make_map(&plan.qmap, q, c.D, std::max<int64_t>(c.Sq, 1), c.Hq, c.B,
                      p.q_strides, "q")) != RA_OK)
     return st;
+  // bf16 O at head_dim 128: each softmax warp's 32 rows x 64 columns leave
+  // its staging area in one asynchronous TMA store (box 64 x 32)
+  if (!out_f32 && c.D == 128 && c.Sq > 0) {
+    if ((st = make_map(&plan.omap, out, c.D, c.Sq, c.Hq, c.B, p.o_strides, "out", 32)) != RA_OK)
+      return st;
+    plan.o_tma = 1;
+  }
   // device-resident tables are assembled here and copied in right before the
   // launch (the copy from pageable memory is staged, so this buffer may be
   // reused as soon as the copy call returns)

@@ -147,6 +147,7 @@ struct TcScratch {
 
 struct alignas(128) TcPlan {
   CUtensorMap qmap;                  // Q  [B, Hq, Sq, D] bf16, box 64 x 128
+  CUtensorMap omap;                  // O  [B, Hq, Sq, D] bf16, box 64 x 32 (when o_tma)
   CUtensorMap kmap[kTcMaxChunks];    // K chunk c [B, Hkv, len, D]
   CUtensorMap vmap[kTcMaxChunks];    // V chunk c
   void* out;                         // O (bf16) or u (fp32, stats mode)
@@ -159,6 +160,7 @@ struct alignas(128) TcPlan {
   int32_t causal, stats_mode, ring, n_chunks;
   float scale, scale_log2;
   int32_t o_fp32;                    // ring mode: O written as fp32 instead of bf16
+  int32_t o_tma;                     // bf16 O at head_dim 128 leaves through omap
   int32_t n_qpieces, n_kvsegs, n_qpairs, has_order;
   int32_t n_units;
   // work split: every CTA first takes dp_rounds whole units round-robin, then

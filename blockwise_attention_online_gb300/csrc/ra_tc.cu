@@ -99,8 +99,9 @@ struct Cfg {
   static constexpr int kKvOff = 2 * kTileBytes;
   static constexpr int kBarOff = kKvOff + kStages * kTileBytes;
   static constexpr int kBarBytes = 256;
-  // output staging: 4 KB per softmax warp (32 rows x 128 bytes)
-  static constexpr int kStageOff = kBarOff + kBarBytes;
+  // output staging: 4 KB per softmax warp (32 rows x 128 bytes), 1024-byte
+  // aligned (the 128-byte swizzle of the O tensor map repeats every 1024)
+  static constexpr int kStageOff = kBarOff + 1024;
   static constexpr int kStageBytes = 8 * 4096;
   static constexpr int kSmemBytes = kStageOff + kStageBytes + 1024;  // + alignment slack
   static_assert(kSmemBytes <= 232448, "shared memory per CTA");
@@ -303,6 +304,28 @@ struct Walker {
 // conflicts); then each store instruction covers 32 / NC whole row pieces
 // instead of 32 rows 16 bytes apart. Rows at and past `rows_valid` are not
 // written. Every lane of the warp must call it.
+// One warp writes the 32 rows x 128 bytes of a 64-column O piece through its
+// staging area (1024-byte aligned) with one asynchronous TMA store: each
+// lane deposits its row in the O map's 128-byte swizzle (16-byte chunk k of
+// row r at slot k ^ (r & 7)), and lane 0 issues the copy. The area is
+// rewritten only after the warp's previous copy has read it. Rows past the
+// end of the sequence are clipped by the map.
+__device__ __forceinline__ void warp_store_tma(uint8_t* stage, uint32_t stage_s, const uint4 (&ch)[8],
+                                               int lane, const CUtensorMap* omap, int col, int row,
+                                               int hq, int b) {
+  if (lane == 0) bulk_wait_read_all();
+  __syncwarp();
+#pragma unroll
+  for (int k = 0; k < 8; ++k)
+    *reinterpret_cast<uint4*>(stage + lane * 128 + ((k ^ (lane & 7)) * 16)) = ch[k];
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    tma_store_4d(omap, stage_s, col, row, hq, b);
+    bulk_commit_group();
+  }
+}
+
 template <int NC>
 __device__ __forceinline__ void warp_store_staged(uint8_t* stage, const uint4 (&ch)[NC], int lane,
                                                   char* row0, int64_t row_bytes, int rows_valid) {
@@ -1084,6 +1107,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ring_kernel(const __grid_const
             ch[k].z = pack_bf16x2(__uint_as_float(o[cc][c + 4]) * fo, __uint_as_float(o[cc][c + 5]) * fo);
             ch[k].w = pack_bf16x2(__uint_as_float(o[cc][c + 6]) * fo, __uint_as_float(o[cc][c + 7]) * fo);
           }
+          if constexpr (NC == 8) {
+            if (p.o_tma) {
+              if (wvalid > 0)
+                warp_store_tma(stage, smem_addr(stage), ch, lane, &p.omap, h * 64, wrow0, U.hq, U.b);
+              continue;
+            }
+          }
           warp_store_staged<NC>(stage, ch, lane,
                                 reinterpret_cast<char*>(static_cast<uint16_t*>(p.out) + wbase + h * kHalf * 32),
                                 p.o_sr * 2, wvalid);
@@ -1095,6 +1125,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ring_kernel(const __grid_const
         p.l[ml_idx] = l * corr;
       }
     }
+    // this warp's O copies are complete before its staging area goes away
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
   }
 
   tc_fence_before();
