@@ -472,6 +472,11 @@ ra_status run_tc(const Common& c, const ra_problem& p, const void* q,
   fill_q_pieces(c, plan.qp, &plan.n_qpieces, ext_tables ? tables.data() + lay.qp : nullptr);
   fill_docs(c, plan.doc_bounds, &plan.n_docs);
   plan.n_kvsegs = int32_t(c.kvspans.size());
+  // every key tile whole and visible to every row: the softmax needs no
+  // column bounds and no walk over the key spans
+  plan.full_tiles = (!c.causal && plan.n_docs == 0) ? 1 : 0;
+  for (const Span& kv : c.kvspans)
+    if (kv.len % 128 != 0) plan.full_tiles = 0;
   if (ext_tables) {
     std::memcpy(tables.data() + lay.kmap, ext_maps.data(), size_t(2) * c.nchunks * sizeof(CUtensorMap));
     for (size_t i = 0; i < c.kvspans.size(); ++i) {

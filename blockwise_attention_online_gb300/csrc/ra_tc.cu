@@ -712,15 +712,20 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ring_kernel(const __grid_const
       int rlo = 0, rhi = 0x7ffffffe;
       if (rvalid && (p.causal || p.n_docs > 0)) key_window(p, row_position(p, grow), rlo, rhi);
       float m_ref = kNegInf, mx = kNegInf, l = 0.f, lr = 0.f;
+      // Launches whose key tiles are all whole and visible to every row skip
+      // the walk over the key spans (its dependent plan reads sat between a
+      // step's P and the next S: 8K +2.3%).
+      const bool walk = !p.full_tiles;
       if (n > 0) {
         TileIter iter;
-        iter.seek(p, U, I.t0);
-        int ks, t;
-        for (int j = 0; j < n && iter.next(p, U, ks, t); ++j) {
+        if (walk) iter.seek(p, U, I.t0);
+        int ks = 0, t = 0;
+        for (int j = 0; j < n; ++j) {
           // visible columns of this row: the range [C0, L) of the tile (known
           // before S arrives; C0 > 0 only where a document starts inside it)
-          int L, C0 = 0;
-          {
+          int L = 128, C0 = 0;
+          if (walk) {
+            if (!iter.next(p, U, ks, t)) break;
             const KvSeg sg = span_of(p, ks);
             L = min(128, sg.len - 128 * t);
             if (p.causal || p.n_docs) {
