@@ -719,14 +719,18 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ring_kernel(const __grid_const
       if (n > 0) {
         TileIter iter;
         if (walk) iter.seek(p, U, I.t0);
-        int ks = 0, t = 0;
+        int ks = 0, t = 0, sg_k = -1;
+        KvSeg sg = {};
         for (int j = 0; j < n; ++j) {
           // visible columns of this row: the range [C0, L) of the tile (known
           // before S arrives; C0 > 0 only where a document starts inside it)
           int L = 128, C0 = 0;
           if (walk) {
             if (!iter.next(p, U, ks, t)) break;
-            const KvSeg sg = span_of(p, ks);
+            if (ks != sg_k) {  // the span's fields stay in registers while its tiles run
+              sg = span_of(p, ks);
+              sg_k = ks;
+            }
             L = min(128, sg.len - 128 * t);
             if (p.causal || p.n_docs) {
               const int first = sg.pos0 + sg.step * (128 * t);
