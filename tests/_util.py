@@ -48,13 +48,21 @@ def bf16_half_ulp(x):
     return np.where(ax > 0, np.exp2(e - 8), 0.0)
 
 
+# Below this |O| a bf16 output's own rounding (at most 2^-8 there) leaves
+# room inside 1e-2, so the plain bound applies; above it half an ulp of the
+# reference (2^-7 from |O| = 2, 2^-6 from 4) is allowed on top.
+BF16_O_SLACK_FROM = 2.0
+
+
 def assert_bf16(O, m, l, Oref, mref, lref, what=""):
-    """O: within 1e-2 of the oracle when O is fp32; a bf16 O may in addition
-    carry its own rounding (half an ulp of the reference value)."""
+    """O: within 1e-2 of the oracle when O is fp32, and for a bf16 O wherever
+    |O_ref| < 2; a bf16 O at |O_ref| >= 2 may in addition carry its own
+    rounding (half an ulp of the reference value)."""
     out_bf16 = isinstance(O, torch.Tensor) and O.dtype == torch.bfloat16
     O, m, l = f64(O), f64(m), f64(l)
     assert not np.isnan(O).any() and not np.isnan(l).any(), f"{what}: NaN"
-    tol = BF16_O_ATOL + (bf16_half_ulp(Oref) if out_bf16 else 0.0)
+    slack = np.where(np.abs(Oref) >= BF16_O_SLACK_FROM, bf16_half_ulp(Oref), 0.0)
+    tol = BF16_O_ATOL + (slack if out_bf16 else 0.0)
     excess = np.abs(O - Oref) - tol
     err = np.abs(O - Oref).max() if O.size else 0.0
     if O.size and excess.max() > 0:
