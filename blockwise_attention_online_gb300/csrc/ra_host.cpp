@@ -571,6 +571,13 @@ ra_status run_tc(const Common& c, const ra_problem& p, const void* q,
   if (R > 1)
     pair_block = int(std::max<int64_t>(1, std::min<int64_t>(npairs, G / (c.Hq / c.Hkv))));
   plan.pair_block = pair_block;
+  // The MMA warp polls its barriers unless the units are very long (more
+  // than 1024 key tiles on average). Measured under the power cap: polling
+  // raises the work per clock but lowers the clock the cap allows, and for
+  // long units the second wins (512K causal: sleeping waits +0.8%, 1M +2%,
+  // 1M with logits of +-60 +7%); up to 128K polling wins by 2-4%, sustained
+  // runs included.
+  plan.mma_poll = total_tiles <= int64_t(1024) * units ? 1 : 0;
   plan.sk_units = int32_t(sk_units);
   int64_t T = 0;
   plan.sk_prefix[0] = 0;

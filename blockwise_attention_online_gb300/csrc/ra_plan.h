@@ -162,6 +162,7 @@ struct alignas(128) TcPlan {
   int32_t o_fp32;                    // ring mode: O written as fp32 instead of bf16
   int32_t o_tma;                     // bf16 O at head_dim 128 leaves through omap
   int32_t full_tiles;                // no causal mask, no documents, key spans of whole 128-row tiles
+  int32_t mma_poll;                  // the MMA warp polls its barriers (two-pass form)
   int32_t n_qpieces, n_kvsegs, n_qpairs, has_order;
   int32_t n_units;
   // work split: every CTA first takes dp_rounds whole units round-robin, then

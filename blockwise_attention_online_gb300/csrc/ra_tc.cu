@@ -548,13 +548,15 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ring_kernel(const __grid_const
     // queues behind PV_0.
     //
     // In the two-pass form the warp polls its barriers instead of sleeping in
-    // try_wait: it then reacts to a landed K/V tile or a finished P at once
-    // (8K non-causal +2.6%, the long causal launches +2%). With packed
-    // documents (one-pass form) the polls' issue slots, taken from the
-    // softmax warps of the same scheduler, cost as much as they save.
+    // try_wait when the plan says so: it then reacts to a landed K/V tile or a
+    // finished P at once (8K non-causal +2.6%, 32K and 128K causal +2-4%).
+    // With packed documents (one-pass form) the polls' issue slots, taken
+    // from the softmax warps of the same scheduler, cost as much as they
+    // save; the host leaves polling off for launches of very long units too.
+    const bool poll = !kOnePass && p.mma_poll;
     auto mwait = [&](uint32_t bar, uint32_t parity, int site) {
-      if constexpr (kOnePass) return warp_wait(bar, parity, abort_flag, budget, site);
-      else return warp_wait_spin(bar, parity, abort_flag, budget, site);
+      return poll ? warp_wait_spin(bar, parity, abort_flag, budget, site)
+                  : warp_wait(bar, parity, abort_flag, budget, site);
     };
     {
       const bool leader = elect_one();
@@ -1090,7 +1092,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ring_kernel(const __grid_const
               }
           }
         }
-        // write this half through the warp's staging area (coalesced rows)
+        // write this half through the warp's staging area: a TMA store of the
+        // staged rows (bf16 O, head_dim 128) or whole-row stores by the warp
         if (p.o_fp32) {
 #pragma unroll
           for (int cc = 0; cc < kHalf; ++cc) {
