@@ -398,7 +398,7 @@ __device__ __noinline__ float4 rescale_p(uint32_t tS, int n, float alpha) {
   return make_float4(racc[0], racc[1], racc[2], racc[3]);
 }
 
-template <int D, bool kOnePass>
+template <int D, bool kOnePass, bool kPoll>
 __global__ void __launch_bounds__(kThreads, 1) tc_ring_kernel(const __grid_constant__ TcPlan p) {
   using C = Cfg<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -547,16 +547,18 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ring_kernel(const __grid_const
     // still be in flight then, is waited for only before the next S, which
     // queues behind PV_0.
     //
-    // In the two-pass form the warp polls its barriers instead of sleeping in
-    // try_wait when the plan says so: it then reacts to a landed K/V tile or a
-    // finished P at once (8K non-causal +2.6%, 32K and 128K causal +2-4%).
-    // With packed documents (one-pass form) the polls' issue slots, taken
-    // from the softmax warps of the same scheduler, cost as much as they
-    // save; the host leaves polling off for launches of very long units too.
-    const bool poll = !kOnePass && p.mma_poll;
+    // With kPoll (two-pass form only) the warp polls its barriers instead of
+    // sleeping in try_wait: it then reacts to a landed K/V tile or a finished
+    // P at once (8K non-causal +2.6%, 32K and 128K causal +2-4%). With packed
+    // documents (one-pass form) the polls' issue slots, taken from the
+    // softmax warps of the same scheduler, cost as much as they save, and the
+    // host leaves polling off for launches of very long units too. The choice
+    // is a template parameter: as a runtime branch between the two inlined
+    // waits it cost 7% at 8K in the generated code alone.
+    static_assert(!(kOnePass && kPoll), "the one-pass form does not poll");
     auto mwait = [&](uint32_t bar, uint32_t parity, int site) {
-      return poll ? warp_wait_spin(bar, parity, abort_flag, budget, site)
-                  : warp_wait(bar, parity, abort_flag, budget, site);
+      if constexpr (kPoll) return warp_wait_spin(bar, parity, abort_flag, budget, site);
+      else return warp_wait(bar, parity, abort_flag, budget, site);
     };
     {
       const bool leader = elect_one();
@@ -1159,9 +1161,9 @@ void tc_scratch_carve(void* base, int grid, int D, TcScratch* s) {
   s->flags = reinterpret_cast<unsigned*>(b);
 }
 
-template <int D, bool kOnePass>
+template <int D, bool kOnePass, bool kPoll>
 static int launch_d(const TcPlan& plan, void* stream) {
-  cudaError_t e = cudaFuncSetAttribute(tc_ring_kernel<D, kOnePass>,
+  cudaError_t e = cudaFuncSetAttribute(tc_ring_kernel<D, kOnePass, kPoll>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::kSmemBytes);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -1175,7 +1177,7 @@ static int launch_d(const TcPlan& plan, void* stream) {
   attr[0].val.cooperative = plan.scratch.flags != nullptr ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, tc_ring_kernel<D, kOnePass>, plan);
+  e = cudaLaunchKernelEx(&cfg, tc_ring_kernel<D, kOnePass, kPoll>, plan);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -1186,10 +1188,17 @@ int launch_tc_bf16(const TcPlan& plan, int D, void* stream) {
   // masked units; measured faster there); otherwise the two-pass one (also
   // faster with documents under a causal mask, where units are longer)
   const bool one = plan.n_docs > 0 && !plan.causal;
+  const bool poll = plan.mma_poll != 0;
   switch (D) {
-    case 128: return one ? launch_d<128, true>(plan, stream) : launch_d<128, false>(plan, stream);
-    case 96: return one ? launch_d<96, true>(plan, stream) : launch_d<96, false>(plan, stream);
-    default: return one ? launch_d<64, true>(plan, stream) : launch_d<64, false>(plan, stream);
+    case 128:
+      return one ? launch_d<128, true, false>(plan, stream)
+                 : (poll ? launch_d<128, false, true>(plan, stream) : launch_d<128, false, false>(plan, stream));
+    case 96:
+      return one ? launch_d<96, true, false>(plan, stream)
+                 : (poll ? launch_d<96, false, true>(plan, stream) : launch_d<96, false, false>(plan, stream));
+    default:
+      return one ? launch_d<64, true, false>(plan, stream)
+                 : (poll ? launch_d<64, false, true>(plan, stream) : launch_d<64, false, false>(plan, stream));
   }
 }
 
