@@ -398,7 +398,7 @@ __device__ __noinline__ float4 rescale_p(uint32_t tS, int n, float alpha) {
   return make_float4(racc[0], racc[1], racc[2], racc[3]);
 }
 
-template <int D, bool kOnePass, bool kPoll>
+template <int D, bool kOnePass, bool kPoll, bool kFull>
 __global__ void __launch_bounds__(kThreads, 1) tc_ring_kernel(const __grid_constant__ TcPlan p) {
   using C = Cfg<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -555,7 +555,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ring_kernel(const __grid_const
     // host leaves polling off for launches of very long units too. The choice
     // is a template parameter: as a runtime branch between the two inlined
     // waits it cost 7% at 8K in the generated code alone.
-    static_assert(!(kOnePass && kPoll), "the one-pass form does not poll");
+    static_assert(!(kOnePass && (kPoll || kFull)), "the one-pass form neither polls nor skips the walk");
     auto mwait = [&](uint32_t bar, uint32_t parity, int site) {
       if constexpr (kPoll) return warp_wait_spin(bar, parity, abort_flag, budget, site);
       else return warp_wait(bar, parity, abort_flag, budget, site);
@@ -716,10 +716,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_ring_kernel(const __grid_const
       int rlo = 0, rhi = 0x7ffffffe;
       if (rvalid && (p.causal || p.n_docs > 0)) key_window(p, row_position(p, grow), rlo, rhi);
       float m_ref = kNegInf, mx = kNegInf, l = 0.f, lr = 0.f;
-      // Launches whose key tiles are all whole and visible to every row skip
-      // the walk over the key spans (its dependent plan reads sat between a
-      // step's P and the next S: 8K +2.3%).
-      const bool walk = !p.full_tiles;
+      // Launches whose key tiles are all whole and visible to every row
+      // (kFull, chosen by the host from full_tiles) skip the walk over the
+      // key spans: its dependent plan reads sat between a step's P and the
+      // next S (8K +2.3%; as a runtime flag only +1%).
+      constexpr bool walk = !kFull;
       if (n > 0) {
         TileIter iter;
         if (walk) iter.seek(p, U, I.t0);
@@ -1161,9 +1162,9 @@ void tc_scratch_carve(void* base, int grid, int D, TcScratch* s) {
   s->flags = reinterpret_cast<unsigned*>(b);
 }
 
-template <int D, bool kOnePass, bool kPoll>
+template <int D, bool kOnePass, bool kPoll, bool kFull>
 static int launch_d(const TcPlan& plan, void* stream) {
-  cudaError_t e = cudaFuncSetAttribute(tc_ring_kernel<D, kOnePass, kPoll>,
+  cudaError_t e = cudaFuncSetAttribute(tc_ring_kernel<D, kOnePass, kPoll, kFull>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::kSmemBytes);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -1177,9 +1178,21 @@ static int launch_d(const TcPlan& plan, void* stream) {
   attr[0].val.cooperative = plan.scratch.flags != nullptr ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, tc_ring_kernel<D, kOnePass, kPoll>, plan);
+  e = cudaLaunchKernelEx(&cfg, tc_ring_kernel<D, kOnePass, kPoll, kFull>, plan);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
+}
+
+// The kernel instance for a plan: the softmax form, the MMA warp's wait mode
+// and whether the softmax warps walk the key spans (all compile-time choices:
+// as runtime branches they cost several percent in the generated code).
+template <int D>
+static int launch_for(const TcPlan& plan, bool one, void* stream) {
+  if (one) return launch_d<D, true, false, false>(plan, stream);
+  const bool poll = plan.mma_poll != 0, full = plan.full_tiles != 0;
+  if (full)
+    return poll ? launch_d<D, false, true, true>(plan, stream) : launch_d<D, false, false, true>(plan, stream);
+  return poll ? launch_d<D, false, true, false>(plan, stream) : launch_d<D, false, false, false>(plan, stream);
 }
 
 int launch_tc_bf16(const TcPlan& plan, int D, void* stream) {
@@ -1188,17 +1201,10 @@ int launch_tc_bf16(const TcPlan& plan, int D, void* stream) {
   // masked units; measured faster there); otherwise the two-pass one (also
   // faster with documents under a causal mask, where units are longer)
   const bool one = plan.n_docs > 0 && !plan.causal;
-  const bool poll = plan.mma_poll != 0;
   switch (D) {
-    case 128:
-      return one ? launch_d<128, true, false>(plan, stream)
-                 : (poll ? launch_d<128, false, true>(plan, stream) : launch_d<128, false, false>(plan, stream));
-    case 96:
-      return one ? launch_d<96, true, false>(plan, stream)
-                 : (poll ? launch_d<96, false, true>(plan, stream) : launch_d<96, false, false>(plan, stream));
-    default:
-      return one ? launch_d<64, true, false>(plan, stream)
-                 : (poll ? launch_d<64, false, true>(plan, stream) : launch_d<64, false, false>(plan, stream));
+    case 128: return launch_for<128>(plan, one, stream);
+    case 96: return launch_for<96>(plan, one, stream);
+    default: return launch_for<64>(plan, one, stream);
   }
 }
 
