@@ -560,16 +560,20 @@ ra_status run_tc(const Common& c, const ra_problem& p, const void* q,
   // key/value stream (batch, key/value head) into every round, so the units
   // sharing a stream's keys are few and far apart in time; with the long
   // causal launches most of the key/value stream then came from DRAM (128K
-  // with 8 key/value heads: 171 GB per launch; 32K: 9.3 GB). Blocks of
-  // G / (Hq / Hkv) pair ranks with the stream outermost make each round one
-  // stream: 11 GB and 1.1 GB, +4-5% at 32K and 128K, +10% at 1M (whose clock
-  // the power cap sets: less DRAM traffic, a higher clock). Inside a round
-  // the CTAs take the pair ranks in order, so alternate rounds run in
-  // reverse CTA order; otherwise CTA 0 takes the costliest unit of every
-  // round and the CTAs drift apart.
+  // with 8 key/value heads: 171 GB per launch). Blocks of G / (Hq / Hkv)
+  // pair ranks with the stream outermost make each round one stream's run of
+  // consecutive pair ranks: 128K 7-11 GB and +4-5% on all three layouts, 1M
+  // +10% (whose clock the power cap sets: less DRAM traffic, a higher
+  // clock). A stream with fewer pair ranks than that would put several
+  // streams' whole cost ranges into one round, which no CTA order balances
+  // (16K causal with 16 heads: -13%), so such launches stay pair-major.
+  // Inside a round the CTAs take the pair ranks in order, so alternate
+  // rounds run in reverse CTA order; otherwise CTA 0 takes the costliest unit
+  // of every round and the CTAs drift apart (32K causal: DRAM reads 21 GB
+  // per launch with plain round-robin, 8.6 GB with the reversal).
   plan.dp_snake = R > 1 ? 1 : 0;
-  if (R > 1)
-    pair_block = int(std::max<int64_t>(1, std::min<int64_t>(npairs, G / (c.Hq / c.Hkv))));
+  const int64_t block = G / (c.Hq / c.Hkv);
+  if (R > 1 && block >= 1 && npairs >= block) pair_block = int(block);
   plan.pair_block = pair_block;
   // The MMA warp polls its barriers unless the units are very long (more
   // than 1024 key tiles on average). Measured under the power cap: polling
